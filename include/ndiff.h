@@ -1,0 +1,269 @@
+/*
+ * ndiff.h — C ABI of libndiff: the decode step over a 32-token block of a
+ * tri-mode (autoregressive / block-wise diffusion / self-speculation) language
+ * model, for one NVIDIA B300 (sm_103a).
+ *
+ * Sources of the operations (page title, then section):
+ *   [TRI]  "Nemotron-Labs-Diffusion: A Tri-Mode Language Model Unifying
+ *          Autoregressive, Diffusion, and Self-Speculation Decoding"
+ *          (hotpaper.ai): Abstract; "기술적 접근법 / 모듈" (technical approach /
+ *          modules: block-wise attention).
+ *   [FFI]  "NVIDIA 发布 Nemotron-Labs Diffusion 语言模型系列，自推测模式下吞吐量达
+ *          自回归的 6 倍" (fintech-frontier-insights): "三种生成模式" (three
+ *          generation modes: 32-token block, iterative denoising, temperature-0
+ *          self-speculation equals AR); "训练路线" (training route: block-wise
+ *          attention of Efficient-DLM, KV-cache compatibility).
+ *   [AIF]  "Nemotron-Labs-Diffusion: 一种统一自回归、扩散和自推测解码的三模式语言
+ *          模型" (ai-feeds.com digest): "问题" (AR is causal, diffusion is
+ *          bidirectional); "方法 / 推理: 三种模式按需切换" (three inference modes,
+ *          one model).
+ *   [GSY]  gsyq.cn explainer, §2.3 "自推测解码" (verification rejects the first
+ *          mismatching token and everything after it; the target model supplies
+ *          the correct token).
+ *   [HFB]  "NVIDIA 发布 Nemotron-Labs Diffusion：三模态语言模型统一 AR 与扩散解码"
+ *          (aimodeling.com digest of the Hugging Face blog): decode is memory-I/O
+ *          bound; fewer refinement steps trade quality for latency.
+ *
+ * Conventions (all entry points):
+ *   - Every call returns an ndiff_status. Argument errors are detected on the
+ *     host before anything is enqueued; nothing is launched in that case.
+ *   - ndiff_last_error() returns a thread-local, human-readable message for the
+ *     last non-OK status returned on the calling thread.
+ *   - Device pointers are raw CUDA device addresses owned by the caller; the
+ *     library never frees them and never allocates on the kernel entry points.
+ *     Work is enqueued asynchronously on the caller's stream (0 = legacy stream).
+ *   - Errors found by a kernel (a bounded wait that expired) are recorded in a
+ *     device status word and reported by ndiff_check() (which synchronises the
+ *     stream) as NDIFF_ERR_TIMEOUT.
+ *   - The model handle (ndiff_model_*) is the one exception to caller
+ *     ownership: it owns its weights, KV cache and scratch.
+ */
+#ifndef NDIFF_H
+#define NDIFF_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NDIFF_OK = 0,
+    NDIFF_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, misaligned */
+    NDIFF_ERR_UNSUPPORTED = 2, /* shape/dtype outside the compiled set */
+    NDIFF_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    NDIFF_ERR_OOM = 4,         /* device allocation failed (model handle only) */
+    NDIFF_ERR_WORKSPACE = 5,   /* caller workspace smaller than *_workspace_size */
+    NDIFF_ERR_TIMEOUT = 6      /* a bounded device-side wait expired */
+} ndiff_status;
+
+typedef enum { NDIFF_BF16 = 0, NDIFF_F32 = 1 } ndiff_dtype;
+
+/* Which block keys a block query sees ([TRI] modules; [AIF] "问题"):
+ * BIDIR  = every key of the block (diffusion drafting),
+ * CAUSAL = block keys up to and including its own slot (AR / verification).
+ * Both see the whole committed prefix. */
+typedef enum { NDIFF_BIDIR = 0, NDIFF_CAUSAL = 1 } ndiff_mask;
+
+/* The three decode modes of one checkpoint ([FFI] "三种生成模式"). */
+typedef enum { NDIFF_MODE_AR = 0, NDIFF_MODE_DIFF = 1, NDIFF_MODE_SELFSPEC = 2 } ndiff_mode;
+
+const char* ndiff_last_error(void);
+const char* ndiff_status_string(ndiff_status s);
+
+/* Reads back and clears the device status word after synchronising `stream`.
+ * Returns NDIFF_ERR_TIMEOUT if any kernel recorded an expired wait since the
+ * last check, NDIFF_ERR_CUDA on a CUDA error, else NDIFF_OK. */
+ndiff_status ndiff_check(cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Block-causal GQA attention over a KV cache ([TRI] modules "Block-wise
+ * attention"; [FFI] "三种生成模式": 32-token block; [FFI] "训练路线").
+ *
+ * For batch b with committed prefix P = kv_len[b], block slot i in [0,T) and
+ * query head h (kv head g = h / (Hq/Hkv)):
+ *     out[b][i][h] = softmax_j( scale * q[b][i][h] . k[b][g][j] ) . v[b][g][j]
+ * over the visible keys j: every j < P, plus the block keys j = P + t with
+ * t in [0,T) (BIDIR) or t <= i (CAUSAL). The block's own keys and values must
+ * already sit in the cache at positions [P, P+T).
+ *
+ * Layouts (row-major, contiguous):
+ *   q, out            [B][T][Hq][D]
+ *   k_cache, v_cache  [B][Hkv][Lmax][D]
+ *   kv_len            [B] int32 on the device, 0 <= kv_len[b] <= Lmax - T
+ * dt = NDIFF_BF16: bf16 q/k/v/out, fp32 accumulation and softmax; requires
+ *   D = 128, (Hq/Hkv) * T <= 128, Hq % Hkv == 0; all pointers 16-byte aligned.
+ * dt = NDIFF_F32: fp32 everywhere; requires D <= 64.
+ * ws/ws_bytes: device scratch of at least ndiff_block_attn_workspace_size()
+ *   bytes (may be NULL when that size is 0). Contents need no initialisation.
+ * Values stored in the cache at positions >= kv_len[b] + T are never used
+ * (they may hold anything, including NaN). kv_len values outside the range
+ * above are clamped on the device.
+ * ------------------------------------------------------------------------ */
+ndiff_status ndiff_block_attn(ndiff_dtype dt, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* kv_len, int B, int T,
+                              int Hq, int Hkv, int D, int Lmax, ndiff_mask mode, float scale,
+                              void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Scratch bytes ndiff_block_attn needs for this shape (0 = none). */
+size_t ndiff_block_attn_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv, int D,
+                                       int Lmax);
+
+/* Same as ndiff_block_attn with an explicit KV split length (keys per CTA,
+ * a positive multiple of 64; 0 = automatic). The split boundaries sit at
+ * absolute key positions, so results for a block row do not depend on T. */
+ndiff_status ndiff_block_attn_split(ndiff_dtype dt, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* kv_len, int B, int T,
+                                    int Hq, int Hkv, int D, int Lmax, ndiff_mask mode,
+                                    float scale, int split_keys, void* out, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream);
+size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv,
+                                             int D, int Lmax, int split_keys);
+
+/* ------------------------------------------------------------------------ *
+ * Logits reduction: per row r of logits [R][V] (row stride ld elements),
+ *   argmax[r] = smallest v in [0,V), v != exclude_id, with the largest logit;
+ *               -1 if every id is excluded (V == 1 and exclude_id == 0);
+ *   conf[r]   = softmax(row)[argmax[r]] over ALL V ids (the excluded id is in
+ *               the normaliser); this is the row's maximum probability unless
+ *               the excluded id holds the maximum. 0 when argmax is -1.
+ * Greedy (temperature-0) selection is the decision rule of AR decoding and of
+ * verification ([FFI] "三种生成模式"); the confidence drives unmasking.
+ * dt: NDIFF_BF16 or NDIFF_F32 logits. Logits must be finite.
+ * argmax: int32 [R]; conf: float [R] (device). ld >= V; for bf16, ld and the
+ * logits pointer must make every row 16-byte aligned (ld % 8 == 0), for f32
+ * ld % 4 == 0. R == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+ndiff_status ndiff_logits_reduce(ndiff_dtype dt, const void* logits, int R, int V, int64_t ld,
+                                 int exclude_id, int32_t* argmax, float* conf,
+                                 cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Diffusion unmask step (one denoising round of a block; [FFI]
+ * "三种生成模式": iterative denoising of a 32-token block; [HFB]: the number
+ * of rounds is the step budget).
+ * For each sequence b, among the slots i < T whose bit i of mask_bits[b] is
+ * set, select the k' = min(k, popcount) slots of highest conf[b][i] (ties go to
+ * the lower slot). For each selected slot i:
+ *     draft[b][i] = pred[b][i];  clear bit i of mask_bits[b];
+ *     if i <= T-2: block_in[b][i+1] = pred[b][i]   (slot i predicts the token
+ *                                                   that input slot i+1 holds)
+ * chosen[b][r] = the slot of rank r (r < k'), -1 for r in [k', k).
+ * Shapes: conf float [B][T], pred int32 [B][T], mask_bits uint32 [B] (in/out),
+ * block_in int32 [B][T] (in/out), draft int32 [B][T] (in/out), chosen int32
+ * [B][k]. 1 <= T <= 32, 1 <= k <= T. B == 0 is a no-op. conf must not be NaN.
+ * ------------------------------------------------------------------------ */
+ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int B, int T, int k,
+                          uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
+                          int32_t* chosen, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Self-speculation verify / accept ([GSY] §2.3; [FFI] "三种生成模式":
+ * diffusion drafts, AR verifies, temperature-0 output equals AR output).
+ * For each sequence b:
+ *   accept_len[b] = L = first i in [0,T) with draft[b][i] != target[b][i], or T;
+ *   n_commit[b]   = n = min(L+1, T)  (the accepted drafts plus the target's
+ *                                     correction token when L < T);
+ *   commit[b][j]  = target[b][j] for j < n, -1 otherwise;
+ *   kv_len[b]    += n   (skipped when kv_len is NULL).
+ * Shapes: draft, target, commit int32 [B][T]; accept_len, n_commit, kv_len
+ * int32 [B]. 1 <= T <= 32. B == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
+                                 int32_t* accept_len, int32_t* commit, int32_t* n_commit,
+                                 int32_t* kv_len, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Random-init tri-mode model (one checkpoint, three modes: [FFI]
+ * "三种生成模式"; [AIF] "方法 / 推理").
+ * Pre-norm transformer: x = E[ids]; per layer
+ *   h = RMSNorm(x); q,k,v = h Wq^T, h Wk^T, h Wv^T; RoPE(q,k);
+ *   x += BlockAttn(q,k,v) Wo^T; h = RMSNorm(x); x += (silu(h Wg^T) * h Wu^T) Wd^T;
+ * logits = RMSNorm(x) Wlm^T. RMSNorm gain 1, eps cfg.eps, RoPE rotate-half with
+ * base cfg.rope_base. Every weight ~ N(0, 0.02^2) drawn with Philox4x64-10
+ * (Salmon et al., SC'11) and Box-Muller from `seed` (see DESIGN notes in the
+ * repository for the exact counter layout). The [MASK] id is vocab-1 and is
+ * never predicted.
+ * dtype NDIFF_F32: fp32 weights/activations (tiny configs: d_model <= 1024,
+ *   head_dim <= 64, vocab <= 65536).
+ * dtype NDIFF_BF16: bf16 weights, bf16 GEMM inputs, fp32 residual stream and
+ *   accumulators; requires head_dim == 128, d_model % 128 == 0, ffn % 128 == 0,
+ *   n_heads/n_kv_heads * 32 <= 128.
+ * Batch 1 only (batch must be 1).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int layers;
+    int d_model;
+    int n_heads;
+    int n_kv_heads;
+    int head_dim;
+    int ffn;
+    int vocab;
+    ndiff_dtype dtype;
+    float rope_base;
+    float eps;
+    int max_seq; /* KV cache capacity in tokens (prompt + generated + 32) */
+    int batch;   /* must be 1 */
+} ndiff_model_config;
+
+typedef struct ndiff_model ndiff_model;
+
+typedef struct {
+    int64_t forwards;        /* model forwards run by the calls so far (prefill excluded) */
+    int64_t tokens;          /* tokens committed by the calls so far */
+    int32_t last_accept_len; /* L of the last SELFSPEC verification (-1 otherwise) */
+    int32_t last_n_commit;   /* tokens committed by the last decode step */
+    int64_t accept_hist[33]; /* histogram of L over SELFSPEC verifications */
+} ndiff_stats;
+
+ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out);
+ndiff_status ndiff_model_destroy(ndiff_model* m);
+
+/* Causal forward over prompt[0..n-2] (host ids) that fills the KV cache;
+ * prompt[n-1] becomes the pending "last" token. Resets the session.
+ * 1 <= n, n + 32 <= max_seq. Synchronous on return. */
+ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n,
+                           cudaStream_t stream);
+
+/* One decode cycle in `mode` (shifted convention: the logits of input slot i
+ * predict the token after it):
+ *   AR:       one forward of [last] (CAUSAL); commits 1 token.
+ *   DIFF:     `steps` forwards of the 32-slot block [last, MASK x 31]
+ *             (BIDIR), each unmasking k = 32/steps slots, then one BIDIR
+ *             forward of the finished block that writes its KV; commits 32
+ *             tokens.
+ *   SELFSPEC: the DIFF draft (steps forwards) then one CAUSAL forward of
+ *             [last, d0..d30]; commits the accepted prefix plus the correction.
+ * steps: drafting forwards per block (1 <= steps <= 32, 32 % steps == 0);
+ *   ignored for AR.
+ * out_tokens_host: host buffer of >= 32 int32; *n_out receives the count.
+ * stats (optional) accumulates counters. Synchronous on return. */
+ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,
+                               int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
+                               cudaStream_t stream);
+
+/* Runs one forward of `T` block tokens (host ids) at the model's current
+ * position with the given mask, writes fp32 logits [T][vocab] to the host
+ * buffer (may be NULL) and returns them without changing the session (the
+ * block's KV entries beyond the committed prefix are scratch). For parity
+ * tests and diagnostics. Synchronous. */
+ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T,
+                                 ndiff_mask mode, float* logits_host, cudaStream_t stream);
+
+/* Session state readout: committed prefix length (KV entries) and the pending
+ * last token. */
+ndiff_status ndiff_model_state(const ndiff_model* m, int* kv_len, int32_t* last_token);
+
+/* Copies `count` elements of weight tensor `tensor_id` starting at flat
+ * element `offset` (the Philox element index of that tensor) to the host as
+ * fp32. For tests of the weight generator. Synchronous. */
+ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_t offset,
+                                     int64_t count, float* host_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NDIFF_H */

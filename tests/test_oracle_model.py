@@ -1,0 +1,118 @@
+"""Pins of the oracle model: component closed forms (RMSNorm, RoPE, SiLU), the
+row independence that makes temperature-0 self-speculation equal AR, exact
+self-spec == AR on the tiny configuration, forced acceptance, and the stored
+tiny-configuration tokens (written by tests/golden/make_golden.py from the
+oracle alone)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention, model
+from self_speculative_lm_block_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tiny_tokens.json")
+
+
+def tiny_cfg():
+    t = synth.TINY
+    return model.Config(layers=t["layers"], d_model=t["d_model"], n_heads=t["n_heads"],
+                        n_kv_heads=t["n_kv_heads"], head_dim=t["head_dim"], ffn=t["ffn"],
+                        vocab=t["vocab"], dtype="f32", seed=t["seed"])
+
+
+def test_rmsnorm_closed_form_and_library():
+    x = np.full((1, 16), -3.0)
+    np.testing.assert_allclose(model.rmsnorm(x, 1e-6), -3 / np.sqrt(9 + 1e-6), rtol=1e-15)
+    y = np.random.default_rng(0).standard_normal((4, 64))
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(y), (64,), eps=1e-6).numpy()
+    np.testing.assert_allclose(model.rmsnorm(y, 1e-6), ref, rtol=1e-13)
+
+
+def test_rope_properties():
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((1, 3, 32))
+    k = rng.standard_normal((1, 3, 32))
+    # position 0 is the identity; rotations keep norms
+    assert np.allclose(model.rope(q, [0], 10000.0), q, rtol=0, atol=0)
+    r = model.rope(q, [77], 10000.0)
+    np.testing.assert_allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(q, axis=-1), rtol=1e-13)
+    # scores depend only on the relative position m - n
+    def score(m, n):
+        return np.sum(model.rope(q, [m], 10000.0) * model.rope(k, [n], 10000.0), axis=-1)
+    np.testing.assert_allclose(score(10, 3), score(107, 100), rtol=1e-10)
+    # rotate-half pairing: a vector with only component i rotates into i + D/2
+    e = np.zeros((1, 1, 32)); e[0, 0, 2] = 1.0
+    th = 5 * 10000.0 ** (-4 / 32)
+    out = model.rope(e, [5], 10000.0)[0, 0]
+    assert abs(out[2] - np.cos(th)) < 1e-15 and abs(out[18] - np.sin(th)) < 1e-15
+    assert np.count_nonzero(np.abs(out) > 1e-15) == 2
+
+
+def test_silu_library():
+    x = np.linspace(-8, 8, 101)
+    np.testing.assert_allclose(model.silu(x), torch.nn.functional.silu(torch.from_numpy(x)).numpy(),
+                               rtol=1e-14, atol=1e-16)
+
+
+def test_forward_rows_do_not_depend_on_block_length():
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    ids = synth.prompt(20, cfg.vocab, 5)
+    s = model.Session(cfg, w, max_seq=64)
+    s.prefill(ids[:9])                    # cache holds ids[0..7], last = ids[8]
+    blk = s.forward(list(ids[8:20]), attention.CAUSAL)
+    for i in range(12):
+        s1 = model.Session(cfg, w, max_seq=64)
+        s1.prefill(ids[:9 + i])           # cache holds ids[0..7+i], last = ids[8+i]
+        one = s1.forward([int(ids[8 + i])], attention.CAUSAL)
+        assert np.array_equal(one[0], blk[i])
+
+
+@pytest.mark.parametrize("steps", [1, 2, 4])
+def test_selfspec_equals_ar_exactly(steps):
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, w, max_seq=200); s.prefill(pr)
+    ar = s.generate("ar", 64)
+    s2 = model.Session(cfg, w, max_seq=200); s2.prefill(pr)
+    assert s2.generate("selfspec", 64, steps) == ar
+
+
+def test_forced_accept_gives_full_block():
+    """Drafting the AR continuation itself is accepted whole (L = 32)."""
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, w, max_seq=200); s.prefill(pr)
+    ar = s.generate("ar", 40)
+    s2 = model.Session(cfg, w, max_seq=200); s2.prefill(pr)
+    logits = s2.forward([s2.last] + ar[:31], attention.CAUSAL)
+    a = model.decode.logits_reduce(logits, exclude_id=cfg.mask_id)[0]
+    assert list(a) == ar[:32]
+
+
+def test_diff_mode_fills_every_slot_and_counts_forwards():
+    cfg = tiny_cfg()
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    for steps in (1, 4, 32):
+        s = model.Session(cfg, max_seq=200); s.prefill(pr)
+        toks = s.generate("diff", 64, steps)
+        assert len(toks) == 64 and all(0 <= t < cfg.vocab - 1 for t in toks)
+        assert s.forwards == 2 * (steps + 1)
+        assert s.kv_len == 31 + 64
+
+
+def test_golden_tiny_tokens():
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    assert g["prompt"] == [int(t) for t in pr]
+    for key, (mode, steps) in {"ar": ("ar", 1), "diff_k4": ("diff", 8), "selfspec_s1": ("selfspec", 1)}.items():
+        s = model.Session(cfg, w, max_seq=200); s.prefill(pr)
+        assert s.generate(mode, 64, steps) == g[key], key
