@@ -45,6 +45,12 @@
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
+#if defined(__GNUC__)
+#define NDIFF_API __attribute__((visibility("default")))
+#else
+#define NDIFF_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -70,13 +76,13 @@ typedef enum { NDIFF_BIDIR = 0, NDIFF_CAUSAL = 1 } ndiff_mask;
 /* The three decode modes of one checkpoint ([FFI] "三种生成模式"). */
 typedef enum { NDIFF_MODE_AR = 0, NDIFF_MODE_DIFF = 1, NDIFF_MODE_SELFSPEC = 2 } ndiff_mode;
 
-const char* ndiff_last_error(void);
-const char* ndiff_status_string(ndiff_status s);
+NDIFF_API const char* ndiff_last_error(void);
+NDIFF_API const char* ndiff_status_string(ndiff_status s);
 
 /* Reads back and clears the device status word after synchronising `stream`.
  * Returns NDIFF_ERR_TIMEOUT if any kernel recorded an expired wait since the
  * last check, NDIFF_ERR_CUDA on a CUDA error, else NDIFF_OK. */
-ndiff_status ndiff_check(cudaStream_t stream);
+NDIFF_API ndiff_status ndiff_check(cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Block-causal GQA attention over a KV cache ([TRI] modules "Block-wise
@@ -102,24 +108,24 @@ ndiff_status ndiff_check(cudaStream_t stream);
  * (they may hold anything, including NaN). kv_len values outside the range
  * above are clamped on the device.
  * ------------------------------------------------------------------------ */
-ndiff_status ndiff_block_attn(ndiff_dtype dt, const void* q, const void* k_cache,
+NDIFF_API ndiff_status ndiff_block_attn(ndiff_dtype dt, const void* q, const void* k_cache,
                               const void* v_cache, const int32_t* kv_len, int B, int T,
                               int Hq, int Hkv, int D, int Lmax, ndiff_mask mode, float scale,
                               void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Scratch bytes ndiff_block_attn needs for this shape (0 = none). */
-size_t ndiff_block_attn_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv, int D,
+NDIFF_API size_t ndiff_block_attn_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv, int D,
                                        int Lmax);
 
 /* Same as ndiff_block_attn with an explicit KV split length (keys per CTA,
  * a positive multiple of 64; 0 = automatic). The split boundaries sit at
  * absolute key positions, so results for a block row do not depend on T. */
-ndiff_status ndiff_block_attn_split(ndiff_dtype dt, const void* q, const void* k_cache,
+NDIFF_API ndiff_status ndiff_block_attn_split(ndiff_dtype dt, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* kv_len, int B, int T,
                                     int Hq, int Hkv, int D, int Lmax, ndiff_mask mode,
                                     float scale, int split_keys, void* out, void* ws,
                                     size_t ws_bytes, cudaStream_t stream);
-size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv,
+NDIFF_API size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv,
                                              int D, int Lmax, int split_keys);
 
 /* ------------------------------------------------------------------------ *
@@ -136,7 +142,7 @@ size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int H
  * logits pointer must make every row 16-byte aligned (ld % 8 == 0), for f32
  * ld % 4 == 0. R == 0 is a no-op.
  * ------------------------------------------------------------------------ */
-ndiff_status ndiff_logits_reduce(ndiff_dtype dt, const void* logits, int R, int V, int64_t ld,
+NDIFF_API ndiff_status ndiff_logits_reduce(ndiff_dtype dt, const void* logits, int R, int V, int64_t ld,
                                  int exclude_id, int32_t* argmax, float* conf,
                                  cudaStream_t stream);
 
@@ -155,7 +161,7 @@ ndiff_status ndiff_logits_reduce(ndiff_dtype dt, const void* logits, int R, int 
  * block_in int32 [B][T] (in/out), draft int32 [B][T] (in/out), chosen int32
  * [B][k]. 1 <= T <= 32, 1 <= k <= T. B == 0 is a no-op. conf must not be NaN.
  * ------------------------------------------------------------------------ */
-ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int B, int T, int k,
+NDIFF_API ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int B, int T, int k,
                           uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                           int32_t* chosen, cudaStream_t stream);
 
@@ -171,7 +177,7 @@ ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int B, int T, 
  * Shapes: draft, target, commit int32 [B][T]; accept_len, n_commit, kv_len
  * int32 [B]. 1 <= T <= 32. B == 0 is a no-op.
  * ------------------------------------------------------------------------ */
-ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
+NDIFF_API ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                  int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                  int32_t* kv_len, cudaStream_t stream);
 
@@ -218,13 +224,13 @@ typedef struct {
     int64_t accept_hist[33]; /* histogram of L over SELFSPEC verifications */
 } ndiff_stats;
 
-ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out);
-ndiff_status ndiff_model_destroy(ndiff_model* m);
+NDIFF_API ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out);
+NDIFF_API ndiff_status ndiff_model_destroy(ndiff_model* m);
 
 /* Causal forward over prompt[0..n-2] (host ids) that fills the KV cache;
  * prompt[n-1] becomes the pending "last" token. Resets the session.
  * 1 <= n, n + 32 <= max_seq. Synchronous on return. */
-ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n,
+NDIFF_API ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n,
                            cudaStream_t stream);
 
 /* One decode cycle in `mode` (shifted convention: the logits of input slot i
@@ -240,7 +246,7 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n,
  *   ignored for AR.
  * out_tokens_host: host buffer of >= 32 int32; *n_out receives the count.
  * stats (optional) accumulates counters. Synchronous on return. */
-ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,
+NDIFF_API ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,
                                int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
                                cudaStream_t stream);
 
@@ -249,17 +255,17 @@ ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,
  * buffer (may be NULL) and returns them without changing the session (the
  * block's KV entries beyond the committed prefix are scratch). For parity
  * tests and diagnostics. Synchronous. */
-ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T,
+NDIFF_API ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T,
                                  ndiff_mask mode, float* logits_host, cudaStream_t stream);
 
 /* Session state readout: committed prefix length (KV entries) and the pending
  * last token. */
-ndiff_status ndiff_model_state(const ndiff_model* m, int* kv_len, int32_t* last_token);
+NDIFF_API ndiff_status ndiff_model_state(const ndiff_model* m, int* kv_len, int32_t* last_token);
 
 /* Copies `count` elements of weight tensor `tensor_id` starting at flat
  * element `offset` (the Philox element index of that tensor) to the host as
  * fp32. For tests of the weight generator. Synchronous. */
-ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_t offset,
+NDIFF_API ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_t offset,
                                      int64_t count, float* host_out);
 
 #ifdef __cplusplus

@@ -1,0 +1,503 @@
+// attn_bf16.cu — block-causal GQA attention over a bf16 KV cache on sm_103a.
+//
+// Operation ("Nemotron-Labs-Diffusion: A Tri-Mode Language Model ..." (hotpaper.ai),
+// technical approach / modules: block-wise attention; "NVIDIA 发布 Nemotron-Labs
+// Diffusion 语言模型系列" (fintech-frontier-insights), "三种生成模式": 32-token
+// blocks; "训练路线": block-wise attention that keeps the KV cache usable):
+//   out[b][i][h] = softmax_j(scale * q[b][i][h].k[b][g][j]) . v[b][g][j]
+// over the committed prefix j < P_b plus the block keys P_b + t, t < T (BIDIR)
+// or t <= i (CAUSAL).
+//
+// Design (one CTA per (batch b, kv head g, KV split s)):
+//   * The G = Hq/Hkv query heads of kv head g and the T block slots form one
+//     128-row tile (row r = t*G + hh), so each K/V tile streamed from HBM feeds
+//     all G heads: S = Q K^T and O += P V are 128 x 64 x 128 and 128 x 128 x 64
+//     tcgen05 MMAs with fp32 accumulators in TMEM (O: 128 columns, S: two
+//     64-column buffers).
+//   * Warp 0 streams Q once and K/V tiles of 64 keys through a 4-stage TMA
+//     ring (128-byte swizzle); warp 1 issues the MMAs; warps 2-5 (one TMEM lane
+//     quarter each, one thread per row) run the online softmax in the log2
+//     domain, write P as bf16 into shared memory and rescale O in TMEM only
+//     when the running maximum grows by more than 2^8 (the final normalisation
+//     uses the same stale maximum, so the result is unchanged).
+//   * KV splits sit at absolute key positions (multiples of the split length),
+//     and masked keys contribute exact zeros, so a row's result does not
+//     depend on T: a CAUSAL block of T rows reproduces T single-row calls.
+//   * Splits of one (b, g) are merged by attn_combine (log-sum-exp weights).
+//   * Every mbarrier wait is bounded; on expiry the CTA records a timeout in
+//     the device status word, drains its TMA loads, frees TMEM and exits.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ndiff {
+namespace attn {
+
+constexpr int BN = 64;      // keys per tile
+constexpr int NST = 4;      // K/V pipeline stages
+constexpr int ROWS = 128;   // MMA M (G * T rows)
+constexpr int DH = 128;     // head dim
+constexpr int Q_BYTES = ROWS * DH * 2;   // 32 KB: two 64-column halves of 16 KB
+constexpr int KT_BYTES = BN * DH * 2;    // 16 KB: two halves of 8 KB
+constexpr int P_BYTES = ROWS * BN * 2;   // 16 KB
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + NST * KT_BYTES;
+constexpr int OFF_P = OFF_V + NST * KT_BYTES;
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int N_BARS = 1 + 3 * NST + 6;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers/flags + alignment slack
+constexpr int TMEM_COLS = 256;                     // O: [0,128), S0: [128,192), S1: [192,256)
+constexpr int THREADS = 192;
+constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+
+struct Params {
+  const int32_t* kv_len;
+  int B, T, Hq, Hkv, G, Lmax;
+  float scale_log2;   // scale * log2(e)
+  int causal;
+  int split;          // keys per split (multiple of BN)
+  int nsplit_max;     // splits per (b, g) in the grid
+  __nv_bfloat16* out;
+  float* ws_o;        // [B][Hkv][nsplit_max][128][128]
+  float2* ws_ml;      // [B][Hkv][nsplit_max][128]
+  unsigned int* status;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sa, float& sb) {
+  __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+  sa = __bfloat162float(ha);
+  sb = __bfloat162float(hb);
+  return (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the result
+// (tcgen05.ld/st that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+}
+
+// Waits that ignore the abort flag (used to drain TMA loads before exit).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t b = smem_u32(bar);
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(b, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  int P = p.kv_len[b];
+  P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+  const int nkeys = P + p.T;
+  const int k_begin = s_idx * p.split;
+  if (k_begin >= nkeys) return;  // this split is past the sequence (uniform per CTA)
+  const int k_end = min(k_begin + p.split, nkeys);
+  const int ntiles = (k_end - k_begin + BN - 1) / BN;
+  const int nsplit_b = (nkeys + p.split - 1) / p.split;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* kv_empty = v_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t* sQ = smem + OFF_Q;
+  uint8_t* sK = smem + OFF_K;
+  uint8_t* sV = smem + OFF_V;
+  uint8_t* sP = smem + OFF_P;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int rowsq = p.G * p.T;
+      mbar_arrive_expect_tx(q_full, 2u * rowsq * 128u);
+      tma_load_3d(sQ, &tmQ, q_full, 0, g * p.G, b * p.T);
+      tma_load_3d(sQ + 16384, &tmQ, q_full, 64, g * p.G, b * p.T);
+      const int row0 = (b * p.Hkv + g) * p.Lmax;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % NST, use = j / NST;
+        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, p.status, abort_flag)) break;
+        const int key = row0 + k_begin + j * BN;
+        uint8_t* dk = sK + st * KT_BYTES;
+        uint8_t* dv = sV + st * KT_BYTES;
+        mbar_arrive_expect_tx(&k_full[st], KT_BYTES);
+        tma_load_2d(dk, &tmK, &k_full[st], 0, key);
+        tma_load_2d(dk + 8192, &tmK, &k_full[st], 64, key);
+        mbar_arrive_expect_tx(&v_full[st], KT_BYTES);
+        tma_load_2d(dv, &tmV, &v_full[st], 0, key);
+        tma_load_2d(dv + 8192, &tmV, &v_full[st], 64, key);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let every issued copy land before the CTA's shared memory goes away.
+        mbar_drain(q_full, 0);
+        for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
+          mbar_drain(&k_full[j % NST], (j / NST) & 1);
+          mbar_drain(&v_full[j % NST], (j / NST) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(ROWS, BN, false, false);
+      const uint32_t idPV = idesc_bf16_f32(ROWS, DH, false, true);
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
+      bool ok = mbar_wait(q_full, 0, p.status, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % NST;
+        if (!mbar_wait(&k_full[st], (j / NST) & 1, p.status, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kb = ka + st * KT_BYTES;
+        const uint32_t dS = tmem + 128 + (j & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * 16384 + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 8192 + off, 16, 1024);
+          umma_f16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && ntiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int st = j % NST;
+        if (!mbar_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) break;
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t vb = va + st * KT_BYTES;
+        const uint32_t pb = pa + (j & 1) * P_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(pb + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 8192, 1024);
+          umma_f16(tmem, ad, bd, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&o_done[j & 1]);
+        umma_commit(&kv_empty[st]);
+        if (j + 2 < ntiles) ok = issue_s(j + 2);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const uint32_t quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const bool valid = r < p.G * p.T;
+    const int t = r / p.G;
+    const int vis_end = valid ? P + (p.causal ? t + 1 : p.T) : 0;
+    const uint32_t tl = tmem + ((quarter * 32u) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    const int tid128 = threadIdx.x - 64;
+    for (int j = 0; j < ntiles; ++j) {
+      const int key0 = k_begin + j * BN;
+      const int st = j % NST;
+      const int nv = min(BN, k_end - key0);
+      if (nv < BN) {
+        // Zero the V rows past the sequence so that P = 0 meets finite values.
+        if (!warp_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) { ok = false; break; }
+        uint8_t* vt = sV + st * KT_BYTES;
+        const int per_half = (BN - nv) * 8;
+        for (int c = tid128; c < 2 * per_half; c += 128) {
+          const int half = c / per_half, rem = c % per_half;
+          const int row = nv + rem / 8;
+          *reinterpret_cast<uint4*>(vt + half * 8192 + row * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      if (!warp_wait(&s_full[j & 1], (j >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float s[BN];
+      tmem_ld32(tl + 128 + (j & 1) * 64, s);
+      tmem_ld32(tl + 128 + (j & 1) * 64 + 32, s + 32);
+      tmem_wait_ld();
+      const int lim = vis_end - key0;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        s[i] = (i < lim) ? s[i] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[i]);
+      }
+      // Raise the running maximum only when it grew by more than 2^8; the
+      // decision is per row, the O rescale in TMEM is warp-collective.
+      float alpha = 1.f;
+      const bool grow = mt > m_run + RESCALE_THRESHOLD;
+      if (grow) alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mt);
+      const bool grow_o = grow && j > 0 && m_run != -INFINITY;
+      if (__any_sync(0xffffffffu, grow_o)) {
+        if (!warp_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float a_o = grow_o ? alpha : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          float o[32];
+          tmem_ld32(tl + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= a_o;
+          tmem_st32(tl + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      if (grow) {
+        l_run *= alpha;
+        m_run = mt;
+      }
+      if (j >= 2) {
+        // P buffer (j & 1) is free once PV(j-2) has completed.
+        if (!warp_wait(&o_done[j & 1], ((j - 2) >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      }
+      uint8_t* prow = sP + (j & 1) * P_BYTES + r * 128;
+      float sum = 0.f;
+      const bool none = (m_run == -INFINITY);
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = none ? 0.f : ex2(s[c * 8 + 2 * e] - m_run);
+          const float x1 = none ? 0.f : ex2(s[c * 8 + 2 * e + 1] - m_run);
+          float r0, r1;
+          w[e] = pack_bf16(x0, x1, r0, r1);
+          sum += r0 + r1;
+        }
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run += sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[j & 1]);
+    }
+    // ---------------------------------------------------------- epilogue
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const int last = ntiles - 1;
+      ok = warp_wait(&o_done[last & 1], (last >> 1) & 1, p.status, abort_flag);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int hh = valid ? r % p.G : 0;
+      const size_t unit = ((size_t)(b * p.Hkv + g) * p.nsplit_max + s_idx) * ROWS + r;
+      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < DH / 32; ++c) {
+        float o[32];
+        tmem_ld32(tl + c * 32, o);
+        tmem_wait_ld();
+        if (!valid) continue;
+        if (nsplit_b == 1) {
+          __nv_bfloat16* dst =
+              p.out + (((size_t)b * p.T + t) * p.Hq + g * p.G + hh) * DH + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            float d0, d1;
+            v.x = pack_bf16(o[i] * inv_l, o[i + 1] * inv_l, d0, d1);
+            v.y = pack_bf16(o[i + 2] * inv_l, o[i + 3] * inv_l, d0, d1);
+            v.z = pack_bf16(o[i + 4] * inv_l, o[i + 5] * inv_l, d0, d1);
+            v.w = pack_bf16(o[i + 6] * inv_l, o[i + 7] * inv_l, d0, d1);
+            *reinterpret_cast<uint4*>(dst + i) = v;
+          }
+        } else {
+          float* dst = p.ws_o + unit * DH + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+        }
+      }
+      if (valid && nsplit_b > 1) p.ws_ml[unit] = make_float2(m_run, l_run);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Merges the KV splits of each (b, g) row: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+__global__ void __launch_bounds__(128)
+    attn_combine_kernel(const Params p) {
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= p.G * p.T) return;
+  int P = p.kv_len[b];
+  P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+  const int nkeys = P + p.T;
+  const int ns = (nkeys + p.split - 1) / p.split;
+  if (ns <= 1) return;  // written directly by the main kernel
+  const size_t base = (size_t)(b * p.Hkv + g) * p.nsplit_max;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.ws_ml[(base + s) * ROWS + r].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float2 ml = p.ws_ml[(base + s) * ROWS + r];
+    const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+    L += w * ml.y;
+    const float4 o =
+        *reinterpret_cast<const float4*>(p.ws_o + ((base + s) * ROWS + r) * DH + lane * 4);
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = 1.f / L;
+  const int t = r / p.G, hh = r % p.G;
+  __nv_bfloat16* dst = p.out + (((size_t)b * p.T + t) * p.Hq + g * p.G + hh) * DH + lane * 4;
+  float d0, d1;
+  uint2 v;
+  v.x = pack_bf16(acc.x * inv, acc.y * inv, d0, d1);
+  v.y = pack_bf16(acc.z * inv, acc.w * inv, d0, d1);
+  *reinterpret_cast<uint2*>(dst) = v;
+}
+
+}  // namespace attn
+
+int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
+  const long long target = 8LL * num_sms();
+  long long want = ((long long)Lmax * B * Hkv + target - 1) / target;
+  want = ((want + attn::BN - 1) / attn::BN) * attn::BN;
+  const long long whole = ((long long)(Lmax + attn::BN - 1) / attn::BN) * attn::BN;
+  if (want < 256) want = 256;
+  if (want > whole) want = whole;
+  return (int)want;
+}
+
+size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
+  (void)T;
+  (void)Hq;
+  const int nsplit = (Lmax + split - 1) / split;
+  if (nsplit <= 1) return 0;
+  return (size_t)B * Hkv * nsplit * attn::ROWS * (attn::DH * sizeof(float) + sizeof(float2));
+}
+
+ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
+                              int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
+                              int split, void* out, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  const int G = Hq / Hkv;
+  const int nsplit = (Lmax + split - 1) / split;
+  const size_t need = attn_bf16_workspace(B, T, Hq, Hkv, Lmax, split);
+  if (need > 0 && (ws == nullptr || ws_bytes < need))
+    return set_error(NDIFF_ERR_WORKSPACE, "ndiff_block_attn: workspace of %zu bytes needed, %zu given",
+                     need, ws_bytes);
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)B * T};
+    const uint64_t strides[2] = {128 * 2, (uint64_t)Hq * 128 * 2};
+    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)T};
+    ndiff_status s = make_tmap_bf16(&tq, q, 3, dims, strides, box);
+    if (s != NDIFF_OK) return s;
+  }
+  {
+    const uint64_t dims[2] = {128, (uint64_t)B * Hkv * Lmax};
+    const uint64_t strides[1] = {128 * 2};
+    const uint32_t box[2] = {64, (uint32_t)attn::BN};
+    ndiff_status s = make_tmap_bf16(&tk, k, 2, dims, strides, box);
+    if (s != NDIFF_OK) return s;
+    s = make_tmap_bf16(&tv, v, 2, dims, strides, box);
+    if (s != NDIFF_OK) return s;
+  }
+  attn::Params prm;
+  prm.kv_len = kv_len;
+  prm.B = B;
+  prm.T = T;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = G;
+  prm.Lmax = Lmax;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.causal = causal;
+  prm.split = split;
+  prm.nsplit_max = nsplit;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.ws_o = static_cast<float*>(ws);
+  prm.ws_ml = need ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
+                                               (size_t)B * Hkv * nsplit * attn::ROWS *
+                                                   attn::DH * sizeof(float))
+                   : nullptr;
+  prm.status = device_status_word();
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  NDIFF_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 64 && !attr_set[dev]) {
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(attn::attn_bf16_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        attn::SMEM_BYTES));
+    attr_set[dev] = true;
+  }
+  dim3 grid(nsplit, Hkv, B);
+  attn::attn_bf16_kernel<<<grid, attn::THREADS, attn::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  if (nsplit > 1) {
+    dim3 g2((G * T + 3) / 4, Hkv, B);
+    attn::attn_combine_kernel<<<g2, 128, 0, stream>>>(prm);
+    NDIFF_CUDA_TRY(cudaGetLastError());
+  }
+  return NDIFF_OK;
+}
+
+}  // namespace ndiff

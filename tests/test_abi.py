@@ -1,0 +1,74 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports every
+entry point that include/ndiff.h declares, and rejects bad arguments on the
+host before touching a device."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nd():
+    from self_speculative_lm_block_b300 import build
+    build.build()
+    from self_speculative_lm_block_b300 import ndiff
+    return ndiff
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"NDIFF_API\s+[\w\s\*]+?\b(ndiff_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(nd):
+    import ctypes
+    lib = ctypes.CDLL(nd.LIB_PATH)
+    declared = _declared()
+    assert len(declared) >= 17
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert declared <= set(nd.exported_names())
+
+
+def test_status_strings(nd):
+    assert nd.ndiff_status_string(0) == "NDIFF_OK"
+    assert nd.ndiff_status_string(6) == "NDIFF_ERR_TIMEOUT"
+
+
+def test_host_side_validation_without_gpu(nd):
+    # every rejection below happens before any CUDA call
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_unmask(1, 1, 4, 33, 1, 1, 1, 1, 1, stream=0)
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_verify_accept(1, 1, 4, 0, 1, 1, 1, None, stream=0)
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_logits_reduce(nd.NDIFF_BF16, 16, 4, 100, 50, -1, 16, 16, stream=0)
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_block_attn(nd.NDIFF_BF16, 16, 16, 16, 16, 1, 32, 32, 8, 64, 100, 0, 0.1, 16,
+                            stream=0)
+    assert e.value.status == nd.NDIFF_ERR_UNSUPPORTED
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_block_attn(nd.NDIFF_BF16, 16, 16, 16, 16, 1, 64, 32, 8, 128, 100, 0, 0.1, 16,
+                            stream=0)
+    assert e.value.status == nd.NDIFF_ERR_UNSUPPORTED  # G*T = 256 > 128
+    # empty batches are no-ops
+    nd.ndiff_unmask(None, None, 0, 32, 1, None, None, None, None, stream=0)
+    nd.ndiff_verify_accept(None, None, 0, 32, None, None, None, None, stream=0)
+    nd.ndiff_logits_reduce(nd.NDIFF_F32, None, 0, 10, 10, -1, None, None, stream=0)
+
+
+def test_workspace_sizes(nd):
+    # one split per (b, g): no scratch; many splits: scratch grows with them
+    assert nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 512) == 0
+    w = nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 128)
+    assert w == 2 * 8 * 4 * 128 * (128 * 4 + 8)
+    assert nd.ndiff_block_attn_workspace_size(nd.NDIFF_F32, 2, 32, 4, 4, 32, 512) == 0
