@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-step hot path on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Workloads (seeded synthetic inputs, shapes of the 8B-like configurations):
+  attn-batched  one decode-step pass over a batch of 64 sequences with KV
+                prefixes uniform in [512, 8192]: block-causal attention
+                (32 query / 8 KV heads x 128, 32-token block), logits
+                reduction over 64 x 32 x 151936 bf16 logits, unmask (k = 8) and
+                verify/accept. value = algorithmic HBM bytes of the pass / time.
+  attn-single   block attention alone, batch 1, prefix 4096 (17 MB of KV,
+                rotated over copies so every launch reads from HBM).
+  attn-long     block attention alone, batch 4, prefix 32768.
+
+Under torchrun (N > 1) each rank runs an independent replica of the workload
+(sequences are independent: no collective on the data path); value is the
+work of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward at 8B"
+SPEC_HBM_GBS = 8000.0
+L2_BYTES = 126e6
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        rows = [r for r in self.rows if len(r) > 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+def attn_bytes(lengths, T, Hq, Hkv, D):
+    """Algorithmic bytes of one attention launch: every visible K and V row
+    once (Hkv x D bf16 each), Q read and O written once."""
+    kv = int(np.sum(np.asarray(lengths, dtype=np.int64) + T)) * Hkv * D * 2 * 2
+    qo = len(lengths) * T * Hq * D * 2 * 2
+    return kv + qo
+
+
+class AttnWorkload:
+    """Attention-only or full batched pass on device-resident inputs."""
+
+    def __init__(self, name, rank):
+        import torch
+        from self_speculative_lm_block_b300 import ndiff as nd
+        from self_speculative_lm_block_b300 import synth
+        self.nd, self.torch = nd, torch
+        self.name = name
+        c = {"attn-single": synth.ATTN_SINGLE, "attn-batched": synth.ATTN_BATCHED,
+             "attn-long": synth.ATTN_LONG}[name]
+        self.c = c
+        seed = c["seed"] + 1000 * rank
+        lengths = synth.attn_lengths(c["B"], seed, c["P_lo"], c["P_hi"])
+        self.lengths = lengths
+        self.Lmax = int(c["P_hi"]) + c["T"]
+        inp = synth.attn_inputs(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], lengths, self.Lmax, seed)
+        self.host = inp
+        dev = "cuda"
+        self.q = inp.q.to(dev)
+        self.kv_len = inp.kv_len.to(dev)
+        self.scale = inp.scale
+        # rotate over copies when one copy would stay resident in L2
+        one = inp.k_cache.numel() * 2 * 2
+        self.ncopy = 1 if one >= 4 * L2_BYTES else int(np.ceil(4 * L2_BYTES / one))
+        self.k = [inp.k_cache.to(dev) for _ in range(self.ncopy)]
+        self.v = [inp.v_cache.to(dev) for _ in range(self.ncopy)]
+        self.out = torch.empty_like(self.q)
+        B, T, Hq, Hkv, D = c["B"], c["T"], c["Hq"], c["Hkv"], c["D"]
+        self.ws_bytes = nd.ndiff_block_attn_workspace_size(nd.NDIFF_BF16, B, T, Hq, Hkv, D, self.Lmax)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.attn_bytes = attn_bytes(lengths, T, Hq, Hkv, D)
+        self.step_bytes = self.attn_bytes
+        self.full = name == "attn-batched"
+        self.attn_launches = 1 + (1 if self.ws_bytes > 0 else 0)
+        self.launches = self.attn_launches
+        if self.full:
+            V = c["V"]
+            R = B * T
+            self.V, self.R = V, R
+            self.logits = synth.logits(R, V, c["logit_sigma"], seed).to(dev)
+            draft, target, _ = synth.draft_target(B, T, V, seed)
+            self.draft = draft.to(dev)
+            self.ids = torch.empty(R, dtype=torch.int32, device=dev)
+            self.conf = torch.empty(R, dtype=torch.float32, device=dev)
+            self.L = torch.empty(B, dtype=torch.int32, device=dev)
+            self.n = torch.empty(B, dtype=torch.int32, device=dev)
+            self.commit = torch.empty((B, T), dtype=torch.int32, device=dev)
+            _, _, mask = synth.unmask_inputs(B, T, V, seed, all_masked=True)
+            self.u_mask0 = mask.to(dev)
+            self.u_mask = self.u_mask0.clone()
+            self.blk = torch.zeros((B, T), dtype=torch.int32, device=dev)
+            self.drf = torch.full((B, T), -1, dtype=torch.int32, device=dev)
+            self.chosen = torch.empty((B, 8), dtype=torch.int32, device=dev)
+            # logits read; ids/conf written; unmask and accept read/write [B][T] ints
+            self.step_bytes += R * V * 2 + R * 8 + B * T * 4 * 10
+            self.launches += 3
+        self.i = 0
+
+    def step(self, attn_only=False):
+        nd = self.nd
+        c = self.c
+        j = self.i % self.ncopy
+        self.i += 1
+        nd.ndiff_block_attn(nd.NDIFF_BF16, self.q, self.k[j], self.v[j], self.kv_len, c["B"], c["T"],
+                            c["Hq"], c["Hkv"], c["D"], self.Lmax, nd.NDIFF_CAUSAL, self.scale,
+                            self.out, self.ws, self.ws_bytes)
+        if self.full and not attn_only:
+            nd.ndiff_logits_reduce(nd.NDIFF_BF16, self.logits, self.R, self.V, self.V, self.V - 1,
+                                   self.ids, self.conf)
+            nd.ndiff_verify_accept(self.draft, self.ids, c["B"], c["T"], self.L, self.commit, self.n,
+                                   None)
+            self.u_mask.copy_(self.u_mask0)
+            nd.ndiff_unmask(self.conf, self.ids, c["B"], c["T"], 8, self.u_mask, self.blk, self.drf,
+                            self.chosen)
+
+    def e2e_step(self, pinned):
+        """Host buffers in, host results out, through the C ABI."""
+        nd = self.nd
+        c = self.c
+        self.q.copy_(pinned["q"], non_blocking=True)
+        self.k[0].copy_(pinned["k"], non_blocking=True)
+        self.v[0].copy_(pinned["v"], non_blocking=True)
+        self.kv_len.copy_(pinned["kv_len"], non_blocking=True)
+        nd.ndiff_block_attn(nd.NDIFF_BF16, self.q, self.k[0], self.v[0], self.kv_len, c["B"], c["T"],
+                            c["Hq"], c["Hkv"], c["D"], self.Lmax, nd.NDIFF_CAUSAL, self.scale,
+                            self.out, self.ws, self.ws_bytes)
+        pinned["out"].copy_(self.out, non_blocking=True)
+        h2d = sum(pinned[x].numel() * pinned[x].element_size() for x in ("q", "k", "v", "kv_len"))
+        d2h = pinned["out"].numel() * 2
+        if self.full:
+            self.logits.copy_(pinned["logits"], non_blocking=True)
+            self.draft.copy_(pinned["draft"], non_blocking=True)
+            nd.ndiff_logits_reduce(nd.NDIFF_BF16, self.logits, self.R, self.V, self.V, self.V - 1,
+                                   self.ids, self.conf)
+            nd.ndiff_verify_accept(self.draft, self.ids, c["B"], c["T"], self.L, self.commit, self.n,
+                                   None)
+            pinned["commit"].copy_(self.commit, non_blocking=True)
+            h2d += pinned["logits"].numel() * 2 + pinned["draft"].numel() * 4
+            d2h += pinned["commit"].numel() * 4
+        return h2d, d2h
+
+    def pinned(self):
+        torch = self.torch
+        d = {"q": self.host.q.pin_memory(), "k": self.host.k_cache.pin_memory(),
+             "v": self.host.v_cache.pin_memory(), "kv_len": self.host.kv_len.pin_memory(),
+             "out": torch.empty(self.q.shape, dtype=self.q.dtype).pin_memory()}
+        if self.full:
+            d["logits"] = self.logits.cpu().pin_memory()
+            d["draft"] = self.draft.cpu().pin_memory()
+            d["commit"] = torch.empty(self.commit.shape, dtype=torch.int32).pin_memory()
+        return d
+
+    def config(self):
+        c = self.c
+        cfg = {"workload": self.name, "batch": c["B"], "q_heads": c["Hq"], "kv_heads": c["Hkv"],
+               "head_dim": c["D"], "block": c["T"],
+               "kv_prefix": [int(c["P_lo"]), int(c["P_hi"])], "mask": "causal",
+               "l2": ("inputs larger than L2" if self.ncopy == 1 else
+                      f"rotating {self.ncopy} KV copies (> 4x L2)")}
+        if self.full:
+            cfg.update({"vocab": self.V, "logits": "bf16 N(0,4^2)", "unmask_k": 8})
+        return cfg
+
+    def oracle_sample(self):
+        """Oracle time on a bounded sample of the same pass -> GB/s of that sample."""
+        from oracle import attention as OA
+        from oracle import decode as OD
+        h = self.host
+        B = 2 if self.name != "attn-long" else 1
+        q = h.q[:B].float().numpy()
+        P = h.kv_len[:B].numpy()
+        Lm = int(P.max()) + self.c["T"]
+        k = h.k_cache[:B, :, :Lm].float().numpy()
+        v = h.v_cache[:B, :, :Lm].float().numpy()
+        t0 = time.perf_counter()
+        OA.block_attn(q, k, v, P, OA.CAUSAL, self.scale)
+        nbytes = attn_bytes(P, self.c["T"], self.c["Hq"], self.c["Hkv"], self.c["D"])
+        desc = f"{B} sequence(s) of the attention"
+        if self.full:
+            rows = 64
+            x = self.logits[:rows].float().cpu().numpy()
+            OD.logits_reduce(x, exclude_id=self.V - 1)
+            nbytes += rows * self.V * 2
+            desc += f" + {rows} logits rows"
+        dt = time.perf_counter() - t0
+        return nbytes / dt / 1e9, desc, dt
+
+
+def _oracle_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [1])
+    except Exception:
+        return os.cpu_count()
+
+
+def make_workload(name, rank):
+    if name.startswith("attn-"):
+        return AttnWorkload(name, rank)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return
+    wl = make_workload(args.workload, 0)
+    vals, desc = [], ""
+    for i in range(args.warmup + args.steps):
+        v, desc, _ = wl.oracle_sample()
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": wl.config(),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": _oracle_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def capture(torch, fn, n):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                fn()
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="attn-batched",
+                    choices=["attn-batched", "attn-single", "attn-long"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    wl = make_workload(args.workload, rank)
+    for _ in range(args.warmup):
+        wl.step()
+    barrier()
+    # The timed region replays CUDA graphs of whole steps, so that host launch
+    # overhead stays out of the device timeline of the small configurations.
+    per_graph = wl.ncopy
+    g_step = capture(torch, wl.step, per_graph)
+    g_attn = capture(torch, lambda: wl.step(attn_only=True), per_graph)
+    reps = max(1, (args.steps + per_graph - 1) // per_graph)
+    for _ in range(2):
+        g_step.replay()
+        g_attn.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record()
+        for _ in range(reps):
+            g_step.replay()
+        e1.record()
+        barrier()
+        a0.record()
+        for _ in range(reps):
+            g_attn.replay()
+        a1.record()
+        barrier()
+    steps_done = reps * per_graph
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / steps_done
+    value = wl.step_bytes * world / (ms_step * 1e-3) / 1e9
+    attn_ms = a0.elapsed_time(a1) / steps_done
+    attn_gbs = wl.attn_bytes / (attn_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with pinned host buffers
+    pinned = wl.pinned()
+    for _ in range(2):
+        wl.e2e_step(pinned)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(2, min(args.steps, 5))
+    f0.record()
+    for _ in range(n_e2e):
+        h2d, d2h = wl.e2e_step(pinned)
+    f1.record()
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / n_e2e
+    e2e_val = wl.step_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    hbm, _, _, src = _peaks()
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+               "steps": steps_done, "warmup": args.warmup, "ms_per_step": ms_step,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+               "data": "synthetic", "config": wl.config(),
+               "roofline": {"kernel": "attn_bf16_kernel (+attn_combine_kernel)", "bound": "hbm",
+                            "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
+                            "frac": attn_gbs / hbm, "peak_source": src,
+                            "frac_of_spec_8tbs": attn_gbs / SPEC_HBM_GBS,
+                            "bytes_per_launch": wl.attn_bytes, "ms_per_launch": attn_ms,
+                            "traffic": None},
+               "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+               "gpu_launches": wl.launches * steps_done,
+               "timing": "CUDA-graph replay of whole steps; attention timed by a graph of its launches",
+               "clocks": clk.summary()}
+        if not args.no_cpu_baseline:
+            cv, desc, dt = wl.oracle_sample()
+            out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": _oracle_threads(),
+                                   "kind": "oracle", "sample": desc, "seconds": dt}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
