@@ -128,6 +128,26 @@ NDIFF_API ndiff_status ndiff_block_attn_split(ndiff_dtype dt, const void* q, con
 NDIFF_API size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv,
                                              int D, int Lmax, int split_keys);
 
+/* Same as ndiff_block_attn, for callers that cannot allocate device memory:
+ * plugin interfaces that pass a kernel only its inputs and outputs, and
+ * processes whose memory manager owns all device memory. The paper has no
+ * counterpart; this is a library convenience. The split-KV scratch comes from
+ * a static array inside the library of NDIFF_NOALLOC_SCRATCH_BYTES per GPU,
+ * held until the process exits; nothing is allocated. Shapes whose
+ * ndiff_block_attn_workspace_size() exceeds that size are rejected with
+ * NDIFF_ERR_WORKSPACE. The first call on a device looks up the array's device
+ * address and should come before any stream capture. All calls share the one
+ * array: calls whose kernels overlap on the GPU race and must be serialised by
+ * the caller. The array keeps what the previous call left in it; nothing in
+ * it has to start at zero, because each call writes every partial result
+ * before its merge step reads it. */
+#define NDIFF_NOALLOC_SCRATCH_BYTES (16u << 20)
+NDIFF_API ndiff_status ndiff_block_attn_noalloc(ndiff_dtype dt, const void* q, const void* k_cache,
+                                                const void* v_cache, const int32_t* kv_len, int B,
+                                                int T, int Hq, int Hkv, int D, int Lmax,
+                                                ndiff_mask mode, float scale, void* out,
+                                                cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Logits reduction: per row r of logits [R][V] (row stride ld elements),
  *   argmax[r] = smallest v in [0,V), v != exclude_id, with the largest logit;

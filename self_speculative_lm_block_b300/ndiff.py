@@ -20,6 +20,7 @@ NDIFF_ERR_CUDA, NDIFF_ERR_OOM, NDIFF_ERR_WORKSPACE, NDIFF_ERR_TIMEOUT = 3, 4, 5,
 NDIFF_BF16, NDIFF_F32 = 0, 1
 NDIFF_BIDIR, NDIFF_CAUSAL = 0, 1
 NDIFF_MODE_AR, NDIFF_MODE_DIFF, NDIFF_MODE_SELFSPEC = 0, 1, 2
+NDIFF_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class NdiffError(RuntimeError):
@@ -56,6 +57,7 @@ _SIGS = {
     "ndiff_block_attn_split": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
                                     _SZ, _P]),
     "ndiff_block_attn_split_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "ndiff_block_attn_noalloc": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "ndiff_logits_reduce": (_I, [_I, _P, _I, _I, _I64, _I, _P, _P, _P]),
     "ndiff_unmask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_verify_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
@@ -142,6 +144,12 @@ def ndiff_block_attn_split(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lm
 
 def ndiff_block_attn_split_workspace_size(dt, B, T, Hq, Hkv, D, Lmax, split_keys) -> int:
     return _lib.ndiff_block_attn_split_workspace_size(dt, B, T, Hq, Hkv, D, Lmax, split_keys)
+
+
+def ndiff_block_attn_noalloc(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lmax, mode, scale,
+                             out, stream=None):
+    return _call("ndiff_block_attn_noalloc", dt, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                 _ptr(kv_len), B, T, Hq, Hkv, D, Lmax, mode, scale, _ptr(out), _stream(stream))
 
 
 def ndiff_logits_reduce(dt, logits, R, V, ld, exclude_id, argmax, conf, stream=None):
