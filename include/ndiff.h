@@ -202,6 +202,22 @@ NDIFF_API ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* 
                                  int32_t* kv_len, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Projection of a token block: y[m][n] = sum_k x[m][k] * w[n][k] for m < M,
+ * n < N — the matrix products of every layer of the model, which decode runs
+ * on at most one 32-token block at a time ([FFI] "三种生成模式"; [HFB]:
+ * decode is bound by memory traffic, i.e. by streaming w).
+ * x: bf16 [M][K] row-major, w: bf16 [N][K] row-major (both 16-byte aligned),
+ * y: fp32 [M][ldy] (ldy >= N). 1 <= M <= 32, N >= 1, K a positive multiple of
+ * 64. fp32 accumulation on the tensor cores; a row's result does not depend on
+ * M (the same row computed alone or inside a block is bit-identical).
+ * ws/ws_bytes: device scratch of at least ndiff_gemm_bf16_workspace_size()
+ *   bytes; its contents need no initialisation (the call clears what it needs).
+ * ------------------------------------------------------------------------ */
+NDIFF_API size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K);
+NDIFF_API ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, float* y,
+                                       int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Random-init tri-mode model (one checkpoint, three modes: [FFI]
  * "三种生成模式"; [AIF] "方法 / 推理").
  * Pre-norm transformer: x = E[ids]; per layer

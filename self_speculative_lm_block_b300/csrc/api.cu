@@ -249,4 +249,43 @@ ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, in
   return launch_verify_accept(draft, target, B, T, accept_len, commit, n_commit, kv_len, stream);
 }
 
+size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 64) return 0;
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  return cnt + gemm_partials_bytes(pl);
+}
+
+ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, float* y,
+                             int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0 || ldy < N)
+    return set_error(NDIFF_ERR_INVALID_ARG,
+                     "ndiff_gemm_bf16: need 1<=M<=32, N>=1, K a positive multiple of 64, ldy>=N "
+                     "(M=%d N=%d K=%d ldy=%lld)",
+                     M, N, K, (long long)ldy);
+  if (!x || !w || !y) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_gemm_bf16: null pointer");
+  if (!aligned16(x) || !aligned16(w))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_gemm_bf16: x and w must be 16-byte aligned");
+  const size_t need = ndiff_gemm_bf16_workspace_size(M, N, K);
+  if (!ws || ws_bytes < need)
+    return set_error(NDIFF_ERR_WORKSPACE, "ndiff_gemm_bf16: workspace of %zu bytes needed, %zu given",
+                     need, ws_bytes);
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  CUtensorMap tw, tx;
+  ndiff_status s = gemm_make_maps(w, N, K, x, M, &tw, &tx);
+  if (s != NDIFF_OK) return s;
+  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.N = N;
+  p.T = M;
+  p.mode = GEMM_EPI_F32;
+  p.counters = static_cast<int*>(ws);
+  p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt);
+  p.out = y;
+  p.ldo = ldy;
+  return launch_gemm_bf16(tw, tx, pl, p, stream);
+}
+
 }  // extern "C"

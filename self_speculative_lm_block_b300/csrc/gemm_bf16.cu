@@ -1,0 +1,404 @@
+// gemm_bf16.cu — the model's projections on sm_103a: y[m][n] = sum_k x[m][k] W[n][k]
+// for a block of at most 32 token rows (the 32-token block of the decode step,
+// or one token in AR mode) against a bf16 weight matrix W [N][K].
+//
+// Where it sits: every linear map of the pre-norm transformer (QKV, output
+// projection, SwiGLU gate/up, down projection, LM head) that one checkpoint
+// runs in all three decode modes ("NVIDIA 发布 Nemotron-Labs Diffusion 语言模型
+// 系列" (fintech-frontier-insights), "三种生成模式"). Decode is bound by the
+// bytes of the weights ("NVIDIA 发布 Nemotron-Labs Diffusion：三模态语言模型统一
+// AR 与扩散解码" (aimodeling.com), on memory-I/O-bound decoding), so the kernel is
+// a weight stream with the tensor cores doing 32 columns of work per weight.
+//
+// Design (swap-AB: the weight tile is the MMA's 128-row A operand, the token
+// rows are its N = 32 columns, so the accumulator is 128 lanes x 32 fp32
+// columns of TMEM):
+//   * Work items are (128-row tile of W, K split). A persistent grid of at most
+//     one CTA per SM walks the items round-robin. Warp 0 streams 128x64 weight
+//     tiles and the matching 32x64 activation tile through an 8-stage TMA ring
+//     (128-byte swizzle); warp 1 issues tcgen05.mma (M128 N32 K16) into one of
+//     two TMEM accumulators; warps 2-5 drain the other accumulator, so the
+//     epilogue of one item overlaps the loads of the next.
+//   * K splits: every split writes its fp32 partial tile to the workspace and
+//     bumps a per-tile counter; the last split to arrive adds the partials in
+//     split order 0..S-1 and runs the fused epilogue, then resets the counter.
+//     The split boundaries depend only on (N, K, SM count), never on the number
+//     of token rows, and the MMA column count is always 32, so a token row's
+//     result is the same whether it is computed alone (AR) or inside a block.
+//   * Fused epilogues: fp32 store (logits), residual add (x += y), SwiGLU over
+//     interleaved 64-row gate/up groups, and QKV with rotate-half RoPE from a
+//     precomputed table plus the K/V-cache write at the block's positions.
+//   * Every mbarrier wait is bounded; on expiry the kernel records a timeout in
+//     the device status word, lets issued TMA copies land, frees TMEM and exits.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ndiff {
+namespace gemm {
+
+constexpr int BM = 128;                    // weight rows per tile (MMA M)
+constexpr int BK = 64;                     // K per stage (one 128-byte swizzle atom)
+constexpr int MT = 32;                     // token rows (MMA N)
+constexpr int NST = 8;                     // pipeline stages
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = MT * BK * 2;       // 4 KB
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NST * A_BYTES;
+constexpr int OFF_X = OFF_B + NST * B_BYTES;         // epilogue exchange [128][33] fp32
+constexpr int X_STRIDE = MT + 1;
+constexpr int OFF_BAR = OFF_X + BM * X_STRIDE * 4;
+constexpr int N_BARS = 2 * NST + 4 + 1;
+constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
+constexpr int TMEM_COLS = 64;              // two 32-column accumulators
+constexpr int THREADS = 192;
+
+static_assert(OFF_B % 1024 == 0 && OFF_X % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+__device__ __forceinline__ bool bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t b = smem_u32(bar);
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(b, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void split_range(int s, int S, int nks, int& lo, int& hi) {
+  lo = (int)(((long long)s * nks) / S);
+  hi = (int)(((long long)(s + 1) * nks) / S);
+}
+
+// Epilogue of one finished 128-row tile. Thread r holds y[m] for weight row
+// tile*128 + r and token rows m < T.
+__device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[MT],
+                                         float* xch) {
+  const int n = tile * BM + r;
+  switch (p.mode) {
+    case GEMM_EPI_F32: {
+      if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < p.T) p.out[(size_t)m * p.ldo + n] = v[m];
+      }
+      break;
+    }
+    case GEMM_EPI_RESID: {
+      if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < p.T) p.out[(size_t)m * p.ldo + n] += v[m];
+      }
+      break;
+    }
+    case GEMM_EPI_SWIGLU: {
+      // rows [0,64) of the tile are gate rows j, rows [64,128) the up rows of the same j
+#pragma unroll
+      for (int m = 0; m < MT; ++m) xch[r * X_STRIDE + m] = v[m];
+      bar_sync128();
+      if (r < 64) {
+        const int j = tile * 64 + r;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < p.T) {
+            const float g = v[m];
+            const float u = xch[(r + 64) * X_STRIDE + m];
+            p.act[(size_t)m * p.lda + j] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+          }
+        }
+      }
+      break;
+    }
+    case GEMM_EPI_QKV: {
+      // tile = one head of 128 dims: q heads, then k heads, then v heads
+#pragma unroll
+      for (int m = 0; m < MT; ++m) xch[r * X_STRIDE + m] = v[m];
+      bar_sync128();
+      int P = p.kv_len[0];
+      P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+      const int h = tile;
+      const bool rot = h < p.Hq + p.Hkv;
+      const int pr = r ^ 64;
+      const float sgn = r < 64 ? -1.f : 1.f;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < p.T) {
+          float y = v[m];
+          if (rot) {
+            const float2 cs = p.rope[(size_t)(P + m) * 64 + (r & 63)];
+            y = y * cs.x + sgn * xch[pr * X_STRIDE + m] * cs.y;
+          }
+          const __nv_bfloat16 o = __float2bfloat16_rn(y);
+          if (h < p.Hq) {
+            p.q[((size_t)m * p.Hq + h) * BM + r] = o;
+          } else if (h < p.Hq + p.Hkv) {
+            p.kc[((size_t)(h - p.Hq) * p.Lmax + P + m) * BM + r] = o;
+          } else {
+            p.vc[((size_t)(h - p.Hq - p.Hkv) * p.Lmax + P + m) * BM + r] = o;
+          }
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + OFF_A;
+  uint8_t* sB = smem + OFF_B;
+  float* xch = reinterpret_cast<float*>(smem + OFF_X);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = full + NST;
+  uint64_t* acc_full = empty + NST;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int grid = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int kc = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < p.items; it += grid) {
+        const int tile = it / p.S, s = it % p.S;
+        int lo, hi;
+        split_range(s, p.S, p.nks, lo, hi);
+        for (int ks = lo; ks < hi; ++ks) {
+          const int st = kc % NST;
+          if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
+          tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
+          tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
+          ++kc;
+        }
+      }
+      if (*abort_flag) {
+        for (int j = (kc > NST ? kc - NST : 0); j < kc; ++j) mbar_drain(&full[j % NST], (j / NST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, MT, false, false);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      int kc = 0, ic = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < p.items; it += grid) {
+        const int s = it % p.S;
+        int lo, hi;
+        split_range(s, p.S, p.nks, lo, hi);
+        const int buf = ic & 1;
+        if (ic >= 2 && !mbar_wait(&acc_empty[buf], ((ic >> 1) - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * MT;
+        for (int ks = lo; ks < hi; ++ks) {
+          const int st = kc % NST;
+          if (!mbar_wait(&full[st], (kc / NST) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a0 + st * A_BYTES + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + st * B_BYTES + kk * 32, 16, 1024);
+            umma_f16(d, ad, bd, idesc, (ks > lo || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
+          ++kc;
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[buf]);
+        ++ic;
+      }
+      // every MMA issued above has finished before TMEM is released
+      umma_commit(mma_done);
+      mbar_drain(mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int tid = threadIdx.x - 64;
+    const uint32_t tl = tmem + ((quarter * 32u) << 16);
+    int ic = 0;
+    for (int it = blockIdx.x; it < p.items; it += grid, ++ic) {
+      const int buf = ic & 1;
+      bool ok = mbar_wait(&acc_full[buf], (ic >> 1) & 1, p.status, abort_flag);
+      if (!bar_and(ok)) break;
+      tc_fence_after();
+      float v[MT];
+      tmem_ld32(tl + buf * MT, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+
+      const int tile = it / p.S, s = it % p.S;
+      if (p.S > 1) {
+        float* part = p.ws + (size_t)it * (MT * BM);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < p.T) __stcg(part + m * BM + r, v[m]);
+        __threadfence();
+        bar_sync128();
+        if (tid == 0) *last_flag = (atomicAdd(&p.counters[tile], 1) == p.S - 1) ? 1 : 0;
+        bar_sync128();
+        if (!*last_flag) continue;
+        __threadfence();
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < p.T) {
+            float acc = 0.f;
+            for (int s2 = 0; s2 < p.S; ++s2)
+              acc += (s2 == s) ? v[m]
+                               : __ldcg(p.ws + ((size_t)(tile * p.S + s2) * MT + m) * BM + r);
+            v[m] = acc;
+          }
+        }
+        if (tid == 0) p.counters[tile] = 0;
+      }
+      epilogue(p, tile, r, v, xch);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace gemm
+
+GemmPlan gemm_plan(int N, int K) {
+  GemmPlan pl;
+  pl.ntiles = (N + gemm::BM - 1) / gemm::BM;
+  pl.nks = K / gemm::BK;
+  const int sms = num_sms();
+  // Cost of a split count S: the busiest CTA's k-steps (16 KB of weights
+  // each) plus, when split, the partial tile it writes and the last split's
+  // reads (about two k-steps' worth). Ties keep the smaller S.
+  long long best = -1;
+  int bestS = 1;
+  const int smax = pl.nks < 32 ? pl.nks : 32;
+  for (int S = 1; S <= smax; ++S) {
+    const long long items = (long long)pl.ntiles * S;
+    const long long waves = (items + sms - 1) / sms;
+    const long long steps = (pl.nks + S - 1) / S;
+    const long long cost = waves * (steps + (S > 1 ? 2 : 0));
+    if (best < 0 || cost < best) {
+      best = cost;
+      bestS = S;
+    }
+  }
+  pl.S = bestS;
+  pl.items = pl.ntiles * pl.S;
+  pl.grid = pl.items < sms ? pl.items : sms;
+  return pl;
+}
+
+size_t gemm_partials_bytes(const GemmPlan& pl) {
+  return pl.S > 1 ? (size_t)pl.items * gemm::MT * gemm::BM * sizeof(float) : 0;
+}
+
+ndiff_status gemm_make_maps(const void* w, int N, int K, const void* x, int M, CUtensorMap* tmW,
+                            CUtensorMap* tmX) {
+  if (tmW) {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {gemm::BK, gemm::BM};
+    ndiff_status s = make_tmap_bf16(tmW, w, 2, dims, strides, box);
+    if (s != NDIFF_OK) return s;
+  }
+  if (tmX) {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {gemm::BK, gemm::MT};
+    ndiff_status s = make_tmap_bf16(tmX, x, 2, dims, strides, box);
+    if (s != NDIFF_OK) return s;
+  }
+  return NDIFF_OK;
+}
+
+ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                              GemmParams p, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  NDIFF_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 64 && !attr_set[dev]) {
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        gemm::SMEM_BYTES));
+    attr_set[dev] = true;
+  }
+  p.S = pl.S;
+  p.nks = pl.nks;
+  p.items = pl.items;
+  p.status = device_status_word();
+  gemm::gemm_bf16_kernel<<<pl.grid, gemm::THREADS, gemm::SMEM_BYTES, stream>>>(tmW, tmX, p);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+}  // namespace ndiff

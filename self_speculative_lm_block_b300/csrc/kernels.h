@@ -2,6 +2,8 @@
 // validation happens in api.cu before any of these is called.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,5 +37,37 @@ ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T,
 ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                   int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                   int32_t* kv_len, cudaStream_t stream);
+
+// gemm_bf16.cu — y = x W^T for at most 32 token rows, with fused epilogues
+enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3 };
+
+struct GemmParams {
+  int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
+  int S, nks, items;       // K splits, 64-wide K steps, work items (set by the launcher)
+  float* ws;               // split partials [items][32][128] fp32 (S > 1)
+  int* counters;           // [tiles] arrival counters, zero between launches
+  unsigned int* status;    // device status word
+  float* out;              // F32: out[m*ldo + n] = y; RESID: out[m*ldo + n] += y
+  int64_t ldo;
+  __nv_bfloat16* act;      // SWIGLU: act[m*lda + j] = silu(gate_j) * up_j
+  int64_t lda;
+  __nv_bfloat16* q;        // QKV: q [T][Hq][128]; k/v caches [Hkv][Lmax][128]
+  __nv_bfloat16* kc;
+  __nv_bfloat16* vc;
+  int Hq, Hkv, Lmax;
+  const int32_t* kv_len;   // QKV: committed prefix (batch 1)
+  const float2* rope;      // QKV: (cos, sin) [Lmax][64]
+};
+
+struct GemmPlan {
+  int ntiles, nks, S, items, grid;
+};
+
+GemmPlan gemm_plan(int N, int K);
+size_t gemm_partials_bytes(const GemmPlan& pl);
+ndiff_status gemm_make_maps(const void* w, int N, int K, const void* x, int M, CUtensorMap* tmW,
+                            CUtensorMap* tmX);
+ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                              GemmParams p, cudaStream_t stream);
 
 }  // namespace ndiff

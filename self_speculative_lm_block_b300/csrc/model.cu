@@ -1,29 +1,616 @@
-// model.cu — placeholder for the model entry points (filled in below).
+// model.cu — the random-init tri-mode model behind the C ABI: weights, KV
+// cache, one forward of a token block, and the three decode modes.
+//
+// Sources (page title, section):
+//   "NVIDIA 发布 Nemotron-Labs Diffusion 语言模型系列" (fintech-frontier-insights),
+//     "三种生成模式": one checkpoint run as AR (token by token), as block
+//     diffusion (a 32-token block refined over several denoising rounds) or as
+//     self-speculation (diffusion drafts, AR verifies; at temperature 0 the
+//     output equals AR output); "训练路线": block-wise attention keeps the KV
+//     cache usable.
+//   "Nemotron-Labs-Diffusion: A Tri-Mode Language Model ..." (hotpaper.ai),
+//     Abstract: in self-speculation the diffusion mode drafts and the AR mode
+//     verifies, within one model.
+//   gsyq.cn explainer, §2.3 "自推测解码": accept the agreeing prefix and take
+//     the verifier's token at the first mismatch.
+//
+// Readings where the pages are silent: the logits of input slot i predict the
+// token after it in every mode; [MASK] = vocab-1, never predicted; a diffusion
+// block enters the cache through one bidirectional forward of the finished
+// block; the self-speculation draft is `steps` bidirectional forwards, each
+// fixing the 32/steps most confident masked slots.
+//
+// Numerics: bf16 models keep bf16 weights and round the inputs of every matrix
+// product (normed activations, attention output, SwiGLU output) and q/k/v to
+// bf16; the residual stream, accumulators and logits are fp32. Every kernel
+// computes a token row independently of the other rows and of the block
+// length, so a causal block forward reproduces single-token forwards bit for
+// bit and temperature-0 self-speculation commits exactly the AR tokens.
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "model_kernels.h"
 
 using namespace ndiff;
 
+#define TRY(expr)                                 \
+  do {                                            \
+    ndiff_status _s = (expr);                     \
+    if (_s != NDIFF_OK) return _s;                \
+  } while (0)
+
+namespace {
+
+constexpr int kBlock = 32;
+constexpr double kSigma = 0.02;
+
+struct Layer {
+  void* wqkv = nullptr;  // [(Hq + 2 Hkv) D][d]: q rows, k rows, v rows
+  void* wo = nullptr;    // [d][Hq D]
+  void* wgu = nullptr;   // [2 ffn][d]: bf16 64-row interleave of gate/up; f32 gate then up
+  void* wd = nullptr;    // [d][ffn]
+  void* kc = nullptr;    // [Hkv][Lmax][D]
+  void* vc = nullptr;
+  CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
+};
+
+}  // namespace
+
+struct ndiff_model {
+  ndiff_model_config cfg;
+  uint64_t seed = 0;
+  int dev = 0;
+  bool bf16 = false;
+  size_t esz = 4;
+  int D = 0, Hq = 0, Hkv = 0, d = 0, ffn = 0, V = 0, L = 0, Lmax = 0, NQKV = 0, HD = 0;
+  int32_t mask_id = 0;
+  float eps = 1e-6f;
+  void* embed = nullptr;
+  void* lm = nullptr;
+  std::vector<Layer> layers;
+  // activations (32 token rows)
+  float* x = nullptr;        // residual stream fp32 [32][d]
+  void* h = nullptr;         // normed input [32][d] (bf16 or f32)
+  void* qb = nullptr;        // q [32][Hq][D]
+  void* ob = nullptr;        // attention output [32][Hq D]
+  void* ab = nullptr;        // SwiGLU output [32][ffn]
+  float* y = nullptr;        // fp32 path projection scratch [32][ymax]
+  float* logits = nullptr;   // [32][ldl] fp32 (rows 16-byte aligned)
+  int ldl = 0;
+  // decode-cycle state
+  int32_t* ids = nullptr;       // [32] forward input of AR / model_forward
+  int32_t* pred = nullptr;      // [32] argmax
+  float* conf = nullptr;        // [32]
+  int32_t* draft = nullptr;     // [32]
+  int32_t* block_in = nullptr;  // [32]
+  int32_t* res = nullptr;       // [34]: commit[32], n_commit, accept_len
+  int32_t* kv_len = nullptr;    // [1]
+  uint32_t* mask = nullptr;     // [1]
+  int32_t* chosen = nullptr;    // [32]
+  int32_t* prompt = nullptr;    // [Lmax]
+  float2* rope = nullptr;       // [Lmax][D/2]
+  float* gws = nullptr;         // GEMM split partials
+  int* gcnt = nullptr;          // GEMM tile counters
+  void* aws = nullptr;          // attention split-KV scratch
+  size_t aws_bytes = 0;
+  int attn_split = 0;
+  CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
+  GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
+  int32_t* pin = nullptr;       // pinned host staging [64]
+  std::vector<void*> allocs;
+  int P = 0;
+  int32_t last = -1;
+  bool ready = false;
+};
+
+namespace {
+
+ndiff_status dalloc(ndiff_model* m, void** p, size_t bytes) {
+  *p = nullptr;
+  cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return set_error(NDIFF_ERR_OOM, "ndiff_model_create: cudaMalloc of %zu bytes failed (%s)", bytes,
+                     cudaGetErrorString(e));
+  }
+  m->allocs.push_back(*p);
+  return NDIFF_OK;
+}
+
+template <typename Tp>
+ndiff_status dalloc_t(ndiff_model* m, Tp** p, size_t bytes) {
+  void* v = nullptr;
+  ndiff_status s = dalloc(m, &v, bytes);
+  *p = static_cast<Tp*>(v);
+  return s;
+}
+
+void free_model(ndiff_model* m) {
+  for (void* p : m->allocs) cudaFree(p);
+  m->allocs.clear();
+  if (m->pin) cudaFreeHost(m->pin);
+  m->pin = nullptr;
+}
+
+int tid_layer(int l, int j) { return 1 + 8 * l + j; }
+
+ndiff_status check_config(const ndiff_model_config* c) {
+  if (!c) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: null config");
+  if (c->layers < 1 || c->d_model < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
+      c->ffn < 1 || c->vocab < 2 || c->max_seq < kBlock + 1 || !(c->eps > 0.f) ||
+      !(c->rope_base > 1.f))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: bad sizes in config");
+  if (c->batch != 1)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_create: batch must be 1 (got %d)", c->batch);
+  if (c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: n_heads %% n_kv_heads and head_dim %% 2 must be 0");
+  if (c->dtype == NDIFF_BF16) {
+    if (c->head_dim != 128 || c->d_model % 128 != 0 || c->ffn % 128 != 0 ||
+        (c->n_heads / c->n_kv_heads) * kBlock > 128)
+      return set_error(NDIFF_ERR_UNSUPPORTED,
+                       "ndiff_model_create: bf16 models need head_dim 128, d_model and ffn multiples "
+                       "of 128, and n_heads/n_kv_heads <= 4");
+    if ((long long)c->n_kv_heads * c->max_seq >= (1LL << 31))
+      return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_create: KV cache too large");
+  } else if (c->dtype == NDIFF_F32) {
+    if (c->head_dim > 64 || c->d_model > 4096 || c->vocab > (1 << 20))
+      return set_error(NDIFF_ERR_UNSUPPORTED,
+                       "ndiff_model_create: fp32 models need head_dim <= 64, d_model <= 4096");
+  } else {
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: bad dtype %d", (int)c->dtype);
+  }
+  return NDIFF_OK;
+}
+
+// ---------------------------------------------------------------- one forward
+// Runs the T (<= 32) tokens `ids` (device) at positions kv_len .. kv_len+T-1,
+// writes their K/V into the cache there, and (want_logits) leaves fp32 logits
+// in m->logits and the argmax / confidence of every row in m->pred / m->conf.
+ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool want_logits,
+                     cudaStream_t s) {
+  const float scale = 1.f / sqrtf((float)m->D);
+  TRY(launch_embed(m->embed, m->bf16, ids, T, m->V, m->d, m->x, s));
+  GemmParams gp;
+  memset(&gp, 0, sizeof(gp));
+  gp.T = T;
+  gp.ws = m->gws;
+  gp.counters = m->gcnt;
+  for (int l = 0; l < m->L; ++l) {
+    Layer& ly = m->layers[l];
+    TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, m->bf16, s));
+    if (m->bf16) {
+      GemmParams p = gp;
+      p.N = m->NQKV;
+      p.mode = GEMM_EPI_QKV;
+      p.q = static_cast<__nv_bfloat16*>(m->qb);
+      p.kc = static_cast<__nv_bfloat16*>(ly.kc);
+      p.vc = static_cast<__nv_bfloat16*>(ly.vc);
+      p.Hq = m->Hq;
+      p.Hkv = m->Hkv;
+      p.Lmax = m->Lmax;
+      p.kv_len = m->kv_len;
+      p.rope = m->rope;
+      TRY(launch_gemm_bf16(ly.tm_qkv, m->tm_h, m->pl_qkv, p, s));
+      TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, 1, T, m->Hq, m->Hkv, m->Lmax, causal,
+                           scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s));
+      p = gp;
+      p.N = m->d;
+      p.mode = GEMM_EPI_RESID;
+      p.out = m->x;
+      p.ldo = m->d;
+      TRY(launch_gemm_bf16(ly.tm_o, m->tm_oact, m->pl_o, p, s));
+      TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, true, s));
+      p = gp;
+      p.N = 2 * m->ffn;
+      p.mode = GEMM_EPI_SWIGLU;
+      p.act = static_cast<__nv_bfloat16*>(m->ab);
+      p.lda = m->ffn;
+      TRY(launch_gemm_bf16(ly.tm_gu, m->tm_h, m->pl_gu, p, s));
+      p = gp;
+      p.N = m->d;
+      p.mode = GEMM_EPI_RESID;
+      p.out = m->x;
+      p.ldo = m->d;
+      TRY(launch_gemm_bf16(ly.tm_d, m->tm_a, m->pl_d, p, s));
+    } else {
+      const float* h = static_cast<const float*>(m->h);
+      TRY(launch_linear_f32(h, m->d, static_cast<const float*>(ly.wqkv), m->NQKV, m->d, m->y,
+                            m->NQKV, T, s));
+      TRY(launch_qkv_rope_f32(m->y, T, m->Hq, m->Hkv, m->D, m->Lmax, m->kv_len, m->rope,
+                              static_cast<float*>(m->qb), static_cast<float*>(ly.kc),
+                              static_cast<float*>(ly.vc), s));
+      TRY(launch_attn_f32(static_cast<const float*>(m->qb), static_cast<const float*>(ly.kc),
+                          static_cast<const float*>(ly.vc), m->kv_len, 1, T, m->Hq, m->Hkv, m->D,
+                          m->Lmax, causal, scale, static_cast<float*>(m->ob), s));
+      TRY(launch_linear_f32(static_cast<const float*>(m->ob), m->HD, static_cast<const float*>(ly.wo),
+                            m->d, m->HD, m->y, m->d, T, s));
+      TRY(launch_resid_add_f32(m->x, m->y, T * m->d, s));
+      TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, false, s));
+      TRY(launch_linear_f32(h, m->d, static_cast<const float*>(ly.wgu), 2 * m->ffn, m->d, m->y,
+                            2 * m->ffn, T, s));
+      TRY(launch_swiglu_f32(m->y, T, m->ffn, static_cast<float*>(m->ab), s));
+      TRY(launch_linear_f32(static_cast<const float*>(m->ab), m->ffn, static_cast<const float*>(ly.wd),
+                            m->d, m->ffn, m->y, m->d, T, s));
+      TRY(launch_resid_add_f32(m->x, m->y, T * m->d, s));
+    }
+  }
+  if (!want_logits) return NDIFF_OK;
+  TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, m->bf16, s));
+  if (m->bf16) {
+    GemmParams p = gp;
+    p.N = m->V;
+    p.mode = GEMM_EPI_F32;
+    p.out = m->logits;
+    p.ldo = m->ldl;
+    TRY(launch_gemm_bf16(m->tm_lm, m->tm_h, m->pl_lm, p, s));
+  } else {
+    TRY(launch_linear_f32(static_cast<const float*>(m->h), m->d, static_cast<const float*>(m->lm),
+                          m->V, m->d, m->logits, m->ldl, T, s));
+  }
+  return launch_logits_reduce(NDIFF_F32, m->logits, T, m->V, m->ldl, m->mask_id, m->pred, m->conf, s);
+}
+
+// Fills the 32-slot draft of the next block: `steps` bidirectional forwards,
+// each fixing the k = 32/steps most confident masked slots.
+ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
+  const int k = kBlock / steps;
+  TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last, m->mask_id, s));
+  for (int i = 0; i < steps; ++i) {
+    TRY(forward(m, m->block_in, kBlock, 0, true, s));
+    TRY(launch_unmask(m->conf, m->pred, 1, kBlock, k, m->mask, m->block_in, m->draft, m->chosen, s));
+  }
+  return NDIFF_OK;
+}
+
+// Waits for the stream and reports device-side timeouts recorded meanwhile.
+ndiff_status finish(cudaStream_t s) {
+  NDIFF_CUDA_TRY(cudaStreamSynchronize(s));
+  unsigned int* w = device_status_word();
+  if (w) {
+    unsigned int v = 0;
+    NDIFF_CUDA_TRY(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost));
+    if (v) {
+      unsigned int z = 0;
+      NDIFF_CUDA_TRY(cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice));
+      return set_error(NDIFF_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", v);
+    }
+  }
+  return NDIFF_OK;
+}
+
+ndiff_status set_device(const ndiff_model* m) {
+  int cur = -1;
+  NDIFF_CUDA_TRY(cudaGetDevice(&cur));
+  if (cur != m->dev) NDIFF_CUDA_TRY(cudaSetDevice(m->dev));
+  return NDIFF_OK;
+}
+
+ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m) {
+  const ndiff_model_config& c = *cfg;
+  m->cfg = c;
+  m->seed = seed;
+  NDIFF_CUDA_TRY(cudaGetDevice(&m->dev));
+  m->bf16 = c.dtype == NDIFF_BF16;
+  m->esz = m->bf16 ? 2 : 4;
+  m->D = c.head_dim;
+  m->Hq = c.n_heads;
+  m->Hkv = c.n_kv_heads;
+  m->d = c.d_model;
+  m->ffn = c.ffn;
+  m->V = c.vocab;
+  m->L = c.layers;
+  m->Lmax = c.max_seq;
+  m->HD = m->Hq * m->D;
+  m->NQKV = (m->Hq + 2 * m->Hkv) * m->D;
+  m->mask_id = m->V - 1;
+  m->ldl = (m->V + 3) & ~3;
+  m->eps = c.eps;
+  const size_t esz = m->esz;
+  const size_t d = m->d;
+  cudaStream_t s = 0;
+
+  TRY(dalloc(m, &m->embed, (size_t)m->V * d * esz));
+  TRY(dalloc(m, &m->lm, (size_t)m->V * d * esz));
+  m->layers.resize(m->L);
+  const size_t kv_elems = (size_t)m->Hkv * m->Lmax * m->D;
+  for (Layer& ly : m->layers) {
+    TRY(dalloc(m, &ly.wqkv, (size_t)m->NQKV * d * esz));
+    TRY(dalloc(m, &ly.wo, d * m->HD * esz));
+    TRY(dalloc(m, &ly.wgu, 2 * (size_t)m->ffn * d * esz));
+    TRY(dalloc(m, &ly.wd, d * m->ffn * esz));
+    TRY(dalloc(m, &ly.kc, kv_elems * esz));
+    TRY(dalloc(m, &ly.vc, kv_elems * esz));
+    NDIFF_CUDA_TRY(cudaMemsetAsync(ly.kc, 0, kv_elems * esz, s));
+    NDIFF_CUDA_TRY(cudaMemsetAsync(ly.vc, 0, kv_elems * esz, s));
+  }
+  const int ymax = m->NQKV > 2 * m->ffn ? m->NQKV : 2 * m->ffn;
+  TRY(dalloc_t(m, &m->x, kBlock * d * 4));
+  TRY(dalloc(m, &m->h, kBlock * d * esz));
+  TRY(dalloc(m, &m->qb, (size_t)kBlock * m->HD * esz));
+  TRY(dalloc(m, &m->ob, (size_t)kBlock * m->HD * esz));
+  TRY(dalloc(m, &m->ab, (size_t)kBlock * m->ffn * esz));
+  TRY(dalloc_t(m, &m->y, (size_t)kBlock * (ymax > m->d ? ymax : m->d) * 4));
+  TRY(dalloc_t(m, &m->logits, (size_t)kBlock * m->ldl * 4));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->x, 0, kBlock * d * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->h, 0, kBlock * d * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->qb, 0, (size_t)kBlock * m->HD * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ob, 0, (size_t)kBlock * m->HD * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ab, 0, (size_t)kBlock * m->ffn * esz, s));
+  TRY(dalloc_t(m, &m->ids, kBlock * 4));
+  TRY(dalloc_t(m, &m->pred, kBlock * 4));
+  TRY(dalloc_t(m, &m->conf, kBlock * 4));
+  TRY(dalloc_t(m, &m->draft, kBlock * 4));
+  TRY(dalloc_t(m, &m->block_in, kBlock * 4));
+  TRY(dalloc_t(m, &m->res, 64 * 4));
+  TRY(dalloc_t(m, &m->kv_len, 16));
+  TRY(dalloc_t(m, &m->mask, 16));
+  TRY(dalloc_t(m, &m->chosen, kBlock * 4));
+  TRY(dalloc_t(m, &m->prompt, (size_t)m->Lmax * 4));
+  TRY(dalloc_t(m, &m->rope, (size_t)m->Lmax * (m->D / 2) * sizeof(float2)));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, kBlock * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, 16, s));
+
+  if (m->bf16) {
+    m->pl_qkv = gemm_plan(m->NQKV, m->d);
+    m->pl_o = gemm_plan(m->d, m->HD);
+    m->pl_gu = gemm_plan(2 * m->ffn, m->d);
+    m->pl_d = gemm_plan(m->d, m->ffn);
+    m->pl_lm = gemm_plan(m->V, m->d);
+    const GemmPlan* pls[5] = {&m->pl_qkv, &m->pl_o, &m->pl_gu, &m->pl_d, &m->pl_lm};
+    size_t ws = 16;
+    int tiles = 1;
+    for (const GemmPlan* pl : pls) {
+      const size_t b = gemm_partials_bytes(*pl);
+      if (b > ws) ws = b;
+      if (pl->ntiles > tiles) tiles = pl->ntiles;
+    }
+    TRY(dalloc_t(m, &m->gws, ws));
+    TRY(dalloc_t(m, &m->gcnt, (size_t)tiles * 4));
+    NDIFF_CUDA_TRY(cudaMemsetAsync(m->gcnt, 0, (size_t)tiles * 4, s));
+    m->attn_split = attn_bf16_auto_split(1, m->Hkv, m->Lmax);
+    m->aws_bytes = attn_bf16_workspace(1, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
+    if (m->aws_bytes) TRY(dalloc(m, &m->aws, m->aws_bytes));
+    TRY(gemm_make_maps(nullptr, 0, m->d, m->h, kBlock, nullptr, &m->tm_h));
+    TRY(gemm_make_maps(nullptr, 0, m->HD, m->ob, kBlock, nullptr, &m->tm_oact));
+    TRY(gemm_make_maps(nullptr, 0, m->ffn, m->ab, kBlock, nullptr, &m->tm_a));
+    TRY(gemm_make_maps(m->lm, m->V, m->d, nullptr, 0, &m->tm_lm, nullptr));
+    for (Layer& ly : m->layers) {
+      TRY(gemm_make_maps(ly.wqkv, m->NQKV, m->d, nullptr, 0, &ly.tm_qkv, nullptr));
+      TRY(gemm_make_maps(ly.wo, m->d, m->HD, nullptr, 0, &ly.tm_o, nullptr));
+      TRY(gemm_make_maps(ly.wgu, 2 * m->ffn, m->d, nullptr, 0, &ly.tm_gu, nullptr));
+      TRY(gemm_make_maps(ly.wd, m->d, m->ffn, nullptr, 0, &ly.tm_d, nullptr));
+    }
+  }
+
+  // weights: tensor ids 0 = embedding, 1 + 8 l + j for layer l
+  // (j: 0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down), 1 + 8 L = LM head
+  const bool b = m->bf16;
+  TRY(launch_init_normal(m->embed, b, 0, m->V, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+  for (int l = 0; l < m->L; ++l) {
+    Layer& ly = m->layers[l];
+    const int64_t kvr = (int64_t)m->Hkv * m->D;
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 0), m->HD, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 1), kvr, m->d, m->HD, ROWMAP_IDENTITY, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 2), kvr, m->d, m->HD + kvr, ROWMAP_IDENTITY, seed,
+                           kSigma, s));
+    TRY(launch_init_normal(ly.wo, b, tid_layer(l, 3), m->d, m->HD, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wgu, b, tid_layer(l, 4), m->ffn, m->d, 0, b ? ROWMAP_GATE : ROWMAP_IDENTITY,
+                           seed, kSigma, s));
+    TRY(launch_init_normal(ly.wgu, b, tid_layer(l, 5), m->ffn, m->d, b ? 0 : m->ffn,
+                           b ? ROWMAP_UP : ROWMAP_IDENTITY, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wd, b, tid_layer(l, 6), m->d, m->ffn, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+  }
+  TRY(launch_init_normal(m->lm, b, 1 + 8 * m->L, m->V, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+  TRY(launch_rope_table(m->rope, m->Lmax, m->D, (double)c.rope_base, s));
+
+  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&m->pin), 64 * sizeof(int32_t));
+  if (e != cudaSuccess) {
+    m->pin = nullptr;
+    return set_error(NDIFF_ERR_OOM, "ndiff_model_create: pinned host buffer: %s", cudaGetErrorString(e));
+  }
+  NDIFF_CUDA_TRY(cudaStreamSynchronize(s));
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+// Locates weight tensor `tid`: storage base, columns, first storage row, row map.
+bool locate(const ndiff_model* m, int tid, const void** base, int64_t* rows, int64_t* cols,
+            int64_t* row_off, int* map) {
+  *row_off = 0;
+  *map = ROWMAP_IDENTITY;
+  if (tid == 0 || tid == 1 + 8 * m->L) {
+    *base = tid == 0 ? m->embed : m->lm;
+    *rows = m->V;
+    *cols = m->d;
+    return true;
+  }
+  if (tid < 1 || tid > 8 * m->L) return false;
+  const int l = (tid - 1) / 8, j = (tid - 1) % 8;
+  const Layer& ly = m->layers[l];
+  const int64_t kvr = (int64_t)m->Hkv * m->D;
+  switch (j) {
+    case 0: *base = ly.wqkv; *rows = m->HD; *cols = m->d; return true;
+    case 1: *base = ly.wqkv; *rows = kvr; *cols = m->d; *row_off = m->HD; return true;
+    case 2: *base = ly.wqkv; *rows = kvr; *cols = m->d; *row_off = m->HD + kvr; return true;
+    case 3: *base = ly.wo; *rows = m->d; *cols = m->HD; return true;
+    case 4:
+      *base = ly.wgu; *rows = m->ffn; *cols = m->d;
+      if (m->bf16) *map = ROWMAP_GATE;
+      return true;
+    case 5:
+      *base = ly.wgu; *rows = m->ffn; *cols = m->d;
+      if (m->bf16) *map = ROWMAP_UP; else *row_off = m->ffn;
+      return true;
+    case 6: *base = ly.wd; *rows = m->d; *cols = m->ffn; return true;
+    default: return false;
+  }
+}
+
+}  // namespace
+
 extern "C" {
-ndiff_status ndiff_model_create(const ndiff_model_config*, uint64_t, ndiff_model**) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out) {
+  if (!out) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: null output pointer");
+  *out = nullptr;
+  TRY(check_config(cfg));
+  ndiff_model* m = new ndiff_model();
+  ndiff_status st = create(cfg, seed, m);
+  if (st != NDIFF_OK) {
+    free_model(m);
+    delete m;
+    return st;
+  }
+  *out = m;
+  return NDIFF_OK;
 }
-ndiff_status ndiff_model_destroy(ndiff_model*) { return NDIFF_OK; }
-ndiff_status ndiff_prefill(ndiff_model*, const int32_t*, int, cudaStream_t) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_model_destroy(ndiff_model* m) {
+  if (!m) return NDIFF_OK;
+  set_device(m);
+  cudaDeviceSynchronize();
+  free_model(m);
+  delete m;
+  return NDIFF_OK;
 }
-ndiff_status ndiff_decode_step(ndiff_model*, ndiff_mode, int, int32_t*, int*, ndiff_stats*,
-                               cudaStream_t) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cudaStream_t stream) {
+  if (!m || !prompt_host) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: null pointer");
+  if (n < 1 || n + kBlock > m->Lmax)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: need 1 <= n and n + 32 <= max_seq (n=%d, max_seq=%d)",
+                     n, m->Lmax);
+  for (int i = 0; i < n; ++i)
+    if (prompt_host[i] < 0 || prompt_host[i] >= m->V)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: token %d at %d out of range", prompt_host[i], i);
+  TRY(set_device(m));
+  m->ready = false;
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, sizeof(int32_t), stream));
+  NDIFF_CUDA_TRY(cudaMemcpyAsync(m->prompt, prompt_host, (size_t)n * 4, cudaMemcpyHostToDevice, stream));
+  for (int off = 0; off < n - 1; off += kBlock) {
+    const int T = (n - 1 - off) < kBlock ? (n - 1 - off) : kBlock;
+    TRY(forward(m, m->prompt + off, T, 1, false, stream));
+    TRY(launch_kv_add(m->kv_len, T, stream));
+  }
+  TRY(finish(stream));
+  m->P = n - 1;
+  m->last = prompt_host[n - 1];
+  m->ready = true;
+  return NDIFF_OK;
 }
-ndiff_status ndiff_model_forward(ndiff_model*, const int32_t*, int, ndiff_mask, float*,
-                                 cudaStream_t) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32_t* out_tokens_host,
+                               int* n_out, ndiff_stats* stats, cudaStream_t stream) {
+  if (!m || !out_tokens_host || !n_out)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: null pointer");
+  *n_out = 0;
+  if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
+  if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad mode %d", (int)mode);
+  if (mode != NDIFF_MODE_AR && (steps < 1 || steps > kBlock || kBlock % steps != 0))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: steps must divide 32 (got %d)", steps);
+  const int need = mode == NDIFF_MODE_AR ? 1 : kBlock;
+  if (m->P + need > m->Lmax)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)", m->P, m->Lmax);
+  TRY(set_device(m));
+  int n = 0, L = -1;
+  int64_t forwards = 0;
+  if (mode == NDIFF_MODE_AR) {
+    TRY(launch_set_token(m->ids, m->last, stream));
+    TRY(forward(m, m->ids, 1, 1, true, stream));
+    TRY(launch_kv_add(m->kv_len, 1, stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, 4, cudaMemcpyDeviceToHost, stream));
+    TRY(finish(stream));
+    n = 1;
+    forwards = 1;
+  } else if (mode == NDIFF_MODE_DIFF) {
+    TRY(draft_block(m, steps, stream));
+    TRY(forward(m, m->block_in, kBlock, 0, false, stream));
+    TRY(launch_kv_add(m->kv_len, kBlock, stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, kBlock * 4, cudaMemcpyDeviceToHost, stream));
+    TRY(finish(stream));
+    n = kBlock;
+    forwards = steps + 1;
+  } else {
+    TRY(draft_block(m, steps, stream));
+    TRY(forward(m, m->block_in, kBlock, 1, true, stream));
+    int32_t* commit = m->res;
+    TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->res + 33, commit, m->res + 32,
+                             m->kv_len, stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, 34 * 4, cudaMemcpyDeviceToHost, stream));
+    TRY(finish(stream));
+    n = m->pin[32];
+    L = m->pin[33];
+    forwards = steps + 1;
+  }
+  for (int i = 0; i < n; ++i) out_tokens_host[i] = m->pin[i];
+  *n_out = n;
+  m->P += n;
+  m->last = m->pin[n - 1];
+  if (stats) {
+    stats->forwards += forwards;
+    stats->tokens += n;
+    stats->last_accept_len = L;
+    stats->last_n_commit = n;
+    if (L >= 0 && L <= kBlock) stats->accept_hist[L] += 1;
+  }
+  return NDIFF_OK;
 }
-ndiff_status ndiff_model_state(const ndiff_model*, int*, int32_t*) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T, ndiff_mask mode,
+                                 float* logits_host, cudaStream_t stream) {
+  if (!m || !ids_host) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: null pointer");
+  if (T < 1 || T > kBlock)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: 1 <= T <= 32 (got %d)", T);
+  if (mode != NDIFF_BIDIR && mode != NDIFF_CAUSAL)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: bad mask mode %d", (int)mode);
+  if (m->P + T > m->Lmax)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: KV cache full");
+  for (int i = 0; i < T; ++i)
+    if (ids_host[i] < 0 || ids_host[i] >= m->V)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: token out of range");
+  TRY(set_device(m));
+  NDIFF_CUDA_TRY(cudaMemcpyAsync(m->ids, ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, stream));
+  TRY(forward(m, m->ids, T, mode == NDIFF_CAUSAL ? 1 : 0, true, stream));
+  if (logits_host)
+    NDIFF_CUDA_TRY(cudaMemcpy2DAsync(logits_host, (size_t)m->V * 4, m->logits, (size_t)m->ldl * 4,
+                                     (size_t)m->V * 4, T, cudaMemcpyDeviceToHost, stream));
+  return finish(stream);
 }
-ndiff_status ndiff_model_read_weight(const ndiff_model*, int, int64_t, int64_t, float*) {
-  return set_error(NDIFF_ERR_UNSUPPORTED, "model not built yet");
+
+ndiff_status ndiff_model_state(const ndiff_model* m, int* kv_len, int32_t* last_token) {
+  if (!m) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_state: null model");
+  if (kv_len) *kv_len = m->P;
+  if (last_token) *last_token = m->last;
+  return NDIFF_OK;
 }
+
+ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_t offset,
+                                     int64_t count, float* host_out) {
+  if (!m || (!host_out && count > 0))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_read_weight: null pointer");
+  const void* base = nullptr;
+  int64_t rows = 0, cols = 0, row_off = 0;
+  int map = 0;
+  if (!locate(m, tensor_id, &base, &rows, &cols, &row_off, &map))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_read_weight: no tensor %d", tensor_id);
+  if (offset < 0 || count < 0 || offset + count > rows * cols)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_read_weight: range outside the tensor");
+  if (count == 0) return NDIFF_OK;
+  TRY(set_device(m));
+  float* tmp = nullptr;
+  NDIFF_CUDA_TRY(cudaMalloc(&tmp, (size_t)count * 4));
+  ndiff_status s = launch_gather_weight(base, m->bf16, cols, row_off, map, offset, count, tmp, 0);
+  if (s == NDIFF_OK) {
+    cudaError_t e = cudaMemcpy(host_out, tmp, (size_t)count * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) s = cuda_error(e, "ndiff_model_read_weight: copy");
+  }
+  cudaFree(tmp);
+  return s;
 }
+
+}  // extern "C"

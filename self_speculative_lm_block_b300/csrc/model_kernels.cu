@@ -1,0 +1,337 @@
+// model_kernels.cu — the small kernels of the random-init tri-mode model:
+// weight generation, RoPE table, embedding gather, RMSNorm, the fp32 path's
+// projections and epilogues, and the session-state updates of a decode cycle.
+//
+// Model ("Nemotron-Labs-Diffusion: 一种统一自回归、扩散和自推测解码的三模式语言
+// 模型" (ai-feeds.com), "方法": one backbone shared by all modes; "NVIDIA 发布
+// Nemotron-Labs Diffusion 语言模型系列" (fintech-frontier-insights), "三种生成
+// 模式": one checkpoint, three decode modes). The pages give no weights; the
+// model is a pre-norm transformer with every weight drawn N(0, 0.02^2).
+//
+// Weight stream: element i of tensor t is lane i % 4 of block i / 4 of
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11) with counter (i / 4, t, 0, 0) and key (seed, 0); lanes
+// 0/1 are the Box-Muller pair (Box & Muller, 1958) of words 0/1, lanes 2/3 the
+// pair of words 2/3; the value is float(0.02 * z), then bf16 (nearest even)
+// for bf16 models.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "model_kernels.h"
+
+namespace ndiff {
+namespace mk {
+
+// ---------------------------------------------------------------- Philox4x64-10
+__device__ __forceinline__ void philox4x64_10(uint64_t& x0, uint64_t& x1, uint64_t& x2,
+                                              uint64_t& x3, uint64_t k0, uint64_t k1) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    if (rnd) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint64_t hi0 = __umul64hi(M0, x0), lo0 = M0 * x0;
+    const uint64_t hi1 = __umul64hi(M1, x2), lo1 = M1 * x2;
+    const uint64_t y0 = hi1 ^ x1 ^ k0, y2 = hi0 ^ x3 ^ k1;
+    x0 = y0;
+    x1 = lo1;
+    x2 = y2;
+    x3 = lo0;
+  }
+}
+
+__device__ __forceinline__ void box_muller(uint64_t wa, uint64_t wb, double& z0, double& z1) {
+  const double u1 = ((double)(wa >> 11) + 1.0) * 0x1p-53;
+  const double u2 = (double)(wb >> 11) * 0x1p-53;
+  const double r = sqrt(-2.0 * log(u1));
+  const double th = u2 * 6.283185307179586;
+  double s, c;
+  sincos(th, &s, &c);
+  z0 = r * c;
+  z1 = r * s;
+}
+
+__device__ __forceinline__ int64_t map_row(int64_t row, int map) {
+  if (map == ROWMAP_GATE) return (row / 64) * 128 + (row % 64);
+  if (map == ROWMAP_UP) return (row / 64) * 128 + 64 + (row % 64);
+  return row;
+}
+
+__global__ void init_normal_kernel(void* dst, int is_bf16, int tensor_id, int64_t rows,
+                                   int64_t cols, int64_t row_off, int map, uint64_t seed,
+                                   double sigma) {
+  const int64_t count = rows * cols;
+  const int64_t nblk = (count + 3) / 4;
+  for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < nblk;
+       n += (int64_t)gridDim.x * blockDim.x) {
+    uint64_t w0 = (uint64_t)n, w1 = (uint64_t)tensor_id, w2 = 0, w3 = 0;
+    philox4x64_10(w0, w1, w2, w3, seed, 0);
+    double z[4];
+    box_muller(w0, w1, z[0], z[1]);
+    box_muller(w2, w3, z[2], z[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t e = n * 4 + j;
+      if (e >= count) break;
+      const int64_t row = e / cols, col = e % cols;
+      const int64_t at = (map_row(row, map) + row_off) * cols + col;
+      const float v = (float)(sigma * z[j]);
+      if (is_bf16)
+        static_cast<__nv_bfloat16*>(dst)[at] = __float2bfloat16_rn(v);
+      else
+        static_cast<float*>(dst)[at] = v;
+    }
+  }
+}
+
+__global__ void gather_weight_kernel(const void* src, int is_bf16, int64_t cols, int64_t row_off,
+                                     int map, int64_t offset, int64_t count, float* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = offset + i;
+    const int64_t row = e / cols, col = e % cols;
+    const int64_t at = (map_row(row, map) + row_off) * cols + col;
+    out[i] = is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[at])
+                     : static_cast<const float*>(src)[at];
+  }
+}
+
+// (cos, sin) of pos * base^(-2i/D) for pos < Lmax, i < D/2; double precision.
+__global__ void rope_table_kernel(float2* tab, int Lmax, int D, double base) {
+  const int half = D / 2;
+  const int64_t total = (int64_t)Lmax * half;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int pos = (int)(e / half), i = (int)(e % half);
+    const double inv = pow(base, -(2.0 * i) / D);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    tab[e] = make_float2((float)c, (float)s);
+  }
+}
+
+// ---------------------------------------------------------------- activations
+template <bool BF16>
+__global__ void embed_kernel(const void* E, const int32_t* ids, int V, int d, float* x) {
+  const int m = blockIdx.x;
+  int id = ids[m];
+  id = id < 0 ? 0 : (id >= V ? V - 1 : id);
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    const size_t at = (size_t)id * d + k;
+    x[(size_t)m * d + k] = BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(E)[at])
+                                : static_cast<const float*>(E)[at];
+  }
+}
+
+// h = x / sqrt(mean(x^2) + eps), one CTA of 256 threads per row, fixed
+// summation order (a row's result does not depend on the other rows).
+template <bool BF16>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int d, float eps, void* out) {
+  const int m = blockIdx.x;
+  const float* xr = x + (size_t)m * d;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < d; k += 256) ss = fmaf(xr[k], xr[k], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float part[8];
+  __shared__ float inv_s;
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w];
+    inv_s = 1.f / sqrtf(t / (float)d + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  for (int k = threadIdx.x; k < d; k += 256) {
+    const float v = xr[k] * inv;
+    if (BF16)
+      static_cast<__nv_bfloat16*>(out)[(size_t)m * d + k] = __float2bfloat16_rn(v);
+    else
+      static_cast<float*>(out)[(size_t)m * d + k] = v;
+  }
+}
+
+// y[m][n] = sum_k x[m][k] W[n][k] in fp32: one warp per (n, m), lane-strided
+// partial sums merged by a fixed shuffle tree.
+__global__ void __launch_bounds__(256) linear_f32_kernel(const float* x, int ldx, const float* W,
+                                                         int N, int K, float* y, int ldy) {
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int m = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  const float* xr = x + (size_t)m * ldx;
+  const float* wr = W + (size_t)n * K;
+  float acc = 0.f;
+  for (int k = lane; k < K; k += 32) acc = fmaf(xr[k], wr[k], acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) y[(size_t)m * ldy + n] = acc;
+}
+
+// fp32 QKV epilogue: rotate-half RoPE on q and k heads, q to qb [T][Hq][D],
+// k and v to the caches [Hkv][Lmax][D] at positions P + m.
+__global__ void qkv_rope_f32_kernel(const float* y, int T, int Hq, int Hkv, int D, int Lmax,
+                                    const int32_t* kv_len, const float2* rope, float* qb,
+                                    float* kc, float* vc) {
+  const int Ntot = (Hq + 2 * Hkv) * D;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= T * Ntot) return;
+  const int m = e / Ntot, c = e % Ntot, h = c / D, d = c % D, half = D / 2;
+  int P = kv_len[0];
+  P = P < 0 ? 0 : (P > Lmax - T ? Lmax - T : P);
+  const float* yr = y + (size_t)m * Ntot + (size_t)h * D;
+  float v = yr[d];
+  if (h < Hq + Hkv) {
+    const float2 cs = rope[(size_t)(P + m) * half + (d % half)];
+    v = d < half ? v * cs.x - yr[d + half] * cs.y : v * cs.x + yr[d - half] * cs.y;
+  }
+  if (h < Hq)
+    qb[((size_t)m * Hq + h) * D + d] = v;
+  else if (h < Hq + Hkv)
+    kc[((size_t)(h - Hq) * Lmax + P + m) * D + d] = v;
+  else
+    vc[((size_t)(h - Hq - Hkv) * Lmax + P + m) * D + d] = v;
+}
+
+__global__ void swiglu_f32_kernel(const float* y, int T, int ffn, float* a) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= T * ffn) return;
+  const int m = e / ffn, j = e % ffn;
+  const float g = y[(size_t)m * 2 * ffn + j], u = y[(size_t)m * 2 * ffn + ffn + j];
+  a[e] = g / (1.f + expf(-g)) * u;
+}
+
+__global__ void resid_add_f32_kernel(float* x, const float* y, int n) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < n) x[e] += y[e];
+}
+
+// ---------------------------------------------------------------- decode state
+// A fresh draft block: slot 0 holds the pending token, slots 1..T-1 [MASK];
+// every slot masked, no draft yet.
+__global__ void block_init_kernel(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
+                                  int32_t last, int32_t mask_id) {
+  const int i = threadIdx.x;
+  if (i < T) {
+    block_in[i] = i == 0 ? last : mask_id;
+    draft[i] = -1;
+  }
+  if (i == 0) *mask = T >= 32 ? 0xffffffffu : ((1u << T) - 1u);
+}
+
+__global__ void set_token_kernel(int32_t* ids, int32_t tok) { ids[0] = tok; }
+
+__global__ void kv_add_kernel(int32_t* kv_len, int add) { kv_len[0] += add; }
+
+}  // namespace mk
+
+// ---------------------------------------------------------------- launchers
+static int grid_for(int64_t work, int threads) {
+  const int64_t cap = (int64_t)num_sms() * 16;
+  int64_t g = (work + threads - 1) / threads;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+ndiff_status launch_init_normal(void* dst, bool bf16, int tensor_id, int64_t rows, int64_t cols,
+                                int64_t row_off, int map, uint64_t seed, double sigma,
+                                cudaStream_t s) {
+  const int64_t nblk = (rows * cols + 3) / 4;
+  mk::init_normal_kernel<<<grid_for(nblk, 256), 256, 0, s>>>(dst, bf16 ? 1 : 0, tensor_id, rows,
+                                                             cols, row_off, map, seed, sigma);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int64_t row_off,
+                                  int map, int64_t offset, int64_t count, float* out,
+                                  cudaStream_t s) {
+  if (count <= 0) return NDIFF_OK;
+  mk::gather_weight_kernel<<<grid_for(count, 256), 256, 0, s>>>(src, bf16 ? 1 : 0, cols, row_off,
+                                                                map, offset, count, out);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaStream_t s) {
+  mk::rope_table_kernel<<<grid_for((int64_t)Lmax * (D / 2), 256), 256, 0, s>>>(tab, Lmax, D, base);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
+                          float* x, cudaStream_t s) {
+  if (bf16)
+    mk::embed_kernel<true><<<T, 256, 0, s>>>(E, ids, V, d, x);
+  else
+    mk::embed_kernel<false><<<T, 256, 0, s>>>(E, ids, V, d, x);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_rmsnorm(const float* x, int T, int d, float eps, void* out, bool bf16,
+                            cudaStream_t s) {
+  if (bf16)
+    mk::rmsnorm_kernel<true><<<T, 256, 0, s>>>(x, d, eps, out);
+  else
+    mk::rmsnorm_kernel<false><<<T, 256, 0, s>>>(x, d, eps, out);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_linear_f32(const float* x, int ldx, const float* W, int N, int K, float* y,
+                               int ldy, int T, cudaStream_t s) {
+  dim3 grid((N + 7) / 8, T);
+  mk::linear_f32_kernel<<<grid, 256, 0, s>>>(x, ldx, W, N, K, y, ldy);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_qkv_rope_f32(const float* y, int T, int Hq, int Hkv, int D, int Lmax,
+                                 const int32_t* kv_len, const float2* rope, float* qb, float* kc,
+                                 float* vc, cudaStream_t s) {
+  const int n = T * (Hq + 2 * Hkv) * D;
+  mk::qkv_rope_f32_kernel<<<(n + 255) / 256, 256, 0, s>>>(y, T, Hq, Hkv, D, Lmax, kv_len, rope,
+                                                          qb, kc, vc);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_swiglu_f32(const float* y, int T, int ffn, float* a, cudaStream_t s) {
+  const int n = T * ffn;
+  mk::swiglu_f32_kernel<<<(n + 255) / 256, 256, 0, s>>>(y, T, ffn, a);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t s) {
+  mk::resid_add_f32_kernel<<<(n + 255) / 256, 256, 0, s>>>(x, y, n);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
+                               int32_t last, int32_t mask_id, cudaStream_t s) {
+  mk::block_init_kernel<<<1, 32, 0, s>>>(block_in, draft, mask, T, last, mask_id);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s) {
+  mk::set_token_kernel<<<1, 1, 0, s>>>(ids, tok);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s) {
+  mk::kv_add_kernel<<<1, 1, 0, s>>>(kv_len, add);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
+}  // namespace ndiff

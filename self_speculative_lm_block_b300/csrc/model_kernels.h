@@ -1,0 +1,40 @@
+// model_kernels.h — host launchers of the model's small kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace ndiff {
+
+// Storage row of logical row r of a weight tensor: identity, or the 64-row
+// interleave of the bf16 SwiGLU weight (gate rows j -> (j/64)*128 + j%64,
+// up rows j -> (j/64)*128 + 64 + j%64) that puts a gate row and its up row in
+// the same 128-row GEMM tile.
+enum { ROWMAP_IDENTITY = 0, ROWMAP_GATE = 1, ROWMAP_UP = 2 };
+
+ndiff_status launch_init_normal(void* dst, bool bf16, int tensor_id, int64_t rows, int64_t cols,
+                                int64_t row_off, int map, uint64_t seed, double sigma,
+                                cudaStream_t s);
+ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int64_t row_off,
+                                  int map, int64_t offset, int64_t count, float* out,
+                                  cudaStream_t s);
+ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaStream_t s);
+ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
+                          float* x, cudaStream_t s);
+ndiff_status launch_rmsnorm(const float* x, int T, int d, float eps, void* out, bool bf16,
+                            cudaStream_t s);
+ndiff_status launch_linear_f32(const float* x, int ldx, const float* W, int N, int K, float* y,
+                               int ldy, int T, cudaStream_t s);
+ndiff_status launch_qkv_rope_f32(const float* y, int T, int Hq, int Hkv, int D, int Lmax,
+                                 const int32_t* kv_len, const float2* rope, float* qb, float* kc,
+                                 float* vc, cudaStream_t s);
+ndiff_status launch_swiglu_f32(const float* y, int T, int ffn, float* a, cudaStream_t s);
+ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t s);
+ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
+                               int32_t last, int32_t mask_id, cudaStream_t s);
+ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s);
+ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s);
+
+}  // namespace ndiff

@@ -59,6 +59,8 @@ _SIGS = {
     "ndiff_block_attn_split_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "ndiff_block_attn_noalloc": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "ndiff_logits_reduce": (_I, [_I, _P, _I, _I, _I64, _I, _P, _P, _P]),
+    "ndiff_gemm_bf16_workspace_size": (_SZ, [_I, _I, _I]),
+    "ndiff_gemm_bf16": (_I, [_P, _P, _I, _I, _I, _P, _I64, _P, _SZ, _P]),
     "ndiff_unmask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_verify_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.c_uint64, ctypes.POINTER(_P)]),
@@ -157,6 +159,15 @@ def ndiff_logits_reduce(dt, logits, R, V, ld, exclude_id, argmax, conf, stream=N
                  _ptr(conf), _stream(stream))
 
 
+def ndiff_gemm_bf16_workspace_size(M, N, K) -> int:
+    return _lib.ndiff_gemm_bf16_workspace_size(M, N, K)
+
+
+def ndiff_gemm_bf16(x, w, M, N, K, y, ldy, ws, ws_bytes, stream=None):
+    return _call("ndiff_gemm_bf16", _ptr(x), _ptr(w), M, N, K, _ptr(y), ldy, _ptr(ws), ws_bytes,
+                 _stream(stream))
+
+
 def ndiff_unmask(conf, pred, B, T, k, mask_bits, block_in, draft, chosen, stream=None):
     return _call("ndiff_unmask", _ptr(conf), _ptr(pred), B, T, k, _ptr(mask_bits), _ptr(block_in),
                  _ptr(draft), _ptr(chosen), _stream(stream))
@@ -229,3 +240,71 @@ def logits_reduce(logits: torch.Tensor, V: int | None = None, exclude_id: int = 
     conf = torch.empty(R, dtype=torch.float32, device=logits.device)
     ndiff_logits_reduce(dt, logits, R, V, ld, exclude_id, ids, conf, stream)
     return ids, conf
+
+
+def gemm_bf16(x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
+    """y = x @ w.T in fp32 for bf16 x [M<=32][K] and w [N][K] (device tensors)."""
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    need = ndiff_gemm_bf16_workspace_size(M, N, K)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ndiff_gemm_bf16(x, w, M, N, K, y, N, ws, need, stream)
+    return y
+
+
+class Model:
+    """Owner of an ndiff_model handle (thin wrapper over the C ABI)."""
+
+    def __init__(self, layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, dtype="f32",
+                 max_seq=4096, seed=0, rope_base=10000.0, eps=1e-6):
+        cfg = ModelConfig(layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab,
+                          NDIFF_BF16 if dtype == "bf16" else NDIFF_F32, rope_base, eps, max_seq, 1)
+        self.cfg = cfg
+        self.vocab = vocab
+        self.handle = ndiff_model_create(cfg, seed)
+        self.stats = Stats()
+
+    def close(self):
+        if self.handle:
+            ndiff_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, prompt):
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(prompt, dtype=np.int32))
+        ndiff_prefill(self.handle, arr.ctypes.data, int(arr.shape[0]))
+
+    def step(self, mode: int, steps: int = 1):
+        buf = (ctypes.c_int32 * 32)()
+        n = ndiff_decode_step(self.handle, mode, steps, ctypes.addressof(buf), self.stats)
+        return list(buf[:n])
+
+    def generate(self, mode: int, n_new: int, steps: int = 1):
+        out = []
+        while len(out) < n_new:
+            out.extend(self.step(mode, steps))
+        return out[:n_new]
+
+    def forward(self, ids, mode: int):
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        T = int(arr.shape[0])
+        logits = np.empty((T, self.vocab), dtype=np.float32)
+        ndiff_model_forward(self.handle, arr.ctypes.data, T, mode, logits.ctypes.data)
+        return logits
+
+    def state(self):
+        return ndiff_model_state(self.handle)
+
+    def read_weight(self, tensor_id: int, offset: int, count: int):
+        import numpy as np
+        out = np.empty(count, dtype=np.float32)
+        ndiff_model_read_weight(self.handle, tensor_id, offset, count, out.ctypes.data)
+        return out

@@ -1,0 +1,283 @@
+"""GPU parity of the model path (projections, weights, forward, decode modes)
+against the oracle, through the C ABI.
+
+Bars:
+- tcgen05 projection: |y - x.w| <= gamma_K * (|x|.|w|) + 1e-30 with
+  gamma_K = K u / (1 - K u), u = 2^-24 — the worst-case bound of any fp32
+  summation order of K products (the products of bf16 values are exact in fp32).
+- Weights: the Philox/Box-Muller stream is computed in double on both sides;
+  the float32 values agree except where the two libms' last-bit differences
+  cross a float32 rounding boundary (rare): at most 1 ulp there.
+- fp32 model logits: |err| <= 1e-4 * max|ref| (float32 arithmetic against the
+  float64 definition through a few layers of d <= 128 sums).
+- bf16 model logits: |err| <= 2e-2 + 2e-2 |ref|: the GPU and the oracle round
+  the same tensors to bf16, but the values before rounding differ in their
+  last fp32 bits and the attention probabilities go to the tensor cores as
+  bf16, so single activations can land one bf16 step (2^-8 relative) apart.
+- Tokens: compared up to the first divergence; a divergence is allowed only
+  where the oracle's top-2 logit gap is below 1e-3. GPU self-speculation
+  tokens equal GPU AR tokens exactly (every kernel computes a row
+  independently of the block length).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import decode as OD
+from oracle import model as OM
+from oracle import philox as OP
+from oracle.numerics import round_to_bf16
+from self_speculative_lm_block_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tiny_tokens.json")
+
+MID_BF16 = dict(layers=2, d_model=1024, n_heads=8, n_kv_heads=2, head_dim=128, ffn=2048,
+                vocab=4096, seed=77)
+
+
+@pytest.fixture(scope="module")
+def nd(cuda_ok):
+    from self_speculative_lm_block_b300 import ndiff
+    return ndiff
+
+
+def _ocfg(c, dtype):
+    return OM.Config(layers=c["layers"], d_model=c["d_model"], n_heads=c["n_heads"],
+                     n_kv_heads=c["n_kv_heads"], head_dim=c["head_dim"], ffn=c["ffn"],
+                     vocab=c["vocab"], dtype=dtype, seed=c["seed"])
+
+
+def _gpu_model(nd, c, dtype, max_seq=512):
+    return nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
+                    c["vocab"], dtype=dtype, max_seq=max_seq, seed=c["seed"])
+
+
+def _gap(logits_row, excl):
+    row = np.array(logits_row, dtype=np.float64)
+    row[excl] = -np.inf
+    top = np.sort(row)[-2:]
+    return float(top[1] - top[0])
+
+
+def _compare_tokens(got, ref, ref_gaps):
+    """Number of tokens compared; fails on a divergence at a gap >= 1e-3."""
+    for i, (a, b) in enumerate(zip(got, ref)):
+        if a != b:
+            assert ref_gaps is not None and ref_gaps[i] < 1e-3, \
+                f"token {i}: {a} != {b} (oracle top-2 gap {None if ref_gaps is None else ref_gaps[i]})"
+            return i
+    return min(len(got), len(ref))
+
+
+def _oracle_ar(cfg, w, prompt, n):
+    """Oracle AR tokens with the top-2 logit gap at each step."""
+    s = OM.Session(cfg, w, max_seq=len(prompt) + n + 40)
+    s.prefill(prompt)
+    toks, gaps = [], []
+    for _ in range(n):
+        logits = s.forward([s.last], OA.CAUSAL)
+        a = int(OD.logits_reduce(logits, exclude_id=cfg.mask_id)[0][0])
+        gaps.append(_gap(logits[0], cfg.mask_id))
+        s.kv_len += 1
+        s.last = a
+        toks.append(a)
+    return toks, gaps
+
+
+# ---------------------------------------------------------------- projection
+def _gemm_check(nd, M, N, K, seed):
+    x = synth.normal_bf16((M, K), 1.0, seed, 1)
+    w = synth.normal_bf16((N, K), 0.02, seed, 2)
+    y = nd.gemm_bf16(x.cuda(), w.cuda()).cpu().numpy().astype(np.float64)
+    xd, wd = x.double().numpy(), w.double().numpy()
+    ref = xd @ wd.T
+    u = 2.0 ** -24
+    gamma = K * u / (1 - K * u)
+    bound = gamma * (np.abs(xd) @ np.abs(wd).T) + 1e-30
+    assert (np.abs(y - ref) <= bound).all(), f"max excess {(np.abs(y - ref) - bound).max()}"
+    return x, w, y
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 300, 128), (32, 4096, 4096), (32, 1000, 12288),
+                                   (17, 6144, 4096), (2, 24576, 4096)])
+def test_gemm_bf16_within_fp32_bound(nd, M, N, K):
+    _gemm_check(nd, M, N, K, seed=M * 7 + N + K)
+
+
+def test_gemm_rows_do_not_depend_on_block(nd):
+    x, w, y = _gemm_check(nd, 32, 4096, 12288, seed=5)
+    for m in (0, 7, 31):
+        one = nd.gemm_bf16(x[m:m + 1].cuda(), w.cuda()).cpu().numpy()
+        assert np.array_equal(one[0], y[m].astype(np.float32)), m
+
+
+def test_gemm_lm_head_shape_sampled(nd):
+    M, N, K = 32, 151936, 4096
+    x = synth.normal_bf16((M, K), 1.0, 9, 1)
+    w = synth.normal_bf16((N, K), 0.02, 9, 2)
+    y = nd.gemm_bf16(x.cuda(), w.cuda()).cpu().numpy().astype(np.float64)
+    cols = np.random.default_rng(0).choice(N, 512, replace=False)
+    cols = np.concatenate([cols, [0, N - 1]])
+    xd, wd = x.double().numpy(), w[cols].double().numpy()
+    ref = xd @ wd.T
+    bound = K * 2.0 ** -24 / (1 - K * 2.0 ** -24) * (np.abs(xd) @ np.abs(wd).T)
+    assert (np.abs(y[:, cols] - ref) <= bound).all()
+
+
+def test_gemm_rejects_bad_shapes(nd):
+    x = torch.zeros((33, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nd.NdiffError):
+        nd.gemm_bf16(x, w)
+    with pytest.raises(nd.NdiffError):
+        nd.gemm_bf16(torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros((8, 96), dtype=torch.bfloat16, device="cuda"))
+
+
+# ---------------------------------------------------------------- weights
+@pytest.mark.parametrize("which", ["tiny", "mid"])
+def test_weights_follow_the_philox_stream(nd, which):
+    c, dtype = (synth.TINY, "f32") if which == "tiny" else (MID_BF16, "bf16")
+    m = _gpu_model(nd, c, dtype, max_seq=64)
+    cfg = _ocfg(c, dtype)
+    rng = np.random.default_rng(3)
+    n_mis, n_tot = 0, 0
+    for tid in [0, *range(1, 8), *range(9, 16), 1 + 8 * cfg.layers]:
+        rows, cols = OM.tensor_shape(cfg, tid)
+        for start in (0, int(rng.integers(0, rows * cols - 1000))):
+            got = m.read_weight(tid, start, 1000).astype(np.float64)
+            ref = OP.weight_values(cfg.seed, tid, start, 1000).astype(np.float64)
+            if dtype == "bf16":
+                ref = round_to_bf16(ref)
+            mis = got != ref
+            n_mis += int(mis.sum())
+            n_tot += got.size
+            if mis.any():
+                ulp = np.spacing(np.abs(ref[mis]).astype(np.float32)).astype(np.float64)
+                if dtype == "bf16":
+                    ulp = ulp * 65536.0
+                assert (np.abs(got[mis] - ref[mis]) <= ulp).all(), tid
+    assert n_mis <= max(2, n_tot // 10000)
+    m.close()
+
+
+# ---------------------------------------------------------------- tiny fp32 model
+def test_tiny_forward_logits_match_oracle(nd):
+    c = synth.TINY
+    cfg = _ocfg(c, "f32")
+    pr = synth.prompt(c["prompt"], c["vocab"], c["seed"])
+    blk = [int(pr[-1])] + [int(t) for t in synth.prompt(40, c["vocab"], 5)[:31]]
+    m = _gpu_model(nd, c, "f32", max_seq=128)
+    m.prefill(pr)
+    for mode in (OA.BIDIR, OA.CAUSAL):
+        got = m.forward(blk, mode)
+        s = OM.Session(cfg, max_seq=128)
+        s.prefill(pr)
+        ref = s.forward(blk, mode)
+        err = np.abs(got - ref).max()
+        assert err <= 1e-4 * np.abs(ref).max(), err
+    assert m.state() == (31, int(pr[-1]))  # forwards do not move the session
+    m.close()
+
+
+def test_tiny_tokens_match_oracle(nd):
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    c = synth.TINY
+    pr = synth.prompt(c["prompt"], c["vocab"], c["seed"])
+    assert g["prompt"] == [int(t) for t in pr]
+    cfg = _ocfg(c, "f32")
+    w = OM.Weights(cfg)
+    m = _gpu_model(nd, c, "f32", max_seq=200)
+    m.prefill(pr)
+    ar = m.generate(0, 64)
+    _, gaps = _oracle_ar(cfg, w, pr, 64)
+    assert _compare_tokens(ar, g["ar"], gaps) == 64
+    for key, mode, steps in (("diff_k4", 1, 8), ("selfspec_s1", 2, 1)):
+        m.prefill(pr)
+        toks = m.generate(mode, 64, steps)
+        if mode == 2:
+            assert _compare_tokens(toks, g[key], gaps) == 64
+        else:
+            assert toks == g[key], key
+    m.close()
+
+
+@pytest.mark.parametrize("steps", [1, 2, 4, 32])
+def test_tiny_selfspec_equals_ar_on_gpu(nd, steps):
+    c = synth.TINY
+    pr = synth.prompt(c["prompt"], c["vocab"], c["seed"])
+    m = _gpu_model(nd, c, "f32", max_seq=260)
+    m.prefill(pr)
+    ar = m.generate(0, 96)
+    m.prefill(pr)
+    m.stats = type(m.stats)()
+    ss = m.generate(2, 96, steps)
+    assert ss == ar
+    assert m.stats.tokens >= 96 and m.stats.forwards > 0
+    m.close()
+
+
+# ---------------------------------------------------------------- bf16 model
+def test_bf16_forward_logits_match_oracle(nd):
+    c = MID_BF16
+    cfg = _ocfg(c, "bf16")
+    w = OM.Weights(cfg)
+    pr = synth.prompt(40, c["vocab"], 11)
+    blk = [int(pr[-1])] + [int(t) for t in synth.prompt(31, c["vocab"], 12)]
+    m = _gpu_model(nd, c, "bf16", max_seq=128)
+    m.prefill(pr)
+    for mode in (OA.BIDIR, OA.CAUSAL):
+        got = m.forward(blk, mode)
+        s = OM.Session(cfg, w, max_seq=128)
+        s.prefill(pr)
+        ref = s.forward(blk, mode)
+        err = np.abs(got - ref)
+        tol = 2e-2 + 2e-2 * np.abs(ref)
+        print(f"mode {mode}: max |err| {err.max():.3e}, max |ref| {np.abs(ref).max():.3f}")
+        assert (err <= tol).all(), err.max()
+    m.close()
+
+
+def test_bf16_block_rows_equal_single_token_forwards(nd):
+    """A causal block forward gives bit-identical logits to AR steps: the
+    property that makes temperature-0 self-speculation reproduce AR."""
+    c = MID_BF16
+    pr = synth.prompt(50, c["vocab"], 13)
+    m = _gpu_model(nd, c, "bf16", max_seq=160)
+    m.prefill(pr)
+    ar = m.generate(0, 12)
+    m.prefill(pr)
+    blk = m.forward([int(pr[-1])] + ar[:11], OA.CAUSAL)
+    # replay the AR steps one by one and compare each row
+    m.prefill(pr)
+    for i in range(12):
+        one = m.forward([int(pr[-1]) if i == 0 else ar[i - 1]], OA.CAUSAL)
+        assert np.array_equal(one[0], blk[i]), i
+        m.step(0)
+    m.close()
+
+
+def test_bf16_selfspec_equals_ar_and_tracks_oracle(nd):
+    c = MID_BF16
+    cfg = _ocfg(c, "bf16")
+    pr = synth.prompt(64, c["vocab"], 14)
+    m = _gpu_model(nd, c, "bf16", max_seq=256)
+    m.prefill(pr)
+    ar = m.generate(0, 64)
+    for steps in (1, 4):
+        m.prefill(pr)
+        assert m.generate(2, 64, steps) == ar
+    m.prefill(pr)
+    diff = m.generate(1, 64, 2)
+    assert len(diff) == 64 and all(0 <= t < c["vocab"] - 1 for t in diff)
+    ref, gaps = _oracle_ar(cfg, OM.Weights(cfg), pr, 24)
+    n = _compare_tokens(ar[:24], ref, gaps)
+    print(f"GPU AR tokens compared with the oracle: {n} of 24")
+    m.close()
