@@ -12,6 +12,7 @@
 
 namespace {
 thread_local char g_last_error[512] = "";
+thread_local bool g_pdl = false;
 __device__ unsigned int g_status_word;
 
 struct DeviceCache {
@@ -23,6 +24,10 @@ std::mutex g_dev_mu;
 }  // namespace
 
 namespace ndiff {
+
+bool pdl_enabled() { return g_pdl; }
+PdlScope::PdlScope(bool on) : prev(g_pdl) { g_pdl = on; }
+PdlScope::~PdlScope() { g_pdl = prev; }
 
 ndiff_status set_error(ndiff_status s, const char* fmt, ...) {
   va_list ap;

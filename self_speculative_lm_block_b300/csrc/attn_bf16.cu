@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  griddep_wait();
   int P = p.kv_len[b];
   P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
   const int nkeys = P + p.T;
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
   const uint32_t tmem = *tmem_slot;
 
   uint8_t* sQ = smem + OFF_Q;
@@ -382,6 +384,8 @@ __global__ void __launch_bounds__(128)
   const int g = blockIdx.y, b = blockIdx.z;
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  griddep_launch();
+  griddep_wait();
   if (r >= p.G * p.T) return;
   int P = p.kv_len[b];
   P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
@@ -490,12 +494,11 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
     attr_set[dev] = true;
   }
   dim3 grid(nsplit, Hkv, B);
-  attn::attn_bf16_kernel<<<grid, attn::THREADS, attn::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(attn::attn_bf16_kernel, grid, dim3(attn::THREADS),
+                          (size_t)attn::SMEM_BYTES, stream, tq, tk, tv, prm));
   if (nsplit > 1) {
     dim3 g2((G * T + 3) / 4, Hkv, B);
-    attn::attn_combine_kernel<<<g2, 128, 0, stream>>>(prm);
-    NDIFF_CUDA_TRY(cudaGetLastError());
+    NDIFF_CUDA_TRY(launch_k(attn::attn_combine_kernel, g2, dim3(128), 0, stream, prm));
   }
   return NDIFF_OK;
 }

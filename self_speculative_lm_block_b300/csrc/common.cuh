@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/ndiff.h"
 
 namespace ndiff {
@@ -26,6 +28,19 @@ constexpr unsigned int kStatusTimeout = 1u;
 // Expiry of bounded device waits, in nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Programmatic dependent launch. Kernels of the model's forward are launched
+// with programmatic stream serialization while a PdlScope is alive on the
+// calling thread; such a kernel may start before its predecessor in the stream
+// has finished, so every kernel calls griddep_wait() before it reads data that
+// an earlier kernel wrote or writes data that an earlier kernel reads. Without
+// the launch attribute griddep_wait() returns at once.
+bool pdl_enabled();
+struct PdlScope {
+  explicit PdlScope(bool on);
+  ~PdlScope();
+  bool prev;
+};
+
 #define NDIFF_CUDA_TRY(expr)                                           \
   do {                                                                 \
     cudaError_t _e = (expr);                                           \
@@ -39,6 +54,11 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -260,5 +280,25 @@ EncodeTiledFn encode_tiled_fn();
 // bf16 tensor map of rank 2..3, 128-byte swizzle, zero fill out of bounds.
 ndiff_status make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides_bytes, const uint32_t* box);
+
+// Launches `kernel` on `stream`, with programmatic stream serialization when
+// a PdlScope is active on this thread.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace ndiff

@@ -15,19 +15,27 @@
 // columns of TMEM):
 //   * Work items are (128-row tile of W, K split). A persistent grid of at most
 //     one CTA per SM walks the items round-robin. Warp 0 streams 128x64 weight
-//     tiles and the matching 32x64 activation tile through an 8-stage TMA ring
+//     tiles and the matching 32x64 activation tile through a 5-stage TMA ring
 //     (128-byte swizzle); warp 1 issues tcgen05.mma (M128 N32 K16) into one of
 //     two TMEM accumulators; warps 2-5 drain the other accumulator, so the
 //     epilogue of one item overlaps the loads of the next.
+//   * About 100 KB of shared memory per CTA, so two CTAs fit on an SM: under
+//     programmatic dependent launch the next projection's CTAs start next to
+//     the running ones and stream their first weight tiles (which no earlier
+//     kernel writes) before griddepcontrol.wait; the activation tiles and every
+//     global write come after it.
 //   * K splits: every split writes its fp32 partial tile to the workspace and
 //     bumps a per-tile counter; the last split to arrive adds the partials in
 //     split order 0..S-1 and runs the fused epilogue, then resets the counter.
 //     The split boundaries depend only on (N, K, SM count), never on the number
 //     of token rows, and the MMA column count is always 32, so a token row's
 //     result is the same whether it is computed alone (AR) or inside a block.
-//   * Fused epilogues: fp32 store (logits), residual add (x += y), SwiGLU over
-//     interleaved 64-row gate/up groups, and QKV with rotate-half RoPE from a
-//     precomputed table plus the K/V-cache write at the block's positions.
+//   * Fused epilogues: fp32 store (logits), residual add (x += y), SwiGLU and
+//     QKV with rotate-half RoPE from a precomputed table plus the K/V-cache
+//     write at the block's positions. The weights are stored so that the two
+//     rows an epilogue combines are adjacent (gate j / up j; RoPE dims i / i+64
+//     of a q or k head), i.e. held by neighbouring lanes, and one warp shuffle
+//     brings them together.
 //   * Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 //     the device status word, lets issued TMA copies land, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -41,20 +49,19 @@ namespace gemm {
 constexpr int BM = 128;                    // weight rows per tile (MMA M)
 constexpr int BK = 64;                     // K per stage (one 128-byte swizzle atom)
 constexpr int MT = 32;                     // token rows (MMA N)
-constexpr int NST = 8;                     // pipeline stages
+constexpr int NST = 5;                     // pipeline stages
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_BYTES = MT * BK * 2;       // 4 KB
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NST * A_BYTES;
-constexpr int OFF_X = OFF_B + NST * B_BYTES;         // epilogue exchange [128][33] fp32
-constexpr int X_STRIDE = MT + 1;
-constexpr int OFF_BAR = OFF_X + BM * X_STRIDE * 4;
+constexpr int OFF_BAR = OFF_B + NST * B_BYTES;
 constexpr int N_BARS = 2 * NST + 4 + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
 constexpr int TMEM_COLS = 64;              // two 32-column accumulators
 constexpr int THREADS = 192;
 
-static_assert(OFF_B % 1024 == 0 && OFF_X % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_B % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(2 * SMEM_BYTES <= 227 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ bool bar_and(bool pred) {
   uint32_t r;
@@ -84,10 +91,10 @@ __device__ __forceinline__ void split_range(int s, int S, int nks, int& lo, int&
   hi = (int)(((long long)(s + 1) * nks) / S);
 }
 
-// Epilogue of one finished 128-row tile. Thread r holds y[m] for weight row
-// tile*128 + r and token rows m < T.
-__device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[MT],
-                                         float* xch) {
+// Epilogue of one finished 128-row tile. Thread r holds y[m] for storage row
+// tile*128 + r and token rows m < T. Loads are issued before stores so that
+// the 32 token rows do not serialise on memory latency.
+__device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[MT]) {
   const int n = tile * BM + r;
   switch (p.mode) {
     case GEMM_EPI_F32: {
@@ -100,56 +107,66 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, f
     }
     case GEMM_EPI_RESID: {
       if (n < p.N) {
+        float old[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) old[m] = (m < p.T) ? p.out[(size_t)m * p.ldo + n] : 0.f;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-          if (m < p.T) p.out[(size_t)m * p.ldo + n] += v[m];
+          if (m < p.T) p.out[(size_t)m * p.ldo + n] = old[m] + v[m];
       }
       break;
     }
     case GEMM_EPI_SWIGLU: {
-      // rows [0,64) of the tile are gate rows j, rows [64,128) the up rows of the same j
+      // even rows: gate j = tile*64 + r/2; odd rows: up of the same j
 #pragma unroll
-      for (int m = 0; m < MT; ++m) xch[r * X_STRIDE + m] = v[m];
-      bar_sync128();
-      if (r < 64) {
-        const int j = tile * 64 + r;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < p.T) {
-            const float g = v[m];
-            const float u = xch[(r + 64) * X_STRIDE + m];
-            p.act[(size_t)m * p.lda + j] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
-          }
+      for (int m = 0; m < MT; ++m) {
+        const float u = __shfl_xor_sync(0xffffffffu, v[m], 1);
+        if (!(r & 1) && m < p.T) {
+          const float g = v[m];
+          p.act[(size_t)m * p.lda + tile * 64 + (r >> 1)] =
+              __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
         }
       }
       break;
     }
     case GEMM_EPI_QKV: {
-      // tile = one head of 128 dims: q heads, then k heads, then v heads
-#pragma unroll
-      for (int m = 0; m < MT; ++m) xch[r * X_STRIDE + m] = v[m];
-      bar_sync128();
+      // tile = one head: q heads, then k heads, then v heads. In q and k heads
+      // even rows hold dim i = r/2 and odd rows dim i + 64 (the RoPE pair).
       int P = p.kv_len[0];
       P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
       const int h = tile;
       const bool rot = h < p.Hq + p.Hkv;
-      const int pr = r ^ 64;
-      const float sgn = r < 64 ? -1.f : 1.f;
+      const int i = r >> 1;
+      const int dim = rot ? ((r & 1) ? i + 64 : i) : r;
+      float pv[MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m < p.T) {
-          float y = v[m];
-          if (rot) {
-            const float2 cs = p.rope[(size_t)(P + m) * 64 + (r & 63)];
-            y = y * cs.x + sgn * xch[pr * X_STRIDE + m] * cs.y;
-          }
-          const __nv_bfloat16 o = __float2bfloat16_rn(y);
-          if (h < p.Hq) {
-            p.q[((size_t)m * p.Hq + h) * BM + r] = o;
-          } else if (h < p.Hq + p.Hkv) {
-            p.kc[((size_t)(h - p.Hq) * p.Lmax + P + m) * BM + r] = o;
-          } else {
-            p.vc[((size_t)(h - p.Hq - p.Hkv) * p.Lmax + P + m) * BM + r] = o;
+      for (int m = 0; m < MT; ++m) pv[m] = __shfl_xor_sync(0xffffffffu, v[m], 1);
+      __nv_bfloat16* dst;
+      size_t mstride;
+      if (h < p.Hq) {
+        dst = p.q + (size_t)h * BM + dim;
+        mstride = (size_t)p.Hq * BM;
+      } else if (h < p.Hq + p.Hkv) {
+        dst = p.kc + ((size_t)(h - p.Hq) * p.Lmax + P) * BM + dim;
+        mstride = BM;
+      } else {
+        dst = p.vc + ((size_t)(h - p.Hq - p.Hkv) * p.Lmax + P) * BM + dim;
+        mstride = BM;
+      }
+#pragma unroll
+      for (int m0 = 0; m0 < MT; m0 += 8) {
+        float2 cs[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          cs[j] = (rot && m0 + j < p.T) ? __ldg(p.rope + (size_t)(P + m0 + j) * 64 + i)
+                                        : make_float2(1.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = m0 + j;
+          if (m < p.T) {
+            float y = v[m];
+            if (rot) y = (r & 1) ? y * cs[j].x + pv[m] * cs[j].y : y * cs[j].x - pv[m] * cs[j].y;
+            dst[(size_t)m * mstride] = __float2bfloat16_rn(y);
           }
         }
       }
@@ -160,7 +177,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, f
   }
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -168,7 +185,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem + OFF_A;
   uint8_t* sB = smem + OFF_B;
-  float* xch = reinterpret_cast<float*>(smem + OFF_X);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = full + NST;
@@ -205,12 +221,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch();
   const uint32_t tmem = *tmem_slot;
   const int grid = gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // Weight tiles of the first NST steps go out before the wait for the
+      // previous kernel (no kernel writes weights); activation tiles after it.
+      int npre = 0;
+      for (int it = blockIdx.x; npre < NST && it < p.items; it += grid) {
+        const int tile = it / p.S;
+        int lo, hi;
+        split_range(it % p.S, p.S, p.nks, lo, hi);
+        for (int ks = lo; ks < hi && npre < NST; ++ks, ++npre) {
+          mbar_arrive_expect_tx(&full[npre], A_BYTES + B_BYTES);
+          tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], ks * BK, tile * BM);
+        }
+      }
+      griddep_wait();
       int kc = 0;
       bool ok = true;
       for (int it = blockIdx.x; ok && it < p.items; it += grid) {
@@ -219,12 +249,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         split_range(s, p.S, p.nks, lo, hi);
         for (int ks = lo; ks < hi; ++ks) {
           const int st = kc % NST;
-          if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
+          if (kc >= npre) {
+            if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
+            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
           }
-          mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
-          tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
           tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
           ++kc;
         }
@@ -281,6 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = quarter * 32 + lane;
     const int tid = threadIdx.x - 64;
     const uint32_t tl = tmem + ((quarter * 32u) << 16);
+    griddep_wait();
     int ic = 0;
     for (int it = blockIdx.x; it < p.items; it += grid, ++ic) {
       const int buf = ic & 1;
@@ -295,29 +328,47 @@ __global__ void __launch_bounds__(THREADS, 1)
 
       const int tile = it / p.S, s = it % p.S;
       if (p.S > 1) {
-        float* part = p.ws + (size_t)it * (MT * BM);
+        // partial tile layout [item][row r][32 token rows]: 16-byte stores per thread
+        float4* part = reinterpret_cast<float4*>(p.ws + ((size_t)it * BM + r) * MT);
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (m < p.T) __stcg(part + m * BM + r, v[m]);
+        for (int c = 0; c < MT / 4; ++c)
+          if (c * 4 < p.T)
+            __stcg(part + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
         __threadfence();
         bar_sync128();
         if (tid == 0) *last_flag = (atomicAdd(&p.counters[tile], 1) == p.S - 1) ? 1 : 0;
         bar_sync128();
         if (!*last_flag) continue;
         __threadfence();
+        // sum the splits in order 0..S-1; every split's loads are issued together
+        float acc[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < p.T) {
-            float acc = 0.f;
-            for (int s2 = 0; s2 < p.S; ++s2)
-              acc += (s2 == s) ? v[m]
-                               : __ldcg(p.ws + ((size_t)(tile * p.S + s2) * MT + m) * BM + r);
-            v[m] = acc;
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int s2 = 0; s2 < p.S; ++s2) {
+          if (s2 == s) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] += v[m];
+            continue;
+          }
+          const float4* src =
+              reinterpret_cast<const float4*>(p.ws + ((size_t)(tile * p.S + s2) * BM + r) * MT);
+          float4 t[MT / 4];
+#pragma unroll
+          for (int c = 0; c < MT / 4; ++c)
+            t[c] = (c * 4 < p.T) ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < MT / 4; ++c) {
+            acc[4 * c] += t[c].x;
+            acc[4 * c + 1] += t[c].y;
+            acc[4 * c + 2] += t[c].z;
+            acc[4 * c + 3] += t[c].w;
           }
         }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = acc[m];
         if (tid == 0) p.counters[tile] = 0;
       }
-      epilogue(p, tile, r, v, xch);
+      epilogue(p, tile, r, v);
     }
   }
 
@@ -396,8 +447,8 @@ ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, co
   p.nks = pl.nks;
   p.items = pl.items;
   p.status = device_status_word();
-  gemm::gemm_bf16_kernel<<<pl.grid, gemm::THREADS, gemm::SMEM_BYTES, stream>>>(tmW, tmX, p);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel, dim3(pl.grid), dim3(gemm::THREADS),
+                          (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
   return NDIFF_OK;
 }
 

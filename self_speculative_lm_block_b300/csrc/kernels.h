@@ -44,7 +44,7 @@ enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV =
 struct GemmParams {
   int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
   int S, nks, items;       // K splits, 64-wide K steps, work items (set by the launcher)
-  float* ws;               // split partials [items][32][128] fp32 (S > 1)
+  float* ws;               // split partials [items][128][32] fp32 (S > 1)
   int* counters;           // [tiles] arrival counters, zero between launches
   unsigned int* status;    // device status word
   float* out;              // F32: out[m*ldo + n] = y; RESID: out[m*ldo + n] += y

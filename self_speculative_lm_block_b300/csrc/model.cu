@@ -29,6 +29,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <map>
 #include <vector>
 
 #include "common.cuh"
@@ -101,6 +102,9 @@ struct ndiff_model {
   CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
   int32_t* pin = nullptr;       // pinned host staging [64]
+  int32_t* last_dev = nullptr;  // [1] pending last token (device copy of `last`)
+  cudaStream_t ms = nullptr;    // the model's own stream (decode graphs run here)
+  std::map<int, cudaGraphExec_t> graphs;  // decode cycles by (mode, steps)
   std::vector<void*> allocs;
   int P = 0;
   int32_t last = -1;
@@ -131,6 +135,10 @@ ndiff_status dalloc_t(ndiff_model* m, Tp** p, size_t bytes) {
 }
 
 void free_model(ndiff_model* m) {
+  for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  m->graphs.clear();
+  if (m->ms) cudaStreamDestroy(m->ms);
+  m->ms = nullptr;
   for (void* p : m->allocs) cudaFree(p);
   m->allocs.clear();
   if (m->pin) cudaFreeHost(m->pin);
@@ -173,6 +181,7 @@ ndiff_status check_config(const ndiff_model_config* c) {
 // in m->logits and the argmax / confidence of every row in m->pred / m->conf.
 ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool want_logits,
                      cudaStream_t s) {
+  PdlScope pdl(m->bf16);
   const float scale = 1.f / sqrtf((float)m->D);
   TRY(launch_embed(m->embed, m->bf16, ids, T, m->V, m->d, m->x, s));
   GemmParams gp;
@@ -259,11 +268,58 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool
 // each fixing the k = 32/steps most confident masked slots.
 ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
   const int k = kBlock / steps;
-  TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last, m->mask_id, s));
+  TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev, m->mask_id, s));
   for (int i = 0; i < steps; ++i) {
     TRY(forward(m, m->block_in, kBlock, 0, true, s));
     TRY(launch_unmask(m->conf, m->pred, 1, kBlock, k, m->mask, m->block_in, m->draft, m->chosen, s));
   }
+  return NDIFF_OK;
+}
+
+// Enqueues one decode cycle; every input it reads (pending token, committed
+// prefix) lives on the device, so the same launches can be replayed.
+ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStream_t s) {
+  if (mode == NDIFF_MODE_AR) {
+    // AR: one causal forward of [last]; commit its argmax.
+    TRY(forward(m, m->last_dev, 1, 1, true, s));
+    return launch_commit(m->pred, nullptr, 1, 1, m->last_dev, m->kv_len, s);
+  }
+  TRY(draft_block(m, steps, s));
+  if (mode == NDIFF_MODE_DIFF) {
+    // the finished block enters the cache through one bidirectional forward
+    TRY(forward(m, m->block_in, kBlock, 0, false, s));
+    return launch_commit(m->draft, nullptr, kBlock, kBlock, m->last_dev, m->kv_len, s);
+  }
+  // SELFSPEC: causal verification of [last, d0..d30], accept the agreeing prefix
+  TRY(forward(m, m->block_in, kBlock, 1, true, s));
+  TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->res + 33, m->res, m->res + 32, m->kv_len,
+                           s));
+  return launch_commit(m->res, m->res + 32, 0, 0, m->last_dev, m->kv_len, s);
+}
+
+// The decode cycle as an instantiated CUDA graph (captured on first use).
+ndiff_status cycle_graph(ndiff_model* m, ndiff_mode mode, int steps, cudaGraphExec_t* out) {
+  const int key = (int)mode * 64 + (mode == NDIFF_MODE_AR ? 0 : steps);
+  auto it = m->graphs.find(key);
+  if (it != m->graphs.end()) {
+    *out = it->second;
+    return NDIFF_OK;
+  }
+  NDIFF_CUDA_TRY(cudaStreamBeginCapture(m->ms, cudaStreamCaptureModeThreadLocal));
+  ndiff_status st = enqueue_cycle(m, mode, steps, m->ms);
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(m->ms, &g);
+  if (st != NDIFF_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (e != cudaSuccess) return cuda_error(e, "cudaStreamEndCapture");
+  cudaGraphExec_t ge = nullptr;
+  e = cudaGraphInstantiate(&ge, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGraphInstantiate");
+  m->graphs[key] = ge;
+  *out = ge;
   return NDIFF_OK;
 }
 
@@ -351,9 +407,12 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(dalloc_t(m, &m->mask, 16));
   TRY(dalloc_t(m, &m->chosen, kBlock * 4));
   TRY(dalloc_t(m, &m->prompt, (size_t)m->Lmax * 4));
+  TRY(dalloc_t(m, &m->last_dev, 16));
   TRY(dalloc_t(m, &m->rope, (size_t)m->Lmax * (m->D / 2) * sizeof(float2)));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, kBlock * 4, s));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, 16, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->last_dev, 0, 16, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->block_in, 0, kBlock * 4, s));
 
   if (m->bf16) {
     m->pl_qkv = gemm_plan(m->NQKV, m->d);
@@ -394,8 +453,9 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
     const int64_t kvr = (int64_t)m->Hkv * m->D;
-    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 0), m->HD, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
-    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 1), kvr, m->d, m->HD, ROWMAP_IDENTITY, seed, kSigma, s));
+    const int qk_map = b ? ROWMAP_ROPE : ROWMAP_IDENTITY;
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 0), m->HD, m->d, 0, qk_map, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 1), kvr, m->d, m->HD, qk_map, seed, kSigma, s));
     TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 2), kvr, m->d, m->HD + kvr, ROWMAP_IDENTITY, seed,
                            kSigma, s));
     TRY(launch_init_normal(ly.wo, b, tid_layer(l, 3), m->d, m->HD, 0, ROWMAP_IDENTITY, seed, kSigma, s));
@@ -413,7 +473,14 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     m->pin = nullptr;
     return set_error(NDIFF_ERR_OOM, "ndiff_model_create: pinned host buffer: %s", cudaGetErrorString(e));
   }
+  NDIFF_CUDA_TRY(cudaStreamCreateWithFlags(&m->ms, cudaStreamNonBlocking));
   NDIFF_CUDA_TRY(cudaStreamSynchronize(s));
+  // One forward of each block length sets every kernel attribute and device
+  // lookup up front, so that later graph captures only record launches. The
+  // cache rows it writes are scratch until a prefill fills them.
+  TRY(forward(m, m->ids, 1, 1, true, m->ms));
+  TRY(forward(m, m->block_in, kBlock, 0, true, m->ms));
+  TRY(finish(m->ms));
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
 }
@@ -434,8 +501,14 @@ bool locate(const ndiff_model* m, int tid, const void** base, int64_t* rows, int
   const Layer& ly = m->layers[l];
   const int64_t kvr = (int64_t)m->Hkv * m->D;
   switch (j) {
-    case 0: *base = ly.wqkv; *rows = m->HD; *cols = m->d; return true;
-    case 1: *base = ly.wqkv; *rows = kvr; *cols = m->d; *row_off = m->HD; return true;
+    case 0:
+      *base = ly.wqkv; *rows = m->HD; *cols = m->d;
+      if (m->bf16) *map = ROWMAP_ROPE;
+      return true;
+    case 1:
+      *base = ly.wqkv; *rows = kvr; *cols = m->d; *row_off = m->HD;
+      if (m->bf16) *map = ROWMAP_ROPE;
+      return true;
     case 2: *base = ly.wqkv; *rows = kvr; *cols = m->d; *row_off = m->HD + kvr; return true;
     case 3: *base = ly.wo; *rows = m->d; *cols = m->HD; return true;
     case 4:
@@ -496,6 +569,8 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cu
     TRY(forward(m, m->prompt + off, T, 1, false, stream));
     TRY(launch_kv_add(m->kv_len, T, stream));
   }
+  m->pin[0] = prompt_host[n - 1];
+  NDIFF_CUDA_TRY(cudaMemcpyAsync(m->last_dev, m->pin, 4, cudaMemcpyHostToDevice, stream));
   TRY(finish(stream));
   m->P = n - 1;
   m->last = prompt_host[n - 1];
@@ -517,32 +592,26 @@ ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32
   if (m->P + need > m->Lmax)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)", m->P, m->Lmax);
   TRY(set_device(m));
+  // the cycle runs on the model's stream, after the caller's earlier work
+  NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
+  cudaGraphExec_t ge = nullptr;
+  TRY(cycle_graph(m, mode, steps, &ge));
+  NDIFF_CUDA_TRY(cudaGraphLaunch(ge, m->ms));
   int n = 0, L = -1;
   int64_t forwards = 0;
   if (mode == NDIFF_MODE_AR) {
-    TRY(launch_set_token(m->ids, m->last, stream));
-    TRY(forward(m, m->ids, 1, 1, true, stream));
-    TRY(launch_kv_add(m->kv_len, 1, stream));
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, 4, cudaMemcpyDeviceToHost, stream));
-    TRY(finish(stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, 4, cudaMemcpyDeviceToHost, m->ms));
+    TRY(finish(m->ms));
     n = 1;
     forwards = 1;
   } else if (mode == NDIFF_MODE_DIFF) {
-    TRY(draft_block(m, steps, stream));
-    TRY(forward(m, m->block_in, kBlock, 0, false, stream));
-    TRY(launch_kv_add(m->kv_len, kBlock, stream));
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, kBlock * 4, cudaMemcpyDeviceToHost, stream));
-    TRY(finish(stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, kBlock * 4, cudaMemcpyDeviceToHost, m->ms));
+    TRY(finish(m->ms));
     n = kBlock;
     forwards = steps + 1;
   } else {
-    TRY(draft_block(m, steps, stream));
-    TRY(forward(m, m->block_in, kBlock, 1, true, stream));
-    int32_t* commit = m->res;
-    TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->res + 33, commit, m->res + 32,
-                             m->kv_len, stream));
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, 34 * 4, cudaMemcpyDeviceToHost, stream));
-    TRY(finish(stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, 34 * 4, cudaMemcpyDeviceToHost, m->ms));
+    TRY(finish(m->ms));
     n = m->pin[32];
     L = m->pin[33];
     forwards = steps + 1;

@@ -55,8 +55,12 @@ __device__ __forceinline__ void box_muller(uint64_t wa, uint64_t wb, double& z0,
 }
 
 __device__ __forceinline__ int64_t map_row(int64_t row, int map) {
-  if (map == ROWMAP_GATE) return (row / 64) * 128 + (row % 64);
-  if (map == ROWMAP_UP) return (row / 64) * 128 + 64 + (row % 64);
+  if (map == ROWMAP_GATE) return (row / 64) * 128 + 2 * (row % 64);
+  if (map == ROWMAP_UP) return (row / 64) * 128 + 2 * (row % 64) + 1;
+  if (map == ROWMAP_ROPE) {
+    const int64_t i = row % 128;
+    return (row / 128) * 128 + (i < 64 ? 2 * i : 2 * (i - 64) + 1);
+  }
   return row;
 }
 
@@ -116,6 +120,8 @@ __global__ void rope_table_kernel(float2* tab, int Lmax, int D, double base) {
 // ---------------------------------------------------------------- activations
 template <bool BF16>
 __global__ void embed_kernel(const void* E, const int32_t* ids, int V, int d, float* x) {
+  griddep_launch();
+  griddep_wait();
   const int m = blockIdx.x;
   int id = ids[m];
   id = id < 0 ? 0 : (id >= V ? V - 1 : id);
@@ -130,6 +136,8 @@ __global__ void embed_kernel(const void* E, const int32_t* ids, int V, int d, fl
 // summation order (a row's result does not depend on the other rows).
 template <bool BF16>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int d, float eps, void* out) {
+  griddep_launch();
+  griddep_wait();
   const int m = blockIdx.x;
   const float* xr = x + (size_t)m * d;
   float ss = 0.f;
@@ -160,6 +168,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int d, flo
 // partial sums merged by a fixed shuffle tree.
 __global__ void __launch_bounds__(256) linear_f32_kernel(const float* x, int ldx, const float* W,
                                                          int N, int K, float* y, int ldy) {
+  griddep_launch();
+  griddep_wait();
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int m = blockIdx.y;
   const int lane = threadIdx.x & 31;
@@ -178,6 +188,8 @@ __global__ void __launch_bounds__(256) linear_f32_kernel(const float* x, int ldx
 __global__ void qkv_rope_f32_kernel(const float* y, int T, int Hq, int Hkv, int D, int Lmax,
                                     const int32_t* kv_len, const float2* rope, float* qb,
                                     float* kc, float* vc) {
+  griddep_launch();
+  griddep_wait();
   const int Ntot = (Hq + 2 * Hkv) * D;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= T * Ntot) return;
@@ -199,6 +211,8 @@ __global__ void qkv_rope_f32_kernel(const float* y, int T, int Hq, int Hkv, int 
 }
 
 __global__ void swiglu_f32_kernel(const float* y, int T, int ffn, float* a) {
+  griddep_launch();
+  griddep_wait();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= T * ffn) return;
   const int m = e / ffn, j = e % ffn;
@@ -207,6 +221,8 @@ __global__ void swiglu_f32_kernel(const float* y, int T, int ffn, float* a) {
 }
 
 __global__ void resid_add_f32_kernel(float* x, const float* y, int n) {
+  griddep_launch();
+  griddep_wait();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < n) x[e] += y[e];
 }
@@ -215,18 +231,40 @@ __global__ void resid_add_f32_kernel(float* x, const float* y, int n) {
 // A fresh draft block: slot 0 holds the pending token, slots 1..T-1 [MASK];
 // every slot masked, no draft yet.
 __global__ void block_init_kernel(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
-                                  int32_t last, int32_t mask_id) {
+                                  const int32_t* last, int32_t mask_id) {
+  griddep_launch();
+  griddep_wait();
   const int i = threadIdx.x;
   if (i < T) {
-    block_in[i] = i == 0 ? last : mask_id;
+    block_in[i] = i == 0 ? last[0] : mask_id;
     draft[i] = -1;
   }
   if (i == 0) *mask = T >= 32 ? 0xffffffffu : ((1u << T) - 1u);
 }
 
-__global__ void set_token_kernel(int32_t* ids, int32_t tok) { ids[0] = tok; }
+// End of a decode cycle: the pending token becomes the last committed one
+// (tokens[n-1], n = *n_ptr or n_const) and the committed prefix grows by
+// kv_add (0 when verification has already advanced it).
+__global__ void commit_kernel(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
+                              int32_t* last, int32_t* kv_len) {
+  griddep_launch();
+  griddep_wait();
+  const int n = n_ptr ? *n_ptr : n_const;
+  last[0] = tokens[n > 0 ? n - 1 : 0];
+  kv_len[0] += kv_add;
+}
 
-__global__ void kv_add_kernel(int32_t* kv_len, int add) { kv_len[0] += add; }
+__global__ void set_token_kernel(int32_t* ids, int32_t tok) {
+  griddep_launch();
+  griddep_wait();
+  ids[0] = tok;
+}
+
+__global__ void kv_add_kernel(int32_t* kv_len, int add) {
+  griddep_launch();
+  griddep_wait();
+  kv_len[0] += add;
+}
 
 }  // namespace mk
 
@@ -267,20 +305,18 @@ ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaSt
 ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
                           float* x, cudaStream_t s) {
   if (bf16)
-    mk::embed_kernel<true><<<T, 256, 0, s>>>(E, ids, V, d, x);
+    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<true>, dim3(T), dim3(256), 0, s, E, ids, V, d, x));
   else
-    mk::embed_kernel<false><<<T, 256, 0, s>>>(E, ids, V, d, x);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<false>, dim3(T), dim3(256), 0, s, E, ids, V, d, x));
   return NDIFF_OK;
 }
 
 ndiff_status launch_rmsnorm(const float* x, int T, int d, float eps, void* out, bool bf16,
                             cudaStream_t s) {
   if (bf16)
-    mk::rmsnorm_kernel<true><<<T, 256, 0, s>>>(x, d, eps, out);
+    NDIFF_CUDA_TRY(launch_k(mk::rmsnorm_kernel<true>, dim3(T), dim3(256), 0, s, x, d, eps, out));
   else
-    mk::rmsnorm_kernel<false><<<T, 256, 0, s>>>(x, d, eps, out);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+    NDIFF_CUDA_TRY(launch_k(mk::rmsnorm_kernel<false>, dim3(T), dim3(256), 0, s, x, d, eps, out));
   return NDIFF_OK;
 }
 
@@ -315,22 +351,27 @@ ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t 
   return NDIFF_OK;
 }
 
+ndiff_status launch_commit(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
+                           int32_t* last, int32_t* kv_len, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::commit_kernel, dim3(1), dim3(1), 0, s, tokens, n_ptr, n_const, kv_add,
+                          last, kv_len));
+  return NDIFF_OK;
+}
+
 ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
-                               int32_t last, int32_t mask_id, cudaStream_t s) {
-  mk::block_init_kernel<<<1, 32, 0, s>>>(block_in, draft, mask, T, last, mask_id);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+                               const int32_t* last, int32_t mask_id, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::block_init_kernel, dim3(1), dim3(32), 0, s, block_in, draft, mask, T,
+                          last, mask_id));
   return NDIFF_OK;
 }
 
 ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s) {
-  mk::set_token_kernel<<<1, 1, 0, s>>>(ids, tok);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(mk::set_token_kernel, dim3(1), dim3(1), 0, s, ids, tok));
   return NDIFF_OK;
 }
 
 ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s) {
-  mk::kv_add_kernel<<<1, 1, 0, s>>>(kv_len, add);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(mk::kv_add_kernel, dim3(1), dim3(1), 0, s, kv_len, add));
   return NDIFF_OK;
 }
 

@@ -8,11 +8,12 @@
 
 namespace ndiff {
 
-// Storage row of logical row r of a weight tensor: identity, or the 64-row
-// interleave of the bf16 SwiGLU weight (gate rows j -> (j/64)*128 + j%64,
-// up rows j -> (j/64)*128 + 64 + j%64) that puts a gate row and its up row in
-// the same 128-row GEMM tile.
-enum { ROWMAP_IDENTITY = 0, ROWMAP_GATE = 1, ROWMAP_UP = 2 };
+// Storage row of logical row r of a bf16 weight tensor, chosen so that the two
+// rows a projection epilogue combines sit next to each other in one 128-row
+// tile: gate row j -> (j/64)*128 + 2(j%64), up row j -> the row after it;
+// in a q or k head of 128 rows, dim i < 64 -> 2i and dim i + 64 -> 2i + 1
+// (the rotate-half RoPE pair). fp32 models store every tensor as is.
+enum { ROWMAP_IDENTITY = 0, ROWMAP_GATE = 1, ROWMAP_UP = 2, ROWMAP_ROPE = 3 };
 
 ndiff_status launch_init_normal(void* dst, bool bf16, int tensor_id, int64_t rows, int64_t cols,
                                 int64_t row_off, int map, uint64_t seed, double sigma,
@@ -33,7 +34,9 @@ ndiff_status launch_qkv_rope_f32(const float* y, int T, int Hq, int Hkv, int D, 
 ndiff_status launch_swiglu_f32(const float* y, int T, int ffn, float* a, cudaStream_t s);
 ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t s);
 ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
-                               int32_t last, int32_t mask_id, cudaStream_t s);
+                               const int32_t* last, int32_t mask_id, cudaStream_t s);
+ndiff_status launch_commit(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
+                           int32_t* last, int32_t* kv_len, cudaStream_t s);
 ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s);
 ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s);
 

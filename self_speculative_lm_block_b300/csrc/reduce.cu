@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(RT) logits_reduce_kernel(const void* __restric
                                                            int32_t* __restrict__ argmax,
                                                            float* __restrict__ conf) {
   constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
+  griddep_launch();
+  griddep_wait();
   const int r = blockIdx.x;
   const char* row = static_cast<const char*>(logits) + (size_t)r * ld * (BF16 ? 2 : 4);
   const uint4* vrow = reinterpret_cast<const uint4*>(row);
@@ -175,10 +177,11 @@ ndiff_status launch_logits_reduce(ndiff_dtype dt, const void* logits, int R, int
                                   cudaStream_t stream) {
   if (R == 0) return NDIFF_OK;
   if (dt == NDIFF_BF16)
-    logits_reduce_kernel<true><<<R, RT, 0, stream>>>(logits, V, ld, exclude_id, argmax, conf);
+    NDIFF_CUDA_TRY(launch_k(logits_reduce_kernel<true>, dim3(R), dim3(RT), 0, stream, logits, V, ld,
+                            exclude_id, argmax, conf));
   else
-    logits_reduce_kernel<false><<<R, RT, 0, stream>>>(logits, V, ld, exclude_id, argmax, conf);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+    NDIFF_CUDA_TRY(launch_k(logits_reduce_kernel<false>, dim3(R), dim3(RT), 0, stream, logits, V,
+                            ld, exclude_id, argmax, conf));
   return NDIFF_OK;
 }
 

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(128) unmask_kernel(const float* __restrict__ c
                                                      int T, int k, uint32_t* mask_bits,
                                                      int32_t* block_in, int32_t* draft,
                                                      int32_t* chosen) {
+  griddep_launch();
+  griddep_wait();
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int i = threadIdx.x & 31;
   if (b >= B) return;
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(128) verify_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ target, int B,
                                                      int T, int32_t* accept_len, int32_t* commit,
                                                      int32_t* n_commit, int32_t* kv_len) {
+  griddep_launch();
+  griddep_wait();
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int i = threadIdx.x & 31;
   if (b >= B) return;
@@ -76,9 +80,8 @@ ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T,
                            uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                            int32_t* chosen, cudaStream_t stream) {
   if (B == 0) return NDIFF_OK;
-  unmask_kernel<<<(B + 3) / 4, 128, 0, stream>>>(conf, pred, B, T, k, mask_bits, block_in, draft,
-                                                 chosen);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(unmask_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, conf, pred, B, T,
+                          k, mask_bits, block_in, draft, chosen));
   return NDIFF_OK;
 }
 
@@ -86,9 +89,8 @@ ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, i
                                   int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                   int32_t* kv_len, cudaStream_t stream) {
   if (B == 0) return NDIFF_OK;
-  verify_kernel<<<(B + 3) / 4, 128, 0, stream>>>(draft, target, B, T, accept_len, commit,
-                                                 n_commit, kv_len);
-  NDIFF_CUDA_TRY(cudaGetLastError());
+  NDIFF_CUDA_TRY(launch_k(verify_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, draft, target, B,
+                          T, accept_len, commit, n_commit, kv_len));
   return NDIFF_OK;
 }
 
