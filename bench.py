@@ -13,6 +13,14 @@ Workloads (seeded synthetic inputs, shapes of the 8B-like configurations):
                 rotated over copies so every launch reads from HBM).
   attn-long     block attention alone, batch 4, prefix 32768.
 
+Every run also decodes with the 8B-shaped random-init model (36 layers,
+d_model 4096, 32/8 heads x 128, SwiGLU 12288, vocab 151936, bf16 weights; batch
+1, 1024-token prompt) unless --model-tokens 0: AR and temperature-0
+self-speculation (32-token diffusion drafts, one drafting forward) each
+generate --model-tokens tokens through the C ABI's decode step; reported as
+tokens/s, tokens per forward and whether the self-speculation tokens equal
+the AR tokens.
+
 Under torchrun (N > 1) each rank runs an independent replica of the workload
 (sequences are independent: no collective on the data path); value is the
 work of all ranks divided by the slowest rank's time.
@@ -277,6 +285,53 @@ def _oracle_threads():
         return os.cpu_count()
 
 
+def weight_bytes_8b(c):
+    d, D, Hq, Hkv, f, V = c["d_model"], c["head_dim"], c["n_heads"], c["n_kv_heads"], c["ffn"], c["vocab"]
+    per_layer = ((Hq + 2 * Hkv) * D * d + d * Hq * D + 2 * f * d + d * f) * 2
+    return c["layers"] * per_layer + V * d * 2
+
+
+def run_model(rank, n_tokens, steps=1):
+    """AR and self-speculative decoding of the 8B-shaped model on this rank."""
+    import torch
+    from self_speculative_lm_block_b300 import ndiff as nd
+    from self_speculative_lm_block_b300 import synth
+    c = synth.MODEL_8B
+    seed = c["seed"] + 1000 * rank
+    m = nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
+                 c["vocab"], dtype="bf16", max_seq=c["prompt"] + n_tokens + 64, seed=seed)
+    prompt = synth.prompt(c["prompt"], c["vocab"], seed)
+    out = {"model": "8B-shaped random init (36L, d4096, 32/8x128, ffn 12288, V151936, bf16)",
+           "prompt": c["prompt"], "tokens": n_tokens}
+    res = {}
+    for name, mode in (("ar", nd.NDIFF_MODE_AR), ("selfspec", nd.NDIFF_MODE_SELFSPEC)):
+        m.prefill(prompt)
+        m.step(mode, steps)                      # warm-up cycle (graph capture)
+        m.prefill(prompt)
+        m.stats = nd.Stats()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        toks = m.generate(mode, n_tokens, steps)
+        dt = time.perf_counter() - t0
+        st = m.stats
+        res[name] = toks
+        out[name] = {"tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+                     "tokens_per_forward": st.tokens / st.forwards,
+                     "ms_per_forward": dt * 1e3 / st.forwards, "seconds": dt}
+        if name == "selfspec":
+            hist = [int(x) for x in st.accept_hist]
+            out[name]["accept_len_hist"] = {str(i): v for i, v in enumerate(hist) if v}
+            out[name]["draft_forwards_per_block"] = steps
+    wb = weight_bytes_8b(c)
+    out["weight_bytes_per_forward"] = wb
+    out["ar"]["weight_stream_gbs"] = wb / (out["ar"]["ms_per_forward"] * 1e-3) / 1e9
+    out["selfspec_equals_ar"] = res["selfspec"] == res["ar"]
+    out["note"] = ("random-init weights: tokens per forward is not the trained model's; "
+                   "decode steps are host-synchronous calls (host buffers in and out)")
+    m.close()
+    return out
+
+
 def make_workload(name, rank):
     if name.startswith("attn-"):
         return AttnWorkload(name, rank)
@@ -326,6 +381,8 @@ def main():
                     choices=["attn-batched", "attn-single", "attn-long"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--model-tokens", type=int, default=512,
+                    help="tokens generated per mode by the 8B-shaped model (0: skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -402,6 +459,13 @@ def main():
     e2e_ms = f0.elapsed_time(f1) / n_e2e
     e2e_val = wl.step_bytes * world / (e2e_ms * 1e-3) / 1e9
 
+    model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
+    if model is not None and world > 1:
+        for k in ("ar", "selfspec"):
+            t = torch.tensor([model[k]["tokens_per_s"]], device="cuda", dtype=torch.float64)
+            torch.distributed.all_reduce(t)
+            model[k]["tokens_per_s_all_ranks"] = float(t.item())
+
     hbm, _, _, src = _peaks()
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -419,6 +483,8 @@ def main():
                "gpu_launches": wl.launches * steps_done,
                "timing": "CUDA-graph replay of whole steps; attention timed by a graph of its launches",
                "clocks": clk.summary()}
+        if model is not None:
+            out["model_8b"] = model
         if not args.no_cpu_baseline:
             cv, desc, dt = wl.oracle_sample()
             out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": _oracle_threads(),

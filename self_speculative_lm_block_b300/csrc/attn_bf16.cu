@@ -35,24 +35,32 @@ namespace ndiff {
 namespace attn {
 
 constexpr int BN = 64;      // keys per tile
-constexpr int NST = 4;      // K/V pipeline stages
+constexpr int NST = 6;      // K/V pipeline stages
 constexpr int ROWS = 128;   // MMA M (G * T rows)
 constexpr int DH = 128;     // head dim
-constexpr int Q_BYTES = ROWS * DH * 2;   // 32 KB: two 64-column halves of 16 KB
 constexpr int KT_BYTES = BN * DH * 2;    // 16 KB: two halves of 8 KB
 constexpr int P_BYTES = ROWS * BN * 2;   // 16 KB
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + NST * KT_BYTES;
 constexpr int OFF_P = OFF_V + NST * KT_BYTES;
+// (m, l) of both softmax groups at the end, in the P buffers (free by then)
+constexpr int OFF_ML = OFF_P;
 constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int N_BARS = 1 + 3 * NST + 6;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers/flags + alignment slack
-constexpr int TMEM_COLS = 256;                     // O: [0,128), S0: [128,192), S1: [192,256)
-constexpr int THREADS = 192;
+constexpr int N_BARS = 1 + 3 * NST + 3 + 2 + 2 + 1;
+constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
+// TMEM columns: O of softmax group 0 [0,128), of group 1 [128,256), Q as the
+// S product's A operand [256,320) (two bf16 per column), three 64-column S
+// buffers [320,512) (tile j uses buffer j % 3).
+constexpr int TMEM_COLS = 512;
+constexpr int TQ = 256;
+constexpr int TS = 320;
+constexpr int NSB = 3;
+constexpr int THREADS = 320;                       // producer, MMA, 2 x 4 softmax warps
 constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
+  const __nv_bfloat16* q;  // [B][T][Hq][128]
   const int32_t* kv_len;
   int B, T, Hq, Hkv, G, Lmax;
   float scale_log2;   // scale * log2(e)
@@ -69,6 +77,13 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// (lo, hi) -> bf16x2 with lo in the low half, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& sa, float& sb) {
@@ -94,9 +109,22 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Named barrier of the 256 softmax threads (both groups).
+__device__ __forceinline__ bool softmax_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK,
+    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -118,30 +146,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NST;
   uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
+  uint64_t* s_full = kv_empty + NST;   // [NSB]
+  uint64_t* p_full = s_full + NSB;     // [2] one per softmax group
+  uint64_t* o_done = p_full + 2;       // [2]
+  uint64_t* mma_done = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* ml = reinterpret_cast<float2*>(smem + OFF_ML);  // [2][128] (m, l) per group
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, 128);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
+    for (int i = 0; i < NSB; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -155,7 +185,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   griddep_launch();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t* sQ = smem + OFF_Q;
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
   uint8_t* sP = smem + OFF_P;
@@ -163,10 +192,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int rowsq = p.G * p.T;
-      mbar_arrive_expect_tx(q_full, 2u * rowsq * 128u);
-      tma_load_3d(sQ, &tmQ, q_full, 0, g * p.G, b * p.T);
-      tma_load_3d(sQ + 16384, &tmQ, q_full, 64, g * p.G, b * p.T);
       const int row0 = (b * p.Hkv + g) * p.Lmax;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
@@ -185,7 +210,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (*abort_flag) {
         // Let every issued copy land before the CTA's shared memory goes away.
-        mbar_drain(q_full, 0);
         for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
           mbar_drain(&k_full[j % NST], (j / NST) & 1);
           mbar_drain(&v_full[j % NST], (j / NST) & 1);
@@ -197,56 +221,123 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(ROWS, BN, false, false);
       const uint32_t idPV = idesc_bf16_f32(ROWS, DH, false, true);
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
+      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
       bool ok = mbar_wait(q_full, 0, p.status, abort_flag);
-      auto issue_s = [&](int j) -> bool {
+      tc_fence_after();
+      auto issue_s = [&](int j) {
         const int st = j % NST;
-        if (!mbar_wait(&k_full[st], (j / NST) & 1, p.status, abort_flag)) return false;
         tc_fence_after();
         const uint32_t kb = ka + st * KT_BYTES;
-        const uint32_t dS = tmem + 128 + (j & 1) * 64;
+        const uint32_t dS = tmem + TS + (j % NSB) * 64;
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * 16384 + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 8192 + off, 16, 1024);
-          umma_f16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
+          umma_f16_ts(dS, tmem + TQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j & 1]);
-        return true;
+        umma_commit(&s_full[j % NSB]);
       };
-      if (ok) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int st = j % NST;
-        if (!mbar_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) break;
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.status, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t vb = va + st * KT_BYTES;
-        const uint32_t pb = pa + (j & 1) * P_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(pb + kk * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 8192, 1024);
-          umma_f16(tmem, ad, bd, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+      // Issue whichever MMA is ready: S(ns) once its K tile landed and its S
+      // buffer is free (PV(ns-3) issued, i.e. S(ns-3) was read), PV(npv) once
+      // its V tile and the group's P are ready. Neither waits behind the other.
+      int ns = 0, npv = 0;
+      uint32_t idle = 0;
+      unsigned long long t0 = 0;
+      while (ok && npv < ntiles) {
+        bool progressed = false;
+        if (ns < ntiles && ns < npv + NSB &&
+            mbar_test_wait(smem_u32(&k_full[ns % NST]), (ns / NST) & 1)) {
+          issue_s(ns);
+          ++ns;
+          progressed = true;
         }
-        umma_commit(&o_done[j & 1]);
-        umma_commit(&kv_empty[st]);
-        if (j + 2 < ntiles) ok = issue_s(j + 2);
+        if (npv < ns) {
+          const int st = npv % NST, w = npv & 1;
+          if (mbar_test_wait(smem_u32(&v_full[st]), (npv / NST) & 1) &&
+              mbar_test_wait(smem_u32(&p_full[w]), (npv >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t vb = va + st * KT_BYTES;
+            const uint32_t pb = pa + w * P_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(pb + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 8192, 1024);
+              umma_f16(tmem + w * DH, ad, bd, idPV, (npv > 1 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&o_done[w]);
+            umma_commit(&kv_empty[st]);
+            ++npv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle = 0;
+          t0 = 0;
+          continue;
+        }
+        // Nothing ready: sleep on the barrier that gates the next PV (or the
+        // next S), so that this thread does not take issue slots from the
+        // softmax warps sharing its sub-partition.
+        if (npv < ns)
+          mbar_try_wait_hint(smem_u32(&p_full[npv & 1]), (npv >> 1) & 1, 400);
+        else if (ns < ntiles)
+          mbar_try_wait_hint(smem_u32(&k_full[ns % NST]), (ns / NST) & 1, 400);
+        if ((++idle & 15u) == 0) {
+          if (t0 == 0) t0 = globaltimer();
+          if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(p.status, kStatusTimeout);
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
       }
+      umma_commit(mma_done);
+      mbar_drain(mma_done, 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax rows
+    // ------------------------------------------------- softmax, two groups
+    // Group w takes the tiles j with j % 2 == w and keeps its own running
+    // maximum, sum and O accumulator; the two are merged at the end.
+    const int grp = (warp - 2) >> 2;            // 0 or 1
     const uint32_t quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const bool valid = r < p.G * p.T;
     const int t = r / p.G;
     const int vis_end = valid ? P + (p.causal ? t + 1 : p.T) : 0;
     const uint32_t tl = tmem + ((quarter * 32u) << 16);
+    const uint32_t tO = tl + grp * DH;
+    if (grp == 0) {
+      // Q row r (slot t, head g*G + r % G) into TMEM columns [TQ, TQ + 64).
+      uint32_t w[64];
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (((size_t)b * p.T + t) * p.Hq + g * p.G + r % p.G) * DH);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 u = src[i];
+          w[4 * i] = u.x;
+          w[4 * i + 1] = u.y;
+          w[4 * i + 2] = u.z;
+          w[4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) w[i] = 0u;
+      }
+      tmem_st32(tl + TQ, reinterpret_cast<const float*>(w));
+      tmem_st32(tl + TQ + 32, reinterpret_cast<const float*>(w + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_full);
+    }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    const int tid128 = threadIdx.x - 64;
-    for (int j = 0; j < ntiles; ++j) {
+    const int tid128 = (threadIdx.x - 64) & 127;
+    const float c = p.scale_log2;
+    int k = 0;                                   // tiles done by this group
+    for (int j = grp; j < ntiles; j += 2, ++k) {
       const int key0 = k_begin + j * BN;
       const int st = j % NST;
       const int nv = min(BN, k_end - key0);
@@ -255,48 +346,54 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!warp_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) { ok = false; break; }
         uint8_t* vt = sV + st * KT_BYTES;
         const int per_half = (BN - nv) * 8;
-        for (int c = tid128; c < 2 * per_half; c += 128) {
-          const int half = c / per_half, rem = c % per_half;
+        for (int cix = tid128; cix < 2 * per_half; cix += 128) {
+          const int half = cix / per_half, rem = cix % per_half;
           const int row = nv + rem / 8;
           *reinterpret_cast<uint4*>(vt + half * 8192 + row * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
-      if (!warp_wait(&s_full[j & 1], (j >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      if (!warp_wait(&s_full[j % NSB], (j / NSB) & 1, p.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[BN];
-      tmem_ld32(tl + 128 + (j & 1) * 64, s);
-      tmem_ld32(tl + 128 + (j & 1) * 64 + 32, s + 32);
+      tmem_ld32(tl + TS + (j % NSB) * 64, s);
+      tmem_ld32(tl + TS + (j % NSB) * 64 + 32, s + 32);
       tmem_wait_ld();
       const int lim = vis_end - key0;
-      float mt = -INFINITY;
+      if (lim < BN) {
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        s[i] = (i < lim) ? s[i] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < BN; ++i) s[i] = (i < lim) ? s[i] : -INFINITY;
       }
+      // row maximum of the raw scores (tree), then in scaled log2 units
+      float mx[BN / 2];
+#pragma unroll
+      for (int i = 0; i < BN / 2; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+      for (int w2 = BN / 4; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
+      }
+      const float mt = mx[0] * c;
       // Raise the running maximum only when it grew by more than 2^8; the
       // decision is per row, the O rescale in TMEM is warp-collective.
       float alpha = 1.f;
       const bool grow = mt > m_run + RESCALE_THRESHOLD;
       if (grow) alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mt);
-      const bool grow_o = grow && j > 0 && m_run != -INFINITY;
+      // P buffer and O of this group are free once its previous PV completed.
+      if (k > 0 && !warp_wait(&o_done[grp], (k - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      const bool grow_o = grow && k > 0 && m_run != -INFINITY;
       if (__any_sync(0xffffffffu, grow_o)) {
-        if (!warp_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
         const float a_o = grow_o ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
+        for (int cc = 0; cc < DH / 32; ++cc) {
           float o[32];
-          tmem_ld32(tl + c * 32, o);
+          tmem_ld32(tO + cc * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= a_o;
-          tmem_st32(tl + c * 32, o);
+          tmem_st32(tO + cc * 32, o);
         }
         tmem_wait_st();
       }
@@ -304,69 +401,81 @@ __global__ void __launch_bounds__(THREADS, 1)
         l_run *= alpha;
         m_run = mt;
       }
-      if (j >= 2) {
-        // P buffer (j & 1) is free once PV(j-2) has completed.
-        if (!warp_wait(&o_done[j & 1], ((j - 2) >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
-      }
-      uint8_t* prow = sP + (j & 1) * P_BYTES + r * 128;
-      float sum = 0.f;
+      uint8_t* prow = sP + grp * P_BYTES + r * 128;
       const bool none = (m_run == -INFINITY);
+      const float nm = none ? 0.f : -m_run;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        uint32_t w[4];
+      for (int cc = 0; cc < BN / 8; ++cc) {
+        uint32_t wds[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = none ? 0.f : ex2(s[c * 8 + 2 * e] - m_run);
-          const float x1 = none ? 0.f : ex2(s[c * 8 + 2 * e + 1] - m_run);
-          float r0, r1;
-          w[e] = pack_bf16(x0, x1, r0, r1);
-          sum += r0 + r1;
+          const float x0 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e], c, nm));
+          const float x1 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e + 1], c, nm));
+          sum0 += x0;
+          sum1 += x1;
+          wds[e] = pack_bf16x2(x0, x1);
         }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(wds[0], wds[1], wds[2], wds[3]);
       }
-      l_run += sum;
+      l_run += sum0 + sum1;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_full[grp]);
     }
     // ---------------------------------------------------------- epilogue
+    // both groups wait for their last PV, then merge (m, l, O) per row
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      const int last = ntiles - 1;
-      ok = warp_wait(&o_done[last & 1], (last >> 1) & 1, p.status, abort_flag);
-    }
+    if (ok && k > 0) ok = warp_wait(&o_done[grp], (k - 1) & 1, p.status, abort_flag);
+    // after this barrier both groups' last PV has completed: the P buffers,
+    // which hold the (m, l) exchange, are free
+    ok = softmax_bar_and(ok);
+    if (ok) ml[grp * ROWS + r] = make_float2(m_run, l_run);
+    ok = softmax_bar_and(ok);
     if (ok) {
       tc_fence_after();
+      const bool has1 = ntiles > 1;
+      const float2 z0 = ml[r];
+      const float2 z1 = has1 ? ml[ROWS + r] : make_float2(-INFINITY, 0.f);
+      const float M = fmaxf(z0.x, z1.x);
+      const float w0 = (z0.x == -INFINITY) ? 0.f : ex2(z0.x - M);
+      const float w1 = (z1.x == -INFINITY) ? 0.f : ex2(z1.x - M);
+      const float L = w0 * z0.y + w1 * z1.y;
       const int hh = valid ? r % p.G : 0;
       const size_t unit = ((size_t)(b * p.Hkv + g) * p.nsplit_max + s_idx) * ROWS + r;
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
+      // group w writes output columns [64 w, 64 w + 64)
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
-        float o[32];
-        tmem_ld32(tl + c * 32, o);
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = grp * 64 + cc * 32;
+        float a[32], bb[32];
+        tmem_ld32(tl + col, a);
+        if (has1) tmem_ld32(tl + DH + col, bb);
         tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = w0 * a[i] + (has1 ? w1 * bb[i] : 0.f);
         if (!valid) continue;
         if (nsplit_b == 1) {
           __nv_bfloat16* dst =
-              p.out + (((size_t)b * p.T + t) * p.Hq + g * p.G + hh) * DH + c * 32;
+              p.out + (((size_t)b * p.T + t) * p.Hq + g * p.G + hh) * DH + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 v;
-            float d0, d1;
-            v.x = pack_bf16(o[i] * inv_l, o[i + 1] * inv_l, d0, d1);
-            v.y = pack_bf16(o[i + 2] * inv_l, o[i + 3] * inv_l, d0, d1);
-            v.z = pack_bf16(o[i + 4] * inv_l, o[i + 5] * inv_l, d0, d1);
-            v.w = pack_bf16(o[i + 6] * inv_l, o[i + 7] * inv_l, d0, d1);
+            v.x = pack_bf16x2(a[i] * inv_l, a[i + 1] * inv_l);
+            v.y = pack_bf16x2(a[i + 2] * inv_l, a[i + 3] * inv_l);
+            v.z = pack_bf16x2(a[i + 4] * inv_l, a[i + 5] * inv_l);
+            v.w = pack_bf16x2(a[i + 6] * inv_l, a[i + 7] * inv_l);
             *reinterpret_cast<uint4*>(dst + i) = v;
           }
         } else {
-          float* dst = p.ws_o + unit * DH + c * 32;
+          float* dst = p.ws_o + unit * DH + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            *reinterpret_cast<float4*>(dst + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
         }
       }
-      if (valid && nsplit_b > 1) p.ws_ml[unit] = make_float2(m_run, l_run);
+      if (valid && nsplit_b > 1 && grp == 0) p.ws_ml[unit] = make_float2(M, L);
     }
   }
 
@@ -420,14 +529,29 @@ __global__ void __launch_bounds__(128)
 
 }  // namespace attn
 
+// KV split length (keys per CTA) for a launch of B x Hkv sequences of at most
+// Lmax keys. One CTA runs per SM, so the time is about
+//   ceil(CTAs / SMs) * (tiles per split + per-CTA overhead),
+// where the overhead (start-up, first loads, partial write and merge) is worth
+// about six 64-key tiles. The smallest cost wins; ties keep the longer split.
 int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
-  const long long target = 8LL * num_sms();
-  long long want = ((long long)Lmax * B * Hkv + target - 1) / target;
-  want = ((want + attn::BN - 1) / attn::BN) * attn::BN;
-  const long long whole = ((long long)(Lmax + attn::BN - 1) / attn::BN) * attn::BN;
-  if (want < 256) want = 256;
-  if (want > whole) want = whole;
-  return (int)want;
+  const long long sms = num_sms();
+  const long long tiles = (Lmax + attn::BN - 1) / attn::BN;
+  long long best = -1;
+  int best_split = (int)(tiles * attn::BN);
+  for (long long per = tiles; per >= 1; --per) {
+    const long long nsplit = (tiles + per - 1) / per;
+    if (per > 1 && (tiles + per - 2) / (per - 1) == nsplit) continue;  // same split count, shorter
+    const long long ctas = (long long)B * Hkv * nsplit;
+    const long long waves = (ctas + sms - 1) / sms;
+    const long long cost = waves * (per + 6);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_split = (int)(per * attn::BN);
+    }
+    if (nsplit >= 256) break;
+  }
+  return best_split;
 }
 
 size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
@@ -448,14 +572,7 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   if (need > 0 && (ws == nullptr || ws_bytes < need))
     return set_error(NDIFF_ERR_WORKSPACE, "ndiff_block_attn: workspace of %zu bytes needed, %zu given",
                      need, ws_bytes);
-  CUtensorMap tq, tk, tv;
-  {
-    const uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)B * T};
-    const uint64_t strides[2] = {128 * 2, (uint64_t)Hq * 128 * 2};
-    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)T};
-    ndiff_status s = make_tmap_bf16(&tq, q, 3, dims, strides, box);
-    if (s != NDIFF_OK) return s;
-  }
+  CUtensorMap tk, tv;
   {
     const uint64_t dims[2] = {128, (uint64_t)B * Hkv * Lmax};
     const uint64_t strides[1] = {128 * 2};
@@ -466,6 +583,7 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
     if (s != NDIFF_OK) return s;
   }
   attn::Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.kv_len = kv_len;
   prm.B = B;
   prm.T = T;
@@ -495,7 +613,7 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   }
   dim3 grid(nsplit, Hkv, B);
   NDIFF_CUDA_TRY(launch_k(attn::attn_bf16_kernel, grid, dim3(attn::THREADS),
-                          (size_t)attn::SMEM_BYTES, stream, tq, tk, tv, prm));
+                          (size_t)attn::SMEM_BYTES, stream, tk, tv, prm));
   if (nsplit > 1) {
     dim3 g2((G * T + 3) / 4, Hkv, B);
     NDIFF_CUDA_TRY(launch_k(attn::attn_combine_kernel, g2, dim3(128), 0, stream, prm));
