@@ -46,7 +46,7 @@ constexpr int OFF_P = OFF_V + NST * KT_BYTES;
 // (m, l) of both softmax groups at the end, in the P buffers (free by then)
 constexpr int OFF_ML = OFF_P;
 constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int N_BARS = 1 + 3 * NST + 3 + 2 + 2 + 1;
+constexpr int N_BARS = 1 + 3 * NST + 2 * 3 + 2 + 2 + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
 // TMEM columns: O of softmax group 0 [0,128), of group 1 [128,256), Q as the
 // S product's A operand [256,320) (two bf16 per column), three 64-column S
@@ -123,6 +123,21 @@ __device__ __forceinline__ bool softmax_bar_and(bool pred) {
   return r != 0;
 }
 
+// Named barrier `id` of the 128 threads of one softmax group; returns the AND
+// of `pred` over them.
+__device__ __forceinline__ bool group_bar_and(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -146,10 +161,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NST;
   uint64_t* kv_empty = v_full + NST;
-  uint64_t* s_full = kv_empty + NST;   // [NSB]
-  uint64_t* p_full = s_full + NSB;     // [2] one per softmax group
-  uint64_t* o_done = p_full + 2;       // [2]
-  uint64_t* mma_done = o_done + 2;
+  uint64_t* s_full = kv_empty + NST;   // [NSB] S product of the buffer landed
+  uint64_t* s_free = s_full + NSB;     // [NSB] S buffer read by its softmax group
+  uint64_t* o_done = s_free + NSB;     // [2] PV products of a group completed
+  uint64_t* g_done = o_done + 2;       // [2] drain of a group's PV products at exit
+  uint64_t* mma_done = g_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* ml = reinterpret_cast<float2*>(smem + OFF_ML);  // [2][128] (m, l) per group
@@ -162,10 +178,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < NSB; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
+      mbar_init(&g_done[i], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -217,81 +236,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
+    // S(j) = Q K_j^T into buffer j % NSB once K_j landed and the group that
+    // read S(j - NSB) released the buffer. PV products are issued by the
+    // softmax groups themselves.
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(ROWS, BN, false, false);
-      const uint32_t idPV = idesc_bf16_f32(ROWS, DH, false, true);
-      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
+      const uint32_t ka = smem_u32(sK);
       bool ok = mbar_wait(q_full, 0, p.status, abort_flag);
       tc_fence_after();
-      auto issue_s = [&](int j) {
-        const int st = j % NST;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int st = j % NST, sb = j % NSB;
+        if (j >= NSB && !mbar_wait(&s_free[sb], ((j / NSB) - 1) & 1, p.status, abort_flag)) break;
+        if (!mbar_wait(&k_full[st], (j / NST) & 1, p.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t kb = ka + st * KT_BYTES;
-        const uint32_t dS = tmem + TS + (j % NSB) * 64;
+        const uint32_t dS = tmem + TS + sb * 64;
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
           const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 8192 + off, 16, 1024);
           umma_f16_ts(dS, tmem + TQ + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j % NSB]);
-      };
-      // Issue whichever MMA is ready: S(ns) once its K tile landed and its S
-      // buffer is free (PV(ns-3) issued, i.e. S(ns-3) was read), PV(npv) once
-      // its V tile and the group's P are ready. Neither waits behind the other.
-      int ns = 0, npv = 0;
-      uint32_t idle = 0;
-      unsigned long long t0 = 0;
-      while (ok && npv < ntiles) {
-        bool progressed = false;
-        if (ns < ntiles && ns < npv + NSB &&
-            mbar_test_wait(smem_u32(&k_full[ns % NST]), (ns / NST) & 1)) {
-          issue_s(ns);
-          ++ns;
-          progressed = true;
-        }
-        if (npv < ns) {
-          const int st = npv % NST, w = npv & 1;
-          if (mbar_test_wait(smem_u32(&v_full[st]), (npv / NST) & 1) &&
-              mbar_test_wait(smem_u32(&p_full[w]), (npv >> 1) & 1)) {
-            tc_fence_after();
-            const uint32_t vb = va + st * KT_BYTES;
-            const uint32_t pb = pa + w * P_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(pb + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 8192, 1024);
-              umma_f16(tmem + w * DH, ad, bd, idPV, (npv > 1 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(&o_done[w]);
-            umma_commit(&kv_empty[st]);
-            ++npv;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          idle = 0;
-          t0 = 0;
-          continue;
-        }
-        // Nothing ready: sleep on the barrier that gates the next PV (or the
-        // next S), so that this thread does not take issue slots from the
-        // softmax warps sharing its sub-partition.
-        if (npv < ns)
-          mbar_try_wait_hint(smem_u32(&p_full[npv & 1]), (npv >> 1) & 1, 400);
-        else if (ns < ntiles)
-          mbar_try_wait_hint(smem_u32(&k_full[ns % NST]), (ns / NST) & 1, 400);
-        if ((++idle & 15u) == 0) {
-          if (t0 == 0) t0 = globaltimer();
-          if (*abort_flag) {
-            ok = false;
-          } else if (globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(p.status, kStatusTimeout);
-            *abort_flag = 1;
-            ok = false;
-          }
-        }
+        umma_commit(&s_full[sb]);
       }
       umma_commit(mma_done);
       mbar_drain(mma_done, 0);
@@ -299,7 +266,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------- softmax, two groups
     // Group w takes the tiles j with j % 2 == w and keeps its own running
-    // maximum, sum and O accumulator; the two are merged at the end.
+    // maximum, sum and O accumulator; the two are merged at the end. After
+    // writing P(j) the group's first thread issues O_w += P(j) V_j itself.
     const int grp = (warp - 2) >> 2;            // 0 or 1
     const uint32_t quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -308,6 +276,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int vis_end = valid ? P + (p.causal ? t + 1 : p.T) : 0;
     const uint32_t tl = tmem + ((quarter * 32u) << 16);
     const uint32_t tO = tl + grp * DH;
+    const int tid128 = (threadIdx.x - 64) & 127;
+    const bool issuer = tid128 == 0;
     if (grp == 0) {
       // Q row r (slot t, head g*G + r % G) into TMEM columns [TQ, TQ + 64).
       uint32_t w[64];
@@ -334,95 +304,126 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    const int tid128 = (threadIdx.x - 64) & 127;
     const float c = p.scale_log2;
+    const uint32_t idPV = idesc_bf16_f32(ROWS, DH, false, true);
+    const uint32_t pa = smem_u32(sP) + grp * P_BYTES, va = smem_u32(sV);
     int k = 0;                                   // tiles done by this group
     for (int j = grp; j < ntiles; j += 2, ++k) {
       const int key0 = k_begin + j * BN;
-      const int st = j % NST;
+      const int st = j % NST, sb = j % NSB;
       const int nv = min(BN, k_end - key0);
+      bool ok_it = true;
       if (nv < BN) {
         // Zero the V rows past the sequence so that P = 0 meets finite values.
-        if (!warp_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) { ok = false; break; }
-        uint8_t* vt = sV + st * KT_BYTES;
-        const int per_half = (BN - nv) * 8;
-        for (int cix = tid128; cix < 2 * per_half; cix += 128) {
-          const int half = cix / per_half, rem = cix % per_half;
-          const int row = nv + rem / 8;
-          *reinterpret_cast<uint4*>(vt + half * 8192 + row * 128 + (rem % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
+        ok_it = warp_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag);
+        if (ok_it) {
+          uint8_t* vt = sV + st * KT_BYTES;
+          const int per_half = (BN - nv) * 8;
+          for (int cix = tid128; cix < 2 * per_half; cix += 128) {
+            const int half = cix / per_half, rem = cix % per_half;
+            const int row = nv + rem / 8;
+            *reinterpret_cast<uint4*>(vt + half * 8192 + row * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
       }
-      if (!warp_wait(&s_full[j % NSB], (j / NSB) & 1, p.status, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      float s[BN];
-      tmem_ld32(tl + TS + (j % NSB) * 64, s);
-      tmem_ld32(tl + TS + (j % NSB) * 64 + 32, s + 32);
-      tmem_wait_ld();
-      const int lim = vis_end - key0;
-      if (lim < BN) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i) s[i] = (i < lim) ? s[i] : -INFINITY;
-      }
-      // row maximum of the raw scores (tree), then in scaled log2 units
-      float mx[BN / 2];
-#pragma unroll
-      for (int i = 0; i < BN / 2; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-      for (int w2 = BN / 4; w2 >= 1; w2 >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
-      }
-      const float mt = mx[0] * c;
-      // Raise the running maximum only when it grew by more than 2^8; the
-      // decision is per row, the O rescale in TMEM is warp-collective.
-      float alpha = 1.f;
-      const bool grow = mt > m_run + RESCALE_THRESHOLD;
-      if (grow) alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mt);
-      // P buffer and O of this group are free once its previous PV completed.
-      if (k > 0 && !warp_wait(&o_done[grp], (k - 1) & 1, p.status, abort_flag)) { ok = false; break; }
-      const bool grow_o = grow && k > 0 && m_run != -INFINITY;
-      if (__any_sync(0xffffffffu, grow_o)) {
+      if (ok_it) ok_it = warp_wait(&s_full[sb], (j / NSB) & 1, p.status, abort_flag);
+      if (ok_it) {
         tc_fence_after();
-        const float a_o = grow_o ? alpha : 1.f;
+        float s[BN];
+        tmem_ld32(tl + TS + sb * 64, s);
+        tmem_ld32(tl + TS + sb * 64 + 32, s + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
+        const int lim = vis_end - key0;
+        if (lim < BN) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) s[i] = (i < lim) ? s[i] : -INFINITY;
+        }
+        // row maximum of the raw scores (tree), then in scaled log2 units
+        float mx[BN / 2];
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int w2 = BN / 4; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+          for (int i = 0; i < w2; ++i) mx[i] = fmaxf(mx[i], mx[i + w2]);
+        }
+        const float mt = mx[0] * c;
+        // Raise the running maximum only when it grew by more than 2^8; the
+        // decision is per row, the O rescale in TMEM is warp-collective.
+        float alpha = 1.f;
+        const bool grow = mt > m_run + RESCALE_THRESHOLD;
+        if (grow) alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mt);
+        // P buffer and O of this group are free once its previous PV completed.
+        if (k > 0) ok_it = warp_wait(&o_done[grp], (k - 1) & 1, p.status, abort_flag);
+        if (ok_it) {
+          const bool grow_o = grow && k > 0 && m_run != -INFINITY;
+          if (__any_sync(0xffffffffu, grow_o)) {
+            tc_fence_after();
+            const float a_o = grow_o ? alpha : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < DH / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + cc * 32, o);
-          tmem_wait_ld();
+            for (int cc = 0; cc < DH / 32; ++cc) {
+              float o[32];
+              tmem_ld32(tO + cc * 32, o);
+              tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= a_o;
-          tmem_st32(tO + cc * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] *= a_o;
+              tmem_st32(tO + cc * 32, o);
+            }
+            tmem_wait_st();
+          }
+          if (grow) {
+            l_run *= alpha;
+            m_run = mt;
+          }
+          uint8_t* prow = sP + grp * P_BYTES + r * 128;
+          const bool none = (m_run == -INFINITY);
+          const float nm = none ? 0.f : -m_run;
+          float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < BN / 8; ++cc) {
+            uint32_t wds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e], c, nm));
+              const float x1 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e + 1], c, nm));
+              sum0 += x0;
+              sum1 += x1;
+              wds[e] = pack_bf16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+                make_uint4(wds[0], wds[1], wds[2], wds[3]);
+          }
+          l_run += sum0 + sum1;
+          fence_proxy_async_smem();
+          tc_fence_before();
         }
-        tmem_wait_st();
       }
-      if (grow) {
-        l_run *= alpha;
-        m_run = mt;
-      }
-      uint8_t* prow = sP + grp * P_BYTES + r * 128;
-      const bool none = (m_run == -INFINITY);
-      const float nm = none ? 0.f : -m_run;
-      float sum0 = 0.f, sum1 = 0.f;
+      // the whole group agrees, then its first thread issues O_w += P(j) V_j
+      ok = group_bar_and(2 + grp, ok_it);
+      if (!ok) break;
+      if (issuer) {
+        if (mbar_wait(&v_full[st], (j / NST) & 1, p.status, abort_flag)) {
+          tc_fence_after();
+          const uint32_t vb = va + st * KT_BYTES;
 #pragma unroll
-      for (int cc = 0; cc < BN / 8; ++cc) {
-        uint32_t wds[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e], c, nm));
-          const float x1 = none ? 0.f : ex2(fmaf(s[cc * 8 + 2 * e + 1], c, nm));
-          sum0 += x0;
-          sum1 += x1;
-          wds[e] = pack_bf16x2(x0, x1);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(pa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 8192, 1024);
+            umma_f16(tmem + grp * DH, ad, bd, idPV, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&o_done[grp]);
+          umma_commit(&kv_empty[st]);
         }
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(wds[0], wds[1], wds[2], wds[3]);
       }
-      l_run += sum0 + sum1;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[grp]);
+    }
+    if (issuer) {
+      // every PV this group issued has finished before TMEM is released
+      umma_commit(&g_done[grp]);
+      mbar_drain(&g_done[grp], 0);
     }
     // ---------------------------------------------------------- epilogue
     // both groups wait for their last PV, then merge (m, l, O) per row
@@ -531,9 +532,10 @@ __global__ void __launch_bounds__(128)
 
 // KV split length (keys per CTA) for a launch of B x Hkv sequences of at most
 // Lmax keys. One CTA runs per SM, so the time is about
-//   ceil(CTAs / SMs) * (tiles per split + per-CTA overhead),
-// where the overhead (start-up, first loads, partial write and merge) is worth
-// about six 64-key tiles. The smallest cost wins; ties keep the longer split.
+//   ceil(CTAs / SMs) * (tiles per split + per-CTA overhead) + merge,
+// where the per-CTA overhead (start-up, first loads, partial write) is worth
+// about twenty 64-key tiles and the merge launch, when the keys are split,
+// about eight. The smallest cost wins; ties keep the longer split.
 int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
   const long long sms = num_sms();
   const long long tiles = (Lmax + attn::BN - 1) / attn::BN;
@@ -544,7 +546,7 @@ int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
     if (per > 1 && (tiles + per - 2) / (per - 1) == nsplit) continue;  // same split count, shorter
     const long long ctas = (long long)B * Hkv * nsplit;
     const long long waves = (ctas + sms - 1) / sms;
-    const long long cost = waves * (per + 6);
+    const long long cost = waves * (per + 20) + (nsplit > 1 ? 8 : 0);
     if (best < 0 || cost < best) {
       best = cost;
       best_split = (int)(per * attn::BN);

@@ -48,7 +48,7 @@ def test_noalloc_matches_regular_entry_point_twice(cuda_ok):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_ok):
     from self_speculative_lm_block_b300 import ndiff as nd
-    B, T, Hq, Hkv, D, Lmax = 4, 32, 32, 8, 128, 32800
+    B, T, Hq, Hkv, D, Lmax = 64, 32, 32, 8, 128, 32800
     assert nd.ndiff_block_attn_workspace_size(nd.NDIFF_BF16, B, T, Hq, Hkv, D, Lmax) > \
         nd.NDIFF_NOALLOC_SCRATCH_BYTES
     with pytest.raises(nd.NdiffError) as e:
