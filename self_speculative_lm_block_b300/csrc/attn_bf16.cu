@@ -533,9 +533,11 @@ __global__ void __launch_bounds__(128)
 // KV split length (keys per CTA) for a launch of B x Hkv sequences of at most
 // Lmax keys. One CTA runs per SM, so the time is about
 //   ceil(CTAs / SMs) * (tiles per split + per-CTA overhead) + merge,
-// where the per-CTA overhead (start-up, first loads, partial write) is worth
-// about twenty 64-key tiles and the merge launch, when the keys are split,
-// about eight. The smallest cost wins; ties keep the longer split.
+// where the per-CTA overhead (start-up, first loads, partial write and the
+// tail of a wave) is worth about forty 64-key tiles and the merge launch,
+// when the keys are split, about eight (calibrated on B300 by sweeping the
+// split length of the batch-1/4096, batch-4/32768 and batch-64 workloads).
+// The smallest cost wins; ties keep the longer split.
 int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
   const long long sms = num_sms();
   const long long tiles = (Lmax + attn::BN - 1) / attn::BN;
@@ -546,7 +548,7 @@ int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
     if (per > 1 && (tiles + per - 2) / (per - 1) == nsplit) continue;  // same split count, shorter
     const long long ctas = (long long)B * Hkv * nsplit;
     const long long waves = (ctas + sms - 1) / sms;
-    const long long cost = waves * (per + 20) + (nsplit > 1 ? 8 : 0);
+    const long long cost = waves * (per + 40) + (nsplit > 1 ? 8 : 0);
     if (best < 0 || cost < best) {
       best = cost;
       best_split = (int)(per * attn::BN);
