@@ -42,6 +42,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward at 8B"
+# DRAM bytes (read + write) of one attention launch, from ncu captures of the
+# current attention kernel (profiles/launches_attn_batched_step.md and
+# profiles/attn_bf16_kernel_attn_long.md); None where no capture exists.
+ATTN_TRAFFIC = {"attn-batched": 1016151040 + 17371904, "attn-long": 539035904 + 3553024,
+                "attn-single": None}
 SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126e6
 
@@ -492,7 +497,7 @@ def main():
                             "frac": attn_gbs / hbm, "peak_source": src,
                             "frac_of_spec_8tbs": attn_gbs / SPEC_HBM_GBS,
                             "bytes_per_launch": wl.attn_bytes, "ms_per_launch": attn_ms,
-                            "traffic": None},
+                            "traffic": ATTN_TRAFFIC.get(args.workload)},
                "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                "gpu_launches": wl.launches * steps_done,
