@@ -43,8 +43,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward at 8B"
 # DRAM bytes (read + write) of one attention launch, from ncu captures of the
-# current attention kernel (profiles/launches_attn_batched_step.md and
-# profiles/attn_bf16_kernel_attn_long.md); None where no capture exists.
+# current attention kernel on these workloads (summaries under profiles/);
+# None where no capture exists.
 ATTN_TRAFFIC = {"attn-batched": 1016151040 + 17371904, "attn-long": 539035904 + 3553024,
                 "attn-single": None}
 SPEC_HBM_GBS = 8000.0

@@ -84,6 +84,15 @@ NDIFF_API const char* ndiff_status_string(ndiff_status s);
  * last check, NDIFF_ERR_CUDA on a CUDA error, else NDIFF_OK. */
 NDIFF_API ndiff_status ndiff_check(cudaStream_t stream);
 
+/* Failure-path self-test (a library facility; the pages have no counterpart):
+ * enqueues one small kernel whose bounded wait on a barrier that nothing
+ * arrives on expires after about limit_us microseconds (1 <= limit_us <=
+ * 2000000). The kernel records the expiry in the device status word, the same
+ * way every kernel of this library reports an expired wait, and returns; the
+ * next ndiff_check() on the stream returns NDIFF_ERR_TIMEOUT and clears the
+ * word. Nothing faults and the CUDA context stays usable. */
+NDIFF_API ndiff_status ndiff_selftest_timeout(int limit_us, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Block-causal GQA attention over a KV cache ([TRI] modules "Block-wise
  * attention"; [FFI] "三种生成模式": 32-token block; [FFI] "训练路线").

@@ -43,7 +43,7 @@ import dataclasses
 import numpy as np
 
 from . import attention, decode, philox
-from .numerics import round_to_bf16
+from .numerics import round_f32_to_bf16, round_to_bf16
 
 BLOCK = 32
 
@@ -98,10 +98,10 @@ class Weights:
         self._cache: dict[int, np.ndarray] = {}
 
     def _values(self, tid: int, start: int, count: int) -> np.ndarray:
-        w = philox.weight_values(self.cfg.seed, tid, start, count).astype(np.float64)
+        w = philox.weight_values(self.cfg.seed, tid, start, count)   # float32
         if self.cfg.dtype == "bf16":
-            w = round_to_bf16(w)
-        return w
+            return round_f32_to_bf16(w)       # exact float32 input: one nearest-even rounding
+        return w.astype(np.float64)
 
     def full(self, tid: int) -> np.ndarray:
         if tid not in self._cache:

@@ -6,18 +6,21 @@ import numpy as np
 
 
 def f32_to_bf16_bits(x) -> np.ndarray:
-    """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even.
-    NaN stays NaN (quiet), infinities stay infinite."""
-    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    nan = (u & 0x7FFFFFFF) > 0x7F800000
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16) & 0xFFFF
-    r = np.where(nan, (u >> 16) | 0x40, r)
-    return r.astype(np.uint16)
+    """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even:
+    add 0x7FFF plus the lowest kept bit, then drop the low 16 bits. The sum can
+    wrap in 32 bits only for NaN patterns, which are handled apart (NaN stays
+    NaN, quiet); infinities stay infinite."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    nan = (u & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    if nan.any():
+        r[nan] = ((u[nan] >> np.uint32(16)) | np.uint32(0x40)).astype(np.uint16)
+    return r
 
 
 def bf16_bits_to_f64(b) -> np.ndarray:
-    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
 def round_f32_to_bf16(x) -> np.ndarray:

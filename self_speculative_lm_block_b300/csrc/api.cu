@@ -139,6 +139,30 @@ ndiff_status ndiff_check(cudaStream_t stream) {
   return NDIFF_OK;
 }
 
+namespace {
+// One warp waits on a barrier that expects an arrival nothing makes; the wait
+// gives up after limit_ns of %globaltimer, records the timeout and returns.
+__global__ void selftest_timeout_kernel(unsigned long long limit_ns, unsigned int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t b = smem_u32(&bar);
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(b, 0)) {
+      if (globaltimer() - t0 > limit_ns) {
+        atomicOr(status, kStatusTimeout);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+}
+}  // namespace
+
 static ndiff_status check_attn_args(ndiff_dtype dt, const void* q, const void* k, const void* v,
                                     const int32_t* kv_len, int B, int T, int Hq, int Hkv, int D,
                                     int Lmax, ndiff_mask mode, const void* out) {
@@ -254,6 +278,17 @@ ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, in
   return launch_verify_accept(draft, target, B, T, accept_len, commit, n_commit, kv_len, stream);
 }
 
+ndiff_status ndiff_selftest_timeout(int limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_selftest_timeout: limit_us in [1, 2000000] (got %d)",
+                     limit_us);
+  unsigned int* w = device_status_word();
+  if (!w) return set_error(NDIFF_ERR_CUDA, "device status word unavailable");
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull, w);
+  NDIFF_CUDA_TRY(cudaGetLastError());
+  return NDIFF_OK;
+}
+
 size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 64) return 0;
   const GemmPlan pl = gemm_plan(N, K);
@@ -278,7 +313,7 @@ ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, 
   const GemmPlan pl = gemm_plan(N, K);
   const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
   CUtensorMap tw, tx;
-  ndiff_status s = gemm_make_maps(w, N, K, x, M, &tw, &tx);
+  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
   if (s != NDIFF_OK) return s;
   NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
   GemmParams p;

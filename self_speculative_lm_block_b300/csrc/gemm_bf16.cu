@@ -237,7 +237,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         split_range(it % p.S, p.S, p.nks, lo, hi);
         for (int ks = lo; ks < hi && npre < NST; ++ks, ++npre) {
           mbar_arrive_expect_tx(&full[npre], A_BYTES + B_BYTES);
-          tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], ks * BK, tile * BM);
+          if (p.w_tiled)
+            tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], 0, (tile * p.nks + ks) * BM);
+          else
+            tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], ks * BK, tile * BM);
         }
       }
       griddep_wait();
@@ -255,7 +258,10 @@ __global__ void __launch_bounds__(THREADS, 2)
               break;
             }
             mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
-            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
+            if (p.w_tiled)
+              tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], 0, (tile * p.nks + ks) * BM);
+            else
+              tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
           }
           tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
           ++kc;
@@ -413,13 +419,22 @@ size_t gemm_partials_bytes(const GemmPlan& pl) {
   return pl.S > 1 ? (size_t)pl.items * gemm::MT * gemm::BM * sizeof(float) : 0;
 }
 
-ndiff_status gemm_make_maps(const void* w, int N, int K, const void* x, int M, CUtensorMap* tmW,
-                            CUtensorMap* tmX) {
+ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
+                            CUtensorMap* tmW, CUtensorMap* tmX) {
   if (tmW) {
-    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
-    const uint64_t strides[1] = {(uint64_t)K * 2};
     const uint32_t box[2] = {gemm::BK, gemm::BM};
-    ndiff_status s = make_tmap_bf16(tmW, w, 2, dims, strides, box);
+    ndiff_status s;
+    if (w_tiled) {
+      // [tiles * K/64 * 128][64]: tile (t, ks) is rows (t * K/64 + ks) * 128 ...
+      const uint64_t rows = (uint64_t)((N + gemm::BM - 1) / gemm::BM) * (K / gemm::BK) * gemm::BM;
+      const uint64_t dims[2] = {(uint64_t)gemm::BK, rows};
+      const uint64_t strides[1] = {(uint64_t)gemm::BK * 2};
+      s = make_tmap_bf16(tmW, w, 2, dims, strides, box);
+    } else {
+      const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+      const uint64_t strides[1] = {(uint64_t)K * 2};
+      s = make_tmap_bf16(tmW, w, 2, dims, strides, box);
+    }
     if (s != NDIFF_OK) return s;
   }
   if (tmX) {

@@ -43,6 +43,7 @@ enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV =
 
 struct GemmParams {
   int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
+  int w_tiled;             // W stored as contiguous 128 x 64 tiles (else row-major)
   int S, nks, items;       // K splits, 64-wide K steps, work items (set by the launcher)
   float* ws;               // split partials [items][128][32] fp32 (S > 1)
   int* counters;           // [tiles] arrival counters, zero between launches
@@ -65,8 +66,8 @@ struct GemmPlan {
 
 GemmPlan gemm_plan(int N, int K);
 size_t gemm_partials_bytes(const GemmPlan& pl);
-ndiff_status gemm_make_maps(const void* w, int N, int K, const void* x, int M, CUtensorMap* tmW,
-                            CUtensorMap* tmX);
+ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
+                            CUtensorMap* tmW, CUtensorMap* tmX);
 ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
                               GemmParams p, cudaStream_t stream);
 

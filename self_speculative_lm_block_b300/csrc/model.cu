@@ -187,6 +187,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
   gp.T = T;
+  gp.w_tiled = 1;
   gp.ws = m->gws;
   gp.counters = m->gcnt;
   for (int l = 0; l < m->L; ++l) {
@@ -371,7 +372,9 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   cudaStream_t s = 0;
 
   TRY(dalloc(m, &m->embed, (size_t)m->V * d * esz));
-  TRY(dalloc(m, &m->lm, (size_t)m->V * d * esz));
+  const size_t vpad = (size_t)((m->V + 127) / 128) * 128;  // whole 128-row tiles
+  TRY(dalloc(m, &m->lm, vpad * d * esz));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->lm, 0, vpad * d * esz, s));
   m->layers.resize(m->L);
   const size_t kv_elems = (size_t)m->Hkv * m->Lmax * m->D;
   for (Layer& ly : m->layers) {
@@ -434,38 +437,41 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     m->attn_split = attn_bf16_auto_split(1, m->Hkv, m->Lmax);
     m->aws_bytes = attn_bf16_workspace(1, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
     if (m->aws_bytes) TRY(dalloc(m, &m->aws, m->aws_bytes));
-    TRY(gemm_make_maps(nullptr, 0, m->d, m->h, kBlock, nullptr, &m->tm_h));
-    TRY(gemm_make_maps(nullptr, 0, m->HD, m->ob, kBlock, nullptr, &m->tm_oact));
-    TRY(gemm_make_maps(nullptr, 0, m->ffn, m->ab, kBlock, nullptr, &m->tm_a));
-    TRY(gemm_make_maps(m->lm, m->V, m->d, nullptr, 0, &m->tm_lm, nullptr));
+    TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, kBlock, nullptr, &m->tm_h));
+    TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, kBlock, nullptr, &m->tm_oact));
+    TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, kBlock, nullptr, &m->tm_a));
+    TRY(gemm_make_maps(m->lm, m->V, m->d, true, nullptr, 0, &m->tm_lm, nullptr));
     for (Layer& ly : m->layers) {
-      TRY(gemm_make_maps(ly.wqkv, m->NQKV, m->d, nullptr, 0, &ly.tm_qkv, nullptr));
-      TRY(gemm_make_maps(ly.wo, m->d, m->HD, nullptr, 0, &ly.tm_o, nullptr));
-      TRY(gemm_make_maps(ly.wgu, 2 * m->ffn, m->d, nullptr, 0, &ly.tm_gu, nullptr));
-      TRY(gemm_make_maps(ly.wd, m->d, m->ffn, nullptr, 0, &ly.tm_d, nullptr));
+      TRY(gemm_make_maps(ly.wqkv, m->NQKV, m->d, true, nullptr, 0, &ly.tm_qkv, nullptr));
+      TRY(gemm_make_maps(ly.wo, m->d, m->HD, true, nullptr, 0, &ly.tm_o, nullptr));
+      TRY(gemm_make_maps(ly.wgu, 2 * m->ffn, m->d, true, nullptr, 0, &ly.tm_gu, nullptr));
+      TRY(gemm_make_maps(ly.wd, m->d, m->ffn, true, nullptr, 0, &ly.tm_d, nullptr));
     }
   }
 
   // weights: tensor ids 0 = embedding, 1 + 8 l + j for layer l
   // (j: 0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down), 1 + 8 L = LM head
   const bool b = m->bf16;
-  TRY(launch_init_normal(m->embed, b, 0, m->V, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+  // bf16 projection weights are stored as contiguous 128 x 64 tiles (each TMA
+  // box of the projection kernel is then one 16 KB run of HBM); the embedding
+  // is read by rows and stays row-major.
+  TRY(launch_init_normal(m->embed, b, 0, m->V, m->d, 0, ROWMAP_IDENTITY, false, seed, kSigma, s));
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
     const int64_t kvr = (int64_t)m->Hkv * m->D;
     const int qk_map = b ? ROWMAP_ROPE : ROWMAP_IDENTITY;
-    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 0), m->HD, m->d, 0, qk_map, seed, kSigma, s));
-    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 1), kvr, m->d, m->HD, qk_map, seed, kSigma, s));
-    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 2), kvr, m->d, m->HD + kvr, ROWMAP_IDENTITY, seed,
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 0), m->HD, m->d, 0, qk_map, b, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 1), kvr, m->d, m->HD, qk_map, b, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wqkv, b, tid_layer(l, 2), kvr, m->d, m->HD + kvr, ROWMAP_IDENTITY, b, seed,
                            kSigma, s));
-    TRY(launch_init_normal(ly.wo, b, tid_layer(l, 3), m->d, m->HD, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wo, b, tid_layer(l, 3), m->d, m->HD, 0, ROWMAP_IDENTITY, b, seed, kSigma, s));
     TRY(launch_init_normal(ly.wgu, b, tid_layer(l, 4), m->ffn, m->d, 0, b ? ROWMAP_GATE : ROWMAP_IDENTITY,
-                           seed, kSigma, s));
+                           b, seed, kSigma, s));
     TRY(launch_init_normal(ly.wgu, b, tid_layer(l, 5), m->ffn, m->d, b ? 0 : m->ffn,
-                           b ? ROWMAP_UP : ROWMAP_IDENTITY, seed, kSigma, s));
-    TRY(launch_init_normal(ly.wd, b, tid_layer(l, 6), m->d, m->ffn, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+                           b ? ROWMAP_UP : ROWMAP_IDENTITY, b, seed, kSigma, s));
+    TRY(launch_init_normal(ly.wd, b, tid_layer(l, 6), m->d, m->ffn, 0, ROWMAP_IDENTITY, b, seed, kSigma, s));
   }
-  TRY(launch_init_normal(m->lm, b, 1 + 8 * m->L, m->V, m->d, 0, ROWMAP_IDENTITY, seed, kSigma, s));
+  TRY(launch_init_normal(m->lm, b, 1 + 8 * m->L, m->V, m->d, 0, ROWMAP_IDENTITY, b, seed, kSigma, s));
   TRY(launch_rope_table(m->rope, m->Lmax, m->D, (double)c.rope_base, s));
 
   cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&m->pin), 64 * sizeof(int32_t));
@@ -487,9 +493,10 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
 
 // Locates weight tensor `tid`: storage base, columns, first storage row, row map.
 bool locate(const ndiff_model* m, int tid, const void** base, int64_t* rows, int64_t* cols,
-            int64_t* row_off, int* map) {
+            int64_t* row_off, int* map, bool* tiled) {
   *row_off = 0;
   *map = ROWMAP_IDENTITY;
+  *tiled = m->bf16 && tid != 0;
   if (tid == 0 || tid == 1 + 8 * m->L) {
     *base = tid == 0 ? m->embed : m->lm;
     *rows = m->V;
@@ -665,7 +672,8 @@ ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_
   const void* base = nullptr;
   int64_t rows = 0, cols = 0, row_off = 0;
   int map = 0;
-  if (!locate(m, tensor_id, &base, &rows, &cols, &row_off, &map))
+  bool tiled = false;
+  if (!locate(m, tensor_id, &base, &rows, &cols, &row_off, &map, &tiled))
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_read_weight: no tensor %d", tensor_id);
   if (offset < 0 || count < 0 || offset + count > rows * cols)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_read_weight: range outside the tensor");
@@ -673,7 +681,7 @@ ndiff_status ndiff_model_read_weight(const ndiff_model* m, int tensor_id, int64_
   TRY(set_device(m));
   float* tmp = nullptr;
   NDIFF_CUDA_TRY(cudaMalloc(&tmp, (size_t)count * 4));
-  ndiff_status s = launch_gather_weight(base, m->bf16, cols, row_off, map, offset, count, tmp, 0);
+  ndiff_status s = launch_gather_weight(base, m->bf16, cols, row_off, map, tiled, offset, count, tmp, 0);
   if (s == NDIFF_OK) {
     cudaError_t e = cudaMemcpy(host_out, tmp, (size_t)count * 4, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) s = cuda_error(e, "ndiff_model_read_weight: copy");

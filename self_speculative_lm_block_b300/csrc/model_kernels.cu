@@ -64,8 +64,17 @@ __device__ __forceinline__ int64_t map_row(int64_t row, int map) {
   return row;
 }
 
+// Element (storage row srow, column col) of a weight stored either row-major
+// or as contiguous 128 x 64 tiles (tile (srow/128, col/64) at index
+// (srow/128) * (cols/64) + col/64, rows of 64 elements inside), the layout
+// the projection kernel streams one 16 KB tile at a time.
+__device__ __forceinline__ int64_t store_index(int64_t srow, int64_t col, int64_t cols, int tiled) {
+  if (!tiled) return srow * cols + col;
+  return ((srow / 128) * (cols / 64) + col / 64) * 8192 + (srow % 128) * 64 + (col % 64);
+}
+
 __global__ void init_normal_kernel(void* dst, int is_bf16, int tensor_id, int64_t rows,
-                                   int64_t cols, int64_t row_off, int map, uint64_t seed,
+                                   int64_t cols, int64_t row_off, int map, int tiled, uint64_t seed,
                                    double sigma) {
   const int64_t count = rows * cols;
   const int64_t nblk = (count + 3) / 4;
@@ -81,7 +90,7 @@ __global__ void init_normal_kernel(void* dst, int is_bf16, int tensor_id, int64_
       const int64_t e = n * 4 + j;
       if (e >= count) break;
       const int64_t row = e / cols, col = e % cols;
-      const int64_t at = (map_row(row, map) + row_off) * cols + col;
+      const int64_t at = store_index(map_row(row, map) + row_off, col, cols, tiled);
       const float v = (float)(sigma * z[j]);
       if (is_bf16)
         static_cast<__nv_bfloat16*>(dst)[at] = __float2bfloat16_rn(v);
@@ -92,12 +101,12 @@ __global__ void init_normal_kernel(void* dst, int is_bf16, int tensor_id, int64_
 }
 
 __global__ void gather_weight_kernel(const void* src, int is_bf16, int64_t cols, int64_t row_off,
-                                     int map, int64_t offset, int64_t count, float* out) {
+                                     int map, int tiled, int64_t offset, int64_t count, float* out) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = offset + i;
     const int64_t row = e / cols, col = e % cols;
-    const int64_t at = (map_row(row, map) + row_off) * cols + col;
+    const int64_t at = store_index(map_row(row, map) + row_off, col, cols, tiled);
     out[i] = is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[at])
                      : static_cast<const float*>(src)[at];
   }
@@ -277,21 +286,23 @@ static int grid_for(int64_t work, int threads) {
 }
 
 ndiff_status launch_init_normal(void* dst, bool bf16, int tensor_id, int64_t rows, int64_t cols,
-                                int64_t row_off, int map, uint64_t seed, double sigma,
+                                int64_t row_off, int map, bool tiled, uint64_t seed, double sigma,
                                 cudaStream_t s) {
   const int64_t nblk = (rows * cols + 3) / 4;
   mk::init_normal_kernel<<<grid_for(nblk, 256), 256, 0, s>>>(dst, bf16 ? 1 : 0, tensor_id, rows,
-                                                             cols, row_off, map, seed, sigma);
+                                                             cols, row_off, map, tiled ? 1 : 0,
+                                                             seed, sigma);
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
 }
 
 ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int64_t row_off,
-                                  int map, int64_t offset, int64_t count, float* out,
+                                  int map, bool tiled, int64_t offset, int64_t count, float* out,
                                   cudaStream_t s) {
   if (count <= 0) return NDIFF_OK;
   mk::gather_weight_kernel<<<grid_for(count, 256), 256, 0, s>>>(src, bf16 ? 1 : 0, cols, row_off,
-                                                                map, offset, count, out);
+                                                                map, tiled ? 1 : 0, offset, count,
+                                                                out);
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
 }

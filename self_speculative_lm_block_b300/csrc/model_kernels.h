@@ -15,11 +15,12 @@ namespace ndiff {
 // (the rotate-half RoPE pair). fp32 models store every tensor as is.
 enum { ROWMAP_IDENTITY = 0, ROWMAP_GATE = 1, ROWMAP_UP = 2, ROWMAP_ROPE = 3 };
 
+// tiled: the weight is stored as contiguous 128 x 64 tiles (see store_index).
 ndiff_status launch_init_normal(void* dst, bool bf16, int tensor_id, int64_t rows, int64_t cols,
-                                int64_t row_off, int map, uint64_t seed, double sigma,
+                                int64_t row_off, int map, bool tiled, uint64_t seed, double sigma,
                                 cudaStream_t s);
 ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int64_t row_off,
-                                  int map, int64_t offset, int64_t count, float* out,
+                                  int map, bool tiled, int64_t offset, int64_t count, float* out,
                                   cudaStream_t s);
 ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaStream_t s);
 ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,

@@ -52,6 +52,7 @@ _SIGS = {
     "ndiff_last_error": (ctypes.c_char_p, []),
     "ndiff_status_string": (ctypes.c_char_p, [_I]),
     "ndiff_check": (_I, [_P]),
+    "ndiff_selftest_timeout": (_I, [_I, _P]),
     "ndiff_block_attn": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ, _P]),
     "ndiff_block_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "ndiff_block_attn_split": (_I, [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
@@ -125,6 +126,10 @@ def ndiff_status_string(s: int) -> str:
 
 def ndiff_check(stream=None):
     return _call("ndiff_check", _stream(stream))
+
+
+def ndiff_selftest_timeout(limit_us: int, stream=None):
+    return _call("ndiff_selftest_timeout", limit_us, _stream(stream))
 
 
 def ndiff_block_attn(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lmax, mode, scale, out,

@@ -10,10 +10,13 @@ Bars:
   cross a float32 rounding boundary (rare): at most 1 ulp there.
 - fp32 model logits: |err| <= 1e-4 * max|ref| (float32 arithmetic against the
   float64 definition through a few layers of d <= 128 sums).
-- bf16 model logits: |err| <= 2e-2 + 2e-2 |ref|: the GPU and the oracle round
-  the same tensors to bf16, but the values before rounding differ in their
-  last fp32 bits and the attention probabilities go to the tensor cores as
-  bf16, so single activations can land one bf16 step (2^-8 relative) apart.
+- bf16 model logits: |err| <= 1e-2 max_row|ref| + 2e-2 |ref|. The GPU and the
+  oracle round the same tensors to bf16, but the values before rounding differ
+  in their last fp32 bits and the attention probabilities go to the tensor
+  cores as bf16, so activations can land one bf16 step (2^-8 relative) apart;
+  a logit is a sum over d_model such products, so its error scales with the
+  magnitude of the row's logits, not with an absolute constant (measured:
+  ~0.5% of max_row|ref| at d_model 1024 and at 4096).
 - Tokens: compared up to the first divergence; a divergence is allowed only
   where the oracle's top-2 logit gap is below 1e-3. GPU self-speculation
   tokens equal GPU AR tokens exactly (every kernel computes a row
@@ -56,6 +59,12 @@ def _ocfg(c, dtype):
 def _gpu_model(nd, c, dtype, max_seq=512):
     return nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
                     c["vocab"], dtype=dtype, max_seq=max_seq, seed=c["seed"])
+
+
+def _bf16_logit_tol(ref):
+    """Per-element bar of the bf16 model's logits (see the module docstring)."""
+    ref = np.asarray(ref)
+    return 1e-2 * np.abs(ref).max(axis=-1, keepdims=True) + 2e-2 * np.abs(ref)
 
 
 def _gap(logits_row, excl):
@@ -239,7 +248,7 @@ def test_bf16_forward_logits_match_oracle(nd):
         s.prefill(pr)
         ref = s.forward(blk, mode)
         err = np.abs(got - ref)
-        tol = 2e-2 + 2e-2 * np.abs(ref)
+        tol = _bf16_logit_tol(ref)
         print(f"mode {mode}: max |err| {err.max():.3e}, max |ref| {np.abs(ref).max():.3f}")
         assert (err <= tol).all(), err.max()
     m.close()
@@ -281,3 +290,37 @@ def test_bf16_selfspec_equals_ar_and_tracks_oracle(nd):
     n = _compare_tokens(ar[:24], ref, gaps)
     print(f"GPU AR tokens compared with the oracle: {n} of 24")
     m.close()
+
+
+def test_bf16_full_width_two_layer_truncation(nd):
+    """The 8B shape at full width (d_model 4096, 32/8 heads x 128, SwiGLU 12288,
+    vocab 151936, bf16) cut to two layers: causal block logits against the
+    float64 oracle at 600 sampled vocabulary rows plus the rows the GPU ranks
+    highest, and the GPU argmax among them."""
+    c = dict(synth.MODEL_8B)
+    c["layers"] = 2
+    cfg = _ocfg(c, "bf16")
+    pr = synth.prompt(16, c["vocab"], 21)
+    blk = [int(pr[-1])] + [int(t) for t in synth.prompt(3, c["vocab"], 22)]
+    m = _gpu_model(nd, c, "bf16", max_seq=64)
+    m.prefill(pr)
+    got = m.forward(blk, OA.CAUSAL)
+    m.close()
+    top = np.argsort(-got, axis=1)[:, :8].reshape(-1)
+    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(c["vocab"], 600, replace=False),
+                                     top, [0, c["vocab"] - 1]]))
+    s = OM.Session(cfg, OM.Weights(cfg), max_seq=64)
+    s.prefill(pr)
+    ref = s.forward(blk, OA.CAUSAL, vocab_rows=rows)
+    g = got[:, rows]
+    err = np.abs(g - ref)
+    print(f"full-width 2-layer: max |err| {err.max():.3e}, max |ref| {np.abs(ref).max():.3f}")
+    assert (err <= _bf16_logit_tol(ref)).all(), err.max()
+    # the GPU's argmax over the whole vocabulary is among the checked rows; the
+    # oracle agrees on it unless its top-2 gap there is below the error bar
+    for t in range(len(blk)):
+        j = int(np.argmax(np.where(rows == c["vocab"] - 1, -np.inf, ref[t])))
+        gpu_id = int(np.argmax(got[t, :-1]))
+        if rows[j] != gpu_id:
+            jg = int(np.nonzero(rows == gpu_id)[0][0])
+            assert ref[t, j] - ref[t, jg] < 4e-2, (t, rows[j], gpu_id)

@@ -28,6 +28,19 @@ def test_philox_matches_numpy_bit_generator():
         assert [int(x) for x in got0] + [int(x) for x in got1] == [int(x) for x in ref]
 
 
+def test_raw_blocks_equal_the_definition():
+    """The bulk generator (NumPy's C Philox started one block early) gives the
+    same words as the pure-NumPy definition, including the counter edges
+    (block 0 of tensor 0 and of tensor 5)."""
+    for seed, tid, n0, nb in ((0, 0, 0, 7), (1005, 5, 0, 3), (77, 9, 12345, 11), (3, 0, 2**40, 4)):
+        got = philox.raw_blocks(seed, tid, n0, nb)
+        n = np.arange(n0, n0 + nb, dtype=np.uint64)
+        ref = philox.philox4x64_10(n, np.uint64(tid), np.uint64(0), np.uint64(0),
+                                   np.uint64(seed), np.uint64(0))
+        for a, b in zip(got, ref):
+            assert np.array_equal(a, b)
+
+
 def test_box_muller_closed_forms():
     top = np.uint64((2**53 - 1) << 11)   # u1 = 1 -> r = 0
     z0, z1 = philox.box_muller(np.array([top]), np.array([np.uint64(0)]))
