@@ -340,12 +340,20 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int c = 0; c < MT / 4; ++c)
           if (c * 4 < p.T)
             __stcg(part + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
-        __threadfence();
+        // The barrier orders the group's partial stores before thread 0's
+        // release-acquire increment (cumulative at GPU scope); the last split
+        // to arrive then sees every other split's partial.
         bar_sync128();
-        if (tid == 0) *last_flag = (atomicAdd(&p.counters[tile], 1) == p.S - 1) ? 1 : 0;
+        if (tid == 0) {
+          int old;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                       : "=r"(old)
+                       : "l"(p.counters + tile)
+                       : "memory");
+          *last_flag = (old == p.S - 1) ? 1 : 0;
+        }
         bar_sync128();
         if (!*last_flag) continue;
-        __threadfence();
         // sum the splits in order 0..S-1; every split's loads are issued together
         float acc[MT];
 #pragma unroll
@@ -394,17 +402,19 @@ GemmPlan gemm_plan(int N, int K) {
   pl.nks = K / gemm::BK;
   const int sms = num_sms();
   // Cost of a split count S: the busiest CTA's k-steps (16 KB of weights
-  // each) plus, when split, the partial tile it writes and the last split's
-  // reads (about two k-steps' worth). Ties keep the smaller S.
+  // each) plus, when split, about eight k-steps' worth for the partial tile
+  // and the last split's merge. Splits stay at three or fewer: on B300 every
+  // projection of the model measured slower with more (the merge epilogue
+  // then outlasts an item's main loop). Ties keep the larger S.
   long long best = -1;
   int bestS = 1;
-  const int smax = pl.nks < 32 ? pl.nks : 32;
+  const int smax = pl.nks < 3 ? pl.nks : 3;
   for (int S = 1; S <= smax; ++S) {
     const long long items = (long long)pl.ntiles * S;
     const long long waves = (items + sms - 1) / sms;
     const long long steps = (pl.nks + S - 1) / S;
-    const long long cost = waves * (steps + (S > 1 ? 2 : 0));
-    if (best < 0 || cost < best) {
+    const long long cost = waves * (steps + (S > 1 ? 8 : 0));
+    if (best < 0 || cost <= best) {
       best = cost;
       bestS = S;
     }
