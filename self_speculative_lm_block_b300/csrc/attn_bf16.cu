@@ -70,6 +70,8 @@ struct Params {
   __nv_bfloat16* out;
   float* ws_o;        // [B][Hkv][nsplit_max][128][128]
   float2* ws_ml;      // [B][Hkv][nsplit_max][128]
+  const int32_t* order;  // [B * nsplit_max] items (b * nsplit_max + split), longest first;
+                         // nullptr: the grid is (nsplit_max, Hkv, B) in natural order
   unsigned int* status;
 };
 
@@ -145,8 +147,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  const int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   griddep_wait();
+  int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  if (p.order != nullptr) {  // 1-D grid: item rank * Hkv + kv head
+    const int item = p.order[blockIdx.x / p.Hkv];
+    g = blockIdx.x % p.Hkv;
+    b = item / p.nsplit_max;
+    s_idx = item % p.nsplit_max;
+  }
   int P = p.kv_len[b];
   P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
   const int nkeys = P + p.T;
@@ -528,6 +536,88 @@ __global__ void __launch_bounds__(128)
   *reinterpret_cast<uint2*>(dst) = v;
 }
 
+// Launch order of the (sequence, KV split) items of a batch with ragged
+// prefixes: longest first. One CTA runs per SM and the hardware hands out
+// CTAs in grid order, so this is list scheduling; taking the longest items
+// first keeps a long item from starting last and leaving the other SMs idle
+// (the longest-processing-time rule). A counting sort on the item's number of
+// 64-key tiles: count, scan from the longest bucket down, scatter. The order
+// inside a bucket is whatever the atomics give; it changes no result, since
+// every item writes its own output and the merge reads the splits in split
+// order.
+constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_BUCKETS = 4096;
+
+__device__ __forceinline__ int plan_key(const int32_t* kv_len, int it, int T, int Lmax, int split,
+                                        int nsplit, int nb) {
+  const int b = it / nsplit, s = it % nsplit;
+  int P = kv_len[b];
+  P = P < 0 ? 0 : (P > Lmax - T ? Lmax - T : P);
+  int len = P + T - s * split;
+  if (len <= 0) return 0;
+  len = len < split ? len : split;
+  const int t = (len + BN - 1) / BN;
+  return t < nb - 1 ? t : nb - 1;
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS)
+    attn_plan_kernel(const int32_t* __restrict__ kv_len, int B, int T, int Lmax, int split,
+                     int nsplit, int32_t* __restrict__ order) {
+  __shared__ int cnt[PLAN_BUCKETS];
+  __shared__ int warp_sum[PLAN_THREADS / 32];
+  griddep_launch();
+  griddep_wait();
+  const int tid = threadIdx.x;
+  const int nb = min(split / BN + 1, PLAN_BUCKETS);
+  for (int i = tid; i < PLAN_BUCKETS; i += PLAN_THREADS) cnt[i] = 0;
+  __syncthreads();
+  const int n = B * nsplit;
+  for (int it = tid; it < n; it += PLAN_THREADS)
+    atomicAdd(&cnt[plan_key(kv_len, it, T, Lmax, split, nsplit, nb)], 1);
+  __syncthreads();
+  // Exclusive scan over the buckets from the longest (nb - 1) down to 0:
+  // thread j owns reversed positions 4j .. 4j+3.
+  constexpr int PER = PLAN_BUCKETS / PLAN_THREADS;
+  int c[PER], local = 0;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int r = tid * PER + k;
+    c[k] = r < nb ? cnt[nb - 1 - r] : 0;
+    local += c[k];
+  }
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = warp_sum[lane], xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += y;
+    }
+    warp_sum[lane] = xi - x;  // exclusive prefix of the warp totals
+  }
+  __syncthreads();
+  int start = warp_sum[w] + incl - local;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int r = tid * PER + k;
+    if (r < nb) cnt[nb - 1 - r] = start;
+    start += c[k];
+  }
+  __syncthreads();
+  for (int it = tid; it < n; it += PLAN_THREADS) {
+    const int pos = atomicAdd(&cnt[plan_key(kv_len, it, T, Lmax, split, nsplit, nb)], 1);
+    order[pos] = it;
+  }
+}
+
 }  // namespace attn
 
 // KV split length (keys per CTA) for a launch of B x Hkv sequences of at most
@@ -558,12 +648,22 @@ int attn_bf16_auto_split(int B, int Hkv, int Lmax) {
   return best_split;
 }
 
+// Workspace: the per-split partial results when the keys are split, then,
+// for a batch of more than one sequence, the launch order of its items.
+static size_t attn_partials_bytes(int B, int Hkv, int nsplit) {
+  if (nsplit <= 1) return 0;
+  return (size_t)B * Hkv * nsplit * attn::ROWS * (attn::DH * sizeof(float) + sizeof(float2));
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
   (void)T;
   (void)Hq;
   const int nsplit = (Lmax + split - 1) / split;
-  if (nsplit <= 1) return 0;
-  return (size_t)B * Hkv * nsplit * attn::ROWS * (attn::DH * sizeof(float) + sizeof(float2));
+  size_t bytes = attn_partials_bytes(B, Hkv, nsplit);
+  if (B > 1) bytes = round256(bytes) + round256((size_t)B * nsplit * sizeof(int32_t));
+  return bytes;
 }
 
 ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
@@ -601,10 +701,14 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   prm.nsplit_max = nsplit;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.ws_o = static_cast<float*>(ws);
-  prm.ws_ml = need ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
-                                               (size_t)B * Hkv * nsplit * attn::ROWS *
-                                                   attn::DH * sizeof(float))
-                   : nullptr;
+  const size_t partials = attn_partials_bytes(B, Hkv, nsplit);
+  prm.ws_ml = partials ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +
+                                                   (size_t)B * Hkv * nsplit * attn::ROWS *
+                                                       attn::DH * sizeof(float))
+                       : nullptr;
+  int32_t* order = B > 1 ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + round256(partials))
+                         : nullptr;
+  prm.order = order;
   prm.status = device_status_word();
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -616,6 +720,11 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
     attr_set[dev] = true;
   }
   dim3 grid(nsplit, Hkv, B);
+  if (order != nullptr) {
+    NDIFF_CUDA_TRY(launch_k(attn::attn_plan_kernel, dim3(1), dim3(attn::PLAN_THREADS), 0, stream,
+                            kv_len, B, T, Lmax, split, nsplit, order));
+    grid = dim3(nsplit * Hkv * B, 1, 1);
+  }
   NDIFF_CUDA_TRY(launch_k(attn::attn_bf16_kernel, grid, dim3(attn::THREADS),
                           (size_t)attn::SMEM_BYTES, stream, tk, tv, prm));
   if (nsplit > 1) {

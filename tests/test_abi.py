@@ -67,8 +67,13 @@ def test_host_side_validation_without_gpu(nd):
 
 
 def test_workspace_sizes(nd):
-    # one split per (b, g): no scratch; many splits: scratch grows with them
-    assert nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 512) == 0
+    # one sequence, one split: no scratch
+    assert nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 1, 32, 32, 8, 128, 512, 512) == 0
+    # one sequence, four splits: the partial results (fp32 O rows + (m, l) per row)
+    w = nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 1, 32, 32, 8, 128, 512, 128)
+    assert w == 1 * 8 * 4 * 128 * (128 * 4 + 8)
+    # a batch adds its launch order (one int per (sequence, split), 256-byte granules)
+    assert nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 512) == 256
     w = nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 128)
-    assert w == 2 * 8 * 4 * 128 * (128 * 4 + 8)
+    assert w == 2 * 8 * 4 * 128 * (128 * 4 + 8) + 256
     assert nd.ndiff_block_attn_workspace_size(nd.NDIFF_F32, 2, 32, 4, 4, 32, 512) == 0

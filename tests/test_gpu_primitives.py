@@ -76,6 +76,22 @@ def test_attn_bf16_many_ragged_sequences(nd, mode):
     assert np.abs(got - alt).max() <= 2e-2
 
 
+@pytest.mark.parametrize("split", [128, 1408])
+def test_attn_bf16_batch_equals_single_sequences(nd, split):
+    """A batch is launched longest item first; every sequence's rows are the
+    same bits as a launch of that sequence alone with the same split grid."""
+    B, T, Lmax = 6, 32, 1400
+    lengths = [0, 5, 100, 1368, 700, 64]
+    inp = synth.attn_inputs(B, T, 32, 8, 128, lengths, Lmax, 43, fill_tail=float("nan"))
+    q, k, v = inp.q.cuda(), inp.k_cache.cuda(), inp.v_cache.cuda()
+    both = nd.block_attn(q, k, v, inp.kv_len.cuda(), 1, inp.scale, split_keys=split)
+    for b in range(B):
+        one = nd.block_attn(q[b:b + 1].contiguous(), k[b:b + 1].contiguous(),
+                            v[b:b + 1].contiguous(), inp.kv_len[b:b + 1].cuda(), 1, inp.scale,
+                            split_keys=split)
+        assert torch.equal(one[0], both[b]), b
+
+
 def test_attn_bf16_gqa_group_2_and_mha(nd):
     _attn_check(nd, 2, 32, 16, 8, 128, [100, 40], 200, 0, seed=31)      # G = 2
     _attn_check(nd, 2, 16, 8, 1, 128, [100, 40], 200, 1, seed=32)       # G = 8, T = 16
