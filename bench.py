@@ -351,6 +351,61 @@ def run_model(rank, n_tokens, steps=1):
     return out
 
 
+def run_lm_head(reps=20):
+    """The 8B LM head (151936 x 4096 bf16, 1.24 GB: larger than L2) at a
+    32-token block and at one token: the fused argmax/confidence epilogue
+    against the GEMM that stores fp32 logits followed by the reduce kernel.
+    Device-timed CUDA-graph replays of `reps` calls each."""
+    import torch
+    from self_speculative_lm_block_b300 import ndiff as nd
+    from self_speculative_lm_block_b300 import synth
+    V, d = synth.MODEL_8B["vocab"], synth.MODEL_8B["d_model"]
+    gen = torch.Generator(device="cuda").manual_seed(1005)
+    w = (torch.randn((V, d), device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    out = {"shape": f"{V} x {d} bf16", "weight_bytes": V * d * 2}
+    s = torch.cuda.Stream()
+
+    def time_graph(fn):
+        with torch.cuda.stream(s):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()                       # replays on the current stream: s
+            e1.record(s)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    for M in (1, 32):
+        x = torch.randn((M, d), device="cuda", generator=gen).to(torch.bfloat16)
+        ids = torch.empty(M, dtype=torch.int32, device="cuda")
+        conf = torch.empty(M, dtype=torch.float32, device="cuda")
+        need_f = nd.ndiff_lm_head_argmax_workspace_size(M, V, d)
+        ws_f = torch.empty(need_f, dtype=torch.uint8, device="cuda")
+        y = torch.empty((M, V), dtype=torch.float32, device="cuda")
+        need_g = nd.ndiff_gemm_bf16_workspace_size(M, V, d)
+        ws_g = torch.empty(max(need_g, 16), dtype=torch.uint8, device="cuda")
+        st = s.cuda_stream
+
+        def fused():
+            nd.ndiff_lm_head_argmax(x, w, M, V, d, V - 1, ids, conf, ws_f, need_f, st)
+
+        def unfused():
+            nd.ndiff_gemm_bf16(x, w, M, V, d, y, V, ws_g, need_g, st)
+            nd.ndiff_logits_reduce(nd.NDIFF_F32, y, M, V, V, V - 1, ids, conf, st)
+
+        tf, tu = time_graph(fused), time_graph(unfused)
+        out[f"tokens_{M}"] = {"fused_us": tf, "unfused_us": tu,
+                              "fused_weight_gbs": V * d * 2 / (tf * 1e-6) / 1e9}
+    return out
+
+
 def make_workload(name, rank):
     if name.startswith("attn-"):
         return AttnWorkload(name, rank)
@@ -480,6 +535,7 @@ def main():
     e2e_val = wl.step_bytes * world / (e2e_ms * 1e-3) / 1e9
 
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
+    lm_head = run_lm_head() if args.model_tokens > 0 else None
     if model is not None and world > 1:
         for k in ("ar", "selfspec"):
             t = torch.tensor([model[k]["tokens_per_s"]], device="cuda", dtype=torch.float64)
@@ -505,6 +561,8 @@ def main():
                "clocks": clk.summary()}
         if model is not None:
             out["model_8b"] = model
+        if lm_head is not None:
+            out["lm_head_8b"] = lm_head
         if not args.no_cpu_baseline:
             cv, desc, dt = wl.oracle_sample()
             out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": _oracle_threads(),

@@ -227,6 +227,30 @@ NDIFF_API ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int 
                                        int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * LM head with the logits reduction fused in: for token rows m < M,
+ *   logits[m][n] = sum_k x[m][k] * w[n][k]   (n < N, never stored)
+ *   argmax[m], conf[m] = the reduction of ndiff_logits_reduce over that row
+ *   (smallest id of the largest logit with exclude_id left out; its softmax
+ *   probability over all N ids).
+ * This is the greedy decision of AR decoding and verification, and the
+ * confidence of the unmask step, taken straight from the last hidden state
+ * ([FFI] "三种生成模式"; [HFB]: decode is bound by memory traffic, and this
+ * removes the write and re-read of the [M][N] logits).
+ * x: bf16 [M][K] row-major, w: bf16 [N][K] row-major (16-byte aligned);
+ * 1 <= M <= 32, N >= 1, K a positive multiple of 64, -1 <= exclude_id < N.
+ * argmax int32 [M], conf float [M] (device). The logits are the fp32 values
+ * ndiff_gemm_bf16 produces, so argmax equals ndiff_gemm_bf16 followed by
+ * ndiff_logits_reduce exactly; conf agrees to fp32 rounding. A row's results
+ * do not depend on M.
+ * ws/ws_bytes: device scratch of at least ndiff_lm_head_argmax_workspace_size()
+ *   bytes; contents need no initialisation.
+ * ------------------------------------------------------------------------ */
+NDIFF_API size_t ndiff_lm_head_argmax_workspace_size(int M, int N, int K);
+NDIFF_API ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M, int N, int K,
+                                            int exclude_id, int32_t* argmax, float* conf, void* ws,
+                                            size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Random-init tri-mode model (one checkpoint, three modes: [FFI]
  * "三种生成模式"; [AIF] "方法 / 推理").
  * Pre-norm transformer: x = E[ids]; per layer
@@ -234,9 +258,14 @@ NDIFF_API ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int 
  *   x += BlockAttn(q,k,v) Wo^T; h = RMSNorm(x); x += (silu(h Wg^T) * h Wu^T) Wd^T;
  * logits = RMSNorm(x) Wlm^T. RMSNorm gain 1, eps cfg.eps, RoPE rotate-half with
  * base cfg.rope_base. Every weight ~ N(0, 0.02^2) drawn with Philox4x64-10
- * (Salmon et al., SC'11) and Box-Muller from `seed` (see DESIGN notes in the
- * repository for the exact counter layout). The [MASK] id is vocab-1 and is
- * never predicted.
+ * (Salmon et al., SC'11) and Box-Muller from `seed`: element i of tensor t
+ * takes the output words (w0..w3) of counter (i/4, t, 0, 0) under key
+ * (seed, 0); lanes i%4 = 0/1 use (w0, w1), lanes 2/3 use (w2, w3), with
+ * u1 = ((wa >> 11) + 1) 2^-53, u2 = (wb >> 11) 2^-53, z = sqrt(-2 ln u1) times
+ * cos (even lane) or sin (odd lane) of 2 pi u2; the weight is float(0.02 z),
+ * then bf16 (round to nearest even) for bf16 models. Tensor ids: 0 embedding,
+ * 1 + 8 l + j for layer l (j = 0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down),
+ * 1 + 8 layers the LM head. The [MASK] id is vocab-1 and is never predicted.
  * dtype NDIFF_F32: fp32 weights/activations (tiny configs: d_model <= 1024,
  *   head_dim <= 64, vocab <= 65536).
  * dtype NDIFF_BF16: bf16 weights, bf16 GEMM inputs, fp32 residual stream and

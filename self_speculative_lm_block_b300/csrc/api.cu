@@ -328,4 +328,49 @@ ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, 
   return launch_gemm_bf16(tw, tx, pl, p, stream);
 }
 
+size_t ndiff_lm_head_argmax_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 64) return 0;
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  const size_t part = (gemm_partials_bytes(pl) + 255) & ~(size_t)255;
+  return cnt + part + (size_t)pl.ntiles * 32 * sizeof(float4);
+}
+
+ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M, int N, int K, int exclude_id,
+                                  int32_t* argmax, float* conf, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0 || exclude_id < -1 || exclude_id >= N)
+    return set_error(NDIFF_ERR_INVALID_ARG,
+                     "ndiff_lm_head_argmax: need 1<=M<=32, N>=1, K a positive multiple of 64, "
+                     "-1<=exclude_id<N (M=%d N=%d K=%d exclude_id=%d)",
+                     M, N, K, exclude_id);
+  if (!x || !w || !argmax || !conf)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_lm_head_argmax: null pointer");
+  if (!aligned16(x) || !aligned16(w))
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_lm_head_argmax: x and w must be 16-byte aligned");
+  const size_t need = ndiff_lm_head_argmax_workspace_size(M, N, K);
+  if (!ws || ws_bytes < need)
+    return set_error(NDIFF_ERR_WORKSPACE,
+                     "ndiff_lm_head_argmax: workspace of %zu bytes needed, %zu given", need, ws_bytes);
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  const size_t part = (gemm_partials_bytes(pl) + 255) & ~(size_t)255;
+  CUtensorMap tw, tx;
+  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
+  if (s != NDIFF_OK) return s;
+  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.N = N;
+  p.T = M;
+  p.mode = GEMM_EPI_ARGMAX;
+  p.counters = static_cast<int*>(ws);
+  p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt);
+  p.red = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + cnt + part);
+  p.excl = exclude_id;
+  s = launch_gemm_bf16(tw, tx, pl, p, stream);
+  if (s != NDIFF_OK) return s;
+  return launch_argmax_merge(p.red, pl.ntiles, M, argmax, conf, stream);
+}
+
 }  // extern "C"

@@ -54,7 +54,9 @@ constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_BYTES = MT * BK * 2;       // 4 KB
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NST * A_BYTES;
-constexpr int OFF_BAR = OFF_B + NST * B_BYTES;
+constexpr int OFF_RED = OFF_B + NST * B_BYTES;   // ARGMAX: [4 warps][32 tokens] float4
+constexpr int RED_BYTES = 4 * MT * 16;
+constexpr int OFF_BAR = OFF_RED + RED_BYTES;
 constexpr int N_BARS = 2 * NST + 4 + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
 constexpr int TMEM_COLS = 64;              // two 32-column accumulators
@@ -177,6 +179,118 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, f
   }
 }
 
+// ---------------------------------------------------------------- ARGMAX
+// The LM head with the greedy decision fused in: instead of storing logits,
+// each finished 128-row vocabulary tile leaves, per token row, the running
+// softmax state (max m, sum of exp(y - m)) and the best allowed (value, id),
+// ties to the lower id. A second kernel merges the tiles in tile order.
+constexpr float L2E = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct Red {
+  float m, s, bv;
+  int bi;
+};
+
+__device__ __forceinline__ void red_merge(Red& a, const Red& b) {
+  if (b.m > a.m) {
+    a.s = b.s + (a.m == -INFINITY ? 0.f : a.s * ex2f((a.m - b.m) * L2E));
+    a.m = b.m;
+  } else {
+    a.s += (b.m == -INFINITY ? 0.f : b.s * ex2f((b.m - a.m) * L2E));
+  }
+  if (b.bv > a.bv || (b.bv == a.bv && b.bi < a.bi)) {
+    a.bv = b.bv;
+    a.bi = b.bi;
+  }
+}
+
+__device__ __forceinline__ Red red_shfl(const Red& a, int off) {
+  Red o;
+  o.m = __shfl_xor_sync(0xffffffffu, a.m, off);
+  o.s = __shfl_xor_sync(0xffffffffu, a.s, off);
+  o.bv = __shfl_xor_sync(0xffffffffu, a.bv, off);
+  o.bi = __shfl_xor_sync(0xffffffffu, a.bi, off);
+  return o;
+}
+
+// One halving step of the warp transpose-reduction: the lane keeps the half
+// of its W columns selected by its `off` bit and merges in the partner's copy
+// of that half.
+template <int W>
+__device__ __forceinline__ void red_halve(Red (&a)[W], Red (&o)[W / 2], int lane, int off) {
+  const bool hi = (lane & off) != 0;
+#pragma unroll
+  for (int j = 0; j < W / 2; ++j) {
+    Red keep = hi ? a[j + W / 2] : a[j];
+    const Red send = hi ? a[j] : a[j + W / 2];
+    red_merge(keep, red_shfl(send, off));
+    o[j] = keep;
+  }
+}
+
+// Thread r of the epilogue holds y[vocab n = tile*128 + r][token m] in v[m].
+__device__ __forceinline__ void epilogue_argmax(const GemmParams& p, int tile, int r, int lane,
+                                                int quarter, const float (&v)[MT], float4* sred) {
+  const int n = tile * BM + r;
+  const bool valid = n < p.N;
+  const bool allowed = valid && n != p.excl;
+  // step 1 (offset 16) starts from single elements
+  Red a16[16];
+  {
+    const bool hi = (lane & 16) != 0;
+    const int n2 = n ^ 16;
+    const bool valid2 = n2 < p.N, allowed2 = valid2 && n2 != p.excl;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float keep = hi ? v[j + 16] : v[j];
+      const float send = hi ? v[j] : v[j + 16];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      const float x0 = valid ? keep : -INFINITY;
+      const float x1 = valid2 ? recv : -INFINITY;
+      Red t;
+      t.m = fmaxf(x0, x1);
+      t.s = (t.m == -INFINITY) ? 0.f
+                               : ((x0 == -INFINITY ? 0.f : ex2f((x0 - t.m) * L2E)) +
+                                  (x1 == -INFINITY ? 0.f : ex2f((x1 - t.m) * L2E)));
+      const float b0 = allowed ? keep : -INFINITY, b1 = allowed2 ? recv : -INFINITY;
+      const int i0 = allowed ? n : 0x7fffffff, i1 = allowed2 ? n2 : 0x7fffffff;
+      const bool take1 = b1 > b0 || (b1 == b0 && i1 < i0);
+      t.bv = take1 ? b1 : b0;
+      t.bi = take1 ? i1 : i0;
+      a16[j] = t;
+    }
+  }
+  Red a8[8], a4[4], a2[2], a1[1];
+  red_halve<16>(a16, a8, lane, 8);
+  red_halve<8>(a8, a4, lane, 4);
+  red_halve<4>(a4, a2, lane, 2);
+  red_halve<2>(a2, a1, lane, 1);
+  // lane l now holds token column l over this warp's 32 vocabulary rows
+  sred[quarter * MT + lane] = make_float4(a1[0].m, a1[0].s, a1[0].bv, __int_as_float(a1[0].bi));
+  bar_sync128();
+  if (quarter == 0 && lane < p.T) {
+    float4 f = sred[lane];
+    Red acc{f.x, f.y, f.z, __float_as_int(f.w)};
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      f = sred[q * MT + lane];
+      red_merge(acc, Red{f.x, f.y, f.z, __float_as_int(f.w)});
+    }
+    __stcg(p.red + (size_t)tile * MT + lane, make_float4(acc.m, acc.s, acc.bv, __int_as_float(acc.bi)));
+  }
+  bar_sync128();
+}
+
+// ARGMAX selects the LM-head epilogue at compile time: a separate
+// instantiation keeps that epilogue's registers and code out of the
+// projections' kernel (measured 7% slower decode when both shared one body).
+template <bool ARGMAX>
 __global__ void __launch_bounds__(THREADS, 2)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const GemmParams p) {
@@ -185,6 +299,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem + OFF_A;
   uint8_t* sB = smem + OFF_B;
+  float4* sred = reinterpret_cast<float4*>(smem + OFF_RED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = full + NST;
@@ -382,7 +497,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int m = 0; m < MT; ++m) v[m] = acc[m];
         if (tid == 0) p.counters[tile] = 0;
       }
-      epilogue(p, tile, r, v);
+      if constexpr (ARGMAX)
+        epilogue_argmax(p, tile, r, lane, quarter, v, sred);
+      else
+        epilogue(p, tile, r, v);
     }
   }
 
@@ -394,7 +512,49 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
 }
 
+// Merges the per-tile partials of one token row in tile order: each of the
+// 256 threads folds tiles tid, tid + 256, ..., then the threads merge by
+// warp shuffles and the warps in order through shared memory.
+constexpr int MERGE_THREADS = 256;
+
+__global__ void __launch_bounds__(MERGE_THREADS)
+    argmax_merge_kernel(const float4* __restrict__ red, int ntiles, int32_t* __restrict__ argmax,
+                        float* __restrict__ conf) {
+  griddep_launch();
+  griddep_wait();
+  const int t = blockIdx.x;
+  Red a{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+  for (int i = threadIdx.x; i < ntiles; i += MERGE_THREADS) {
+    const float4 f = __ldcg(red + (size_t)i * MT + t);
+    red_merge(a, Red{f.x, f.y, f.z, __float_as_int(f.w)});
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) red_merge(a, red_shfl(a, off));
+  __shared__ Red sh[MERGE_THREADS / 32];
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Red acc = sh[0];
+    for (int w = 1; w < MERGE_THREADS / 32; ++w) red_merge(acc, sh[w]);
+    if (acc.bi == 0x7fffffff) {
+      argmax[t] = -1;
+      conf[t] = 0.f;
+    } else {
+      argmax[t] = acc.bi;
+      conf[t] = ex2f((acc.bv - acc.m) * L2E) / acc.s;
+    }
+  }
+}
+
 }  // namespace gemm
+
+ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int32_t* argmax, float* conf,
+                                 cudaStream_t stream) {
+  if (T <= 0) return NDIFF_OK;
+  NDIFF_CUDA_TRY(launch_k(gemm::argmax_merge_kernel, dim3(T), dim3(gemm::MERGE_THREADS), 0, stream,
+                          red, ntiles, argmax, conf));
+  return NDIFF_OK;
+}
 
 GemmPlan gemm_plan(int N, int K) {
   GemmPlan pl;
@@ -463,7 +623,10 @@ ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, co
   int dev = 0;
   NDIFF_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 64 && !attr_set[dev]) {
-    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel,
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        gemm::SMEM_BYTES));
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel<true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         gemm::SMEM_BYTES));
     attr_set[dev] = true;
@@ -472,8 +635,12 @@ ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, co
   p.nks = pl.nks;
   p.items = pl.items;
   p.status = device_status_word();
-  NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel, dim3(pl.grid), dim3(gemm::THREADS),
-                          (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
+  if (p.mode == GEMM_EPI_ARGMAX)
+    NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel<true>, dim3(pl.grid), dim3(gemm::THREADS),
+                            (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
+  else
+    NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel<false>, dim3(pl.grid), dim3(gemm::THREADS),
+                            (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
   return NDIFF_OK;
 }
 

@@ -39,7 +39,7 @@ ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, i
                                   int32_t* kv_len, cudaStream_t stream);
 
 // gemm_bf16.cu — y = x W^T for at most 32 token rows, with fused epilogues
-enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3 };
+enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3, GEMM_EPI_ARGMAX = 4 };
 
 struct GemmParams {
   int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
@@ -58,6 +58,9 @@ struct GemmParams {
   int Hq, Hkv, Lmax;
   const int32_t* kv_len;   // QKV: committed prefix (batch 1)
   const float2* rope;      // QKV: (cos, sin) [Lmax][64]
+  float4* red;             // ARGMAX: per (tile, token row) (max, sum of exp(y - max),
+                           // best allowed value, its id as int bits) [tiles][32]
+  int excl;                // ARGMAX: id left out of the argmax (-1: none)
 };
 
 struct GemmPlan {
@@ -70,5 +73,9 @@ ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const voi
                             CUtensorMap* tmW, CUtensorMap* tmX);
 ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
                               GemmParams p, cudaStream_t stream);
+// Merges the per-tile partials of a GEMM_EPI_ARGMAX launch: argmax[t] and the
+// softmax probability conf[t] of that id for token rows t < T.
+ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int32_t* argmax, float* conf,
+                                 cudaStream_t stream);
 
 }  // namespace ndiff

@@ -95,6 +95,7 @@ struct ndiff_model {
   int32_t* prompt = nullptr;    // [Lmax]
   float2* rope = nullptr;       // [Lmax][D/2]
   float* gws = nullptr;         // GEMM split partials
+  float4* red = nullptr;        // LM head per-tile argmax partials [tiles][32]
   int* gcnt = nullptr;          // GEMM tile counters
   void* aws = nullptr;          // attention split-KV scratch
   size_t aws_bytes = 0;
@@ -176,10 +177,16 @@ ndiff_status check_config(const ndiff_model_config* c) {
 }
 
 // ---------------------------------------------------------------- one forward
-// Runs the T (<= 32) tokens `ids` (device) at positions kv_len .. kv_len+T-1,
-// writes their K/V into the cache there, and (want_logits) leaves fp32 logits
-// in m->logits and the argmax / confidence of every row in m->pred / m->conf.
-ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool want_logits,
+// What a forward leaves behind: nothing (the KV cache only), the argmax /
+// confidence of every row in m->pred / m->conf, or those plus the fp32 logits
+// in m->logits. For bf16 models FWD_TOKENS never stores logits: the LM head
+// GEMM reduces each 128-id vocabulary tile in its epilogue and a merge kernel
+// folds the tiles.
+enum { FWD_NONE = 0, FWD_TOKENS = 1, FWD_LOGITS = 2 };
+
+// Runs the T (<= 32) tokens `ids` (device) at positions kv_len .. kv_len+T-1
+// and writes their K/V into the cache there.
+ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int out,
                      cudaStream_t s) {
   PdlScope pdl(m->bf16);
   const float scale = 1.f / sqrtf((float)m->D);
@@ -249,8 +256,17 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, bool
       TRY(launch_resid_add_f32(m->x, m->y, T * m->d, s));
     }
   }
-  if (!want_logits) return NDIFF_OK;
+  if (out == FWD_NONE) return NDIFF_OK;
   TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, m->bf16, s));
+  if (m->bf16 && out == FWD_TOKENS) {
+    GemmParams p = gp;
+    p.N = m->V;
+    p.mode = GEMM_EPI_ARGMAX;
+    p.red = m->red;
+    p.excl = m->mask_id;
+    TRY(launch_gemm_bf16(m->tm_lm, m->tm_h, m->pl_lm, p, s));
+    return launch_argmax_merge(m->red, m->pl_lm.ntiles, T, m->pred, m->conf, s);
+  }
   if (m->bf16) {
     GemmParams p = gp;
     p.N = m->V;
@@ -271,7 +287,7 @@ ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
   const int k = kBlock / steps;
   TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev, m->mask_id, s));
   for (int i = 0; i < steps; ++i) {
-    TRY(forward(m, m->block_in, kBlock, 0, true, s));
+    TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, s));
     TRY(launch_unmask(m->conf, m->pred, 1, kBlock, k, m->mask, m->block_in, m->draft, m->chosen, s));
   }
   return NDIFF_OK;
@@ -282,17 +298,17 @@ ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
 ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStream_t s) {
   if (mode == NDIFF_MODE_AR) {
     // AR: one causal forward of [last]; commit its argmax.
-    TRY(forward(m, m->last_dev, 1, 1, true, s));
+    TRY(forward(m, m->last_dev, 1, 1, FWD_TOKENS, s));
     return launch_commit(m->pred, nullptr, 1, 1, m->last_dev, m->kv_len, s);
   }
   TRY(draft_block(m, steps, s));
   if (mode == NDIFF_MODE_DIFF) {
     // the finished block enters the cache through one bidirectional forward
-    TRY(forward(m, m->block_in, kBlock, 0, false, s));
+    TRY(forward(m, m->block_in, kBlock, 0, FWD_NONE, s));
     return launch_commit(m->draft, nullptr, kBlock, kBlock, m->last_dev, m->kv_len, s);
   }
   // SELFSPEC: causal verification of [last, d0..d30], accept the agreeing prefix
-  TRY(forward(m, m->block_in, kBlock, 1, true, s));
+  TRY(forward(m, m->block_in, kBlock, 1, FWD_TOKENS, s));
   TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->res + 33, m->res, m->res + 32, m->kv_len,
                            s));
   return launch_commit(m->res, m->res + 32, 0, 0, m->last_dev, m->kv_len, s);
@@ -433,6 +449,7 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     }
     TRY(dalloc_t(m, &m->gws, ws));
     TRY(dalloc_t(m, &m->gcnt, (size_t)tiles * 4));
+    TRY(dalloc_t(m, &m->red, (size_t)m->pl_lm.ntiles * kBlock * sizeof(float4)));
     NDIFF_CUDA_TRY(cudaMemsetAsync(m->gcnt, 0, (size_t)tiles * 4, s));
     m->attn_split = attn_bf16_auto_split(1, m->Hkv, m->Lmax);
     m->aws_bytes = attn_bf16_workspace(1, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
@@ -484,8 +501,8 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   // One forward of each block length sets every kernel attribute and device
   // lookup up front, so that later graph captures only record launches. The
   // cache rows it writes are scratch until a prefill fills them.
-  TRY(forward(m, m->ids, 1, 1, true, m->ms));
-  TRY(forward(m, m->block_in, kBlock, 0, true, m->ms));
+  TRY(forward(m, m->ids, 1, 1, FWD_LOGITS, m->ms));
+  TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, m->ms));
   TRY(finish(m->ms));
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
@@ -573,7 +590,7 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cu
   NDIFF_CUDA_TRY(cudaMemcpyAsync(m->prompt, prompt_host, (size_t)n * 4, cudaMemcpyHostToDevice, stream));
   for (int off = 0; off < n - 1; off += kBlock) {
     const int T = (n - 1 - off) < kBlock ? (n - 1 - off) : kBlock;
-    TRY(forward(m, m->prompt + off, T, 1, false, stream));
+    TRY(forward(m, m->prompt + off, T, 1, FWD_NONE, stream));
     TRY(launch_kv_add(m->kv_len, T, stream));
   }
   m->pin[0] = prompt_host[n - 1];
@@ -651,7 +668,7 @@ ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T,
       return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: token out of range");
   TRY(set_device(m));
   NDIFF_CUDA_TRY(cudaMemcpyAsync(m->ids, ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, stream));
-  TRY(forward(m, m->ids, T, mode == NDIFF_CAUSAL ? 1 : 0, true, stream));
+  TRY(forward(m, m->ids, T, mode == NDIFF_CAUSAL ? 1 : 0, FWD_LOGITS, stream));
   if (logits_host)
     NDIFF_CUDA_TRY(cudaMemcpy2DAsync(logits_host, (size_t)m->V * 4, m->logits, (size_t)m->ldl * 4,
                                      (size_t)m->V * 4, T, cudaMemcpyDeviceToHost, stream));

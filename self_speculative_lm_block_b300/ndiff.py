@@ -62,6 +62,8 @@ _SIGS = {
     "ndiff_logits_reduce": (_I, [_I, _P, _I, _I, _I64, _I, _P, _P, _P]),
     "ndiff_gemm_bf16_workspace_size": (_SZ, [_I, _I, _I]),
     "ndiff_gemm_bf16": (_I, [_P, _P, _I, _I, _I, _P, _I64, _P, _SZ, _P]),
+    "ndiff_lm_head_argmax_workspace_size": (_SZ, [_I, _I, _I]),
+    "ndiff_lm_head_argmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "ndiff_unmask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_verify_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.c_uint64, ctypes.POINTER(_P)]),
@@ -173,6 +175,15 @@ def ndiff_gemm_bf16(x, w, M, N, K, y, ldy, ws, ws_bytes, stream=None):
                  _stream(stream))
 
 
+def ndiff_lm_head_argmax_workspace_size(M, N, K) -> int:
+    return _lib.ndiff_lm_head_argmax_workspace_size(M, N, K)
+
+
+def ndiff_lm_head_argmax(x, w, M, N, K, exclude_id, argmax, conf, ws, ws_bytes, stream=None):
+    return _call("ndiff_lm_head_argmax", _ptr(x), _ptr(w), M, N, K, exclude_id, _ptr(argmax),
+                 _ptr(conf), _ptr(ws), ws_bytes, _stream(stream))
+
+
 def ndiff_unmask(conf, pred, B, T, k, mask_bits, block_in, draft, chosen, stream=None):
     return _call("ndiff_unmask", _ptr(conf), _ptr(pred), B, T, k, _ptr(mask_bits), _ptr(block_in),
                  _ptr(draft), _ptr(chosen), _stream(stream))
@@ -256,6 +267,19 @@ def gemm_bf16(x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     ndiff_gemm_bf16(x, w, M, N, K, y, N, ws, need, stream)
     return y
+
+
+def lm_head_argmax(x: torch.Tensor, w: torch.Tensor, exclude_id: int = -1, stream=None):
+    """(argmax, conf) of the rows of x @ w.T without storing the logits; bf16
+    x [M<=32][K] and w [N][K] (device tensors)."""
+    M, K = x.shape
+    N = w.shape[0]
+    ids = torch.empty(M, dtype=torch.int32, device=x.device)
+    conf = torch.empty(M, dtype=torch.float32, device=x.device)
+    need = ndiff_lm_head_argmax_workspace_size(M, N, K)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ndiff_lm_head_argmax(x, w, M, N, K, exclude_id, ids, conf, ws, need, stream)
+    return ids, conf
 
 
 class Model:

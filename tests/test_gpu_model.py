@@ -149,6 +149,95 @@ def test_gemm_rejects_bad_shapes(nd):
                      torch.zeros((8, 96), dtype=torch.bfloat16, device="cuda"))
 
 
+# ---------------------------------------------------------------- fused LM head + reduce
+def _lm_head_check(nd, M, N, K, excl, seed, sigma_w=0.05, oracle_rows=None):
+    """The fused LM head against (1) the unfused GPU path on the same fp32
+    logits: argmax identical, conf to fp32 rounding; (2) the oracle's reduction
+    of the float64 logits: an argmax may differ only where the oracle's gap
+    between its choice and the GPU's is within twice the row's gamma_K bound,
+    and conf matches the oracle's probability of the GPU's id within the
+    relative change that logit errors of that bound can cause."""
+    x = synth.normal_bf16((M, K), 1.0, seed, 1)
+    w = synth.normal_bf16((N, K), sigma_w, seed, 2)
+    xc, wc = x.cuda(), w.cuda()
+    ids, conf = nd.lm_head_argmax(xc, wc, excl)
+    nd.ndiff_check()
+    ids, conf = ids.cpu().numpy(), conf.cpu().numpy().astype(np.float64)
+    ld = (N + 3) // 4 * 4              # fp32 logits rows must start 16-byte aligned
+    y = torch.empty((M, ld), dtype=torch.float32, device="cuda")
+    need = nd.ndiff_gemm_bf16_workspace_size(M, N, K)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    nd.ndiff_gemm_bf16(xc, wc, M, N, K, y, ld, ws, need)
+    ids2, conf2 = nd.logits_reduce(y, V=N, exclude_id=excl)
+    assert np.array_equal(ids, ids2.cpu().numpy())
+    assert np.allclose(conf, conf2.cpu().numpy(), rtol=2e-5, atol=0)
+    rows = range(M) if oracle_rows is None else oracle_rows
+    xd, wd = x.double().numpy(), w.double().numpy()
+    u = 2.0 ** -24
+    gamma = K * u / (1 - K * u)
+    for m in rows:
+        ref = wd @ xd[m]
+        bound = gamma * float((np.abs(wd) @ np.abs(xd[m])).max())
+        rid, _ = OD.logits_reduce(ref[None], exclude_id=excl)
+        if ids[m] != rid[0]:
+            assert ref[rid[0]] - ref[ids[m]] <= 2 * bound, (m, ids[m], rid[0])
+        p = np.exp(ref[ids[m]] - ref.max()) / np.exp(ref - ref.max()).sum()
+        assert abs(conf[m] - p) <= (np.expm1(2 * bound) + 1e-5) * p, (m, conf[m], p)
+    return ids, conf
+
+
+@pytest.mark.parametrize("M,N,K,excl", [(1, 128, 64, -1), (5, 4173, 512, 4172), (32, 4173, 512, 0),
+                                        (32, 3000, 12288, 17), (7, 60000, 1024, 59999)])
+def test_lm_head_argmax_matches_unfused_and_oracle(nd, M, N, K, excl):
+    _lm_head_check(nd, M, N, K, excl, seed=M + N + K)
+
+
+def test_lm_head_argmax_8b_shape(nd):
+    """The 8B LM head (151936 x 4096) at a 32-token block, every row against
+    the oracle's float64 logits."""
+    _lm_head_check(nd, 32, 151936, 4096, 151935, seed=12, sigma_w=0.02)
+
+
+def test_lm_head_argmax_rows_do_not_depend_on_block(nd):
+    x = synth.normal_bf16((32, 4096), 1.0, 13, 1).cuda()
+    w = synth.normal_bf16((20000, 4096), 0.05, 13, 2).cuda()
+    ids, conf = nd.lm_head_argmax(x, w, 5)
+    for m in (0, 9, 31):
+        i1, c1 = nd.lm_head_argmax(x[m:m + 1].contiguous(), w, 5)
+        assert int(i1[0]) == int(ids[m]) and torch.equal(c1[0], conf[m]), m
+
+
+def test_lm_head_argmax_ties_go_to_the_lower_id(nd):
+    """Duplicate weight rows give exactly equal logits; the lower id wins, and
+    an excluded id never does."""
+    M, N, K = 4, 1000, 256
+    x = synth.normal_bf16((M, K), 1.0, 14, 1)
+    w = synth.normal_bf16((N, K), 0.05, 14, 2)
+    ref = x.double().numpy() @ w.double().numpy().T
+    best = ref.argmax(axis=1)
+    w2 = w.clone()
+    for m in range(M):             # copy each row's best weight row to a lower and a higher id
+        w2[(best[m] + 331 * (m + 1)) % N] = w[best[m]]
+        w2[(best[m] + 997) % N] = w[best[m]]
+    ids, _ = nd.lm_head_argmax(x.cuda(), w2.cuda(), -1)
+    y = nd.gemm_bf16(x.cuda(), w2.cuda()).cpu().numpy()
+    for m in range(M):
+        top = np.flatnonzero(y[m] == y[m].max())
+        assert int(ids[m]) == int(top.min()), (m, top)
+    ex = int(ids[0])
+    ids_ex, _ = nd.lm_head_argmax(x.cuda(), w2.cuda(), ex)
+    assert int(ids_ex[0]) != ex
+
+
+def test_lm_head_argmax_rejects_bad_arguments(nd):
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(nd.NdiffError):
+        nd.lm_head_argmax(x, w, 128)          # exclude_id >= N
+    with pytest.raises(nd.NdiffError):
+        nd.lm_head_argmax(torch.zeros((33, 64), dtype=torch.bfloat16, device="cuda"), w, -1)
+
+
 # ---------------------------------------------------------------- weights
 @pytest.mark.parametrize("which", ["tiny", "mid"])
 def test_weights_follow_the_philox_stream(nd, which):
