@@ -341,6 +341,21 @@ def run_model(rank, n_tokens, steps=1):
             hist = [int(x) for x in st.accept_hist]
             out[name]["accept_len_hist"] = {str(i): v for i, v in enumerate(hist) if v}
             out[name]["draft_forwards_per_block"] = steps
+    # the threshold sampler's host-driven round loop (a 4-byte read between
+    # rounds), at tau = 0: one drafting round per block, the same forwards as
+    # the one-round top-k draft above, so the difference is the loop's cost
+    m.prefill(prompt)
+    m.step(nd.NDIFF_MODE_SELFSPEC, 1, tau=0.0)
+    m.prefill(prompt)
+    m.stats = nd.Stats()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    toks = m.generate(nd.NDIFF_MODE_SELFSPEC, min(n_tokens, 64), 1, tau=0.0)
+    dt = time.perf_counter() - t0
+    st = m.stats
+    out["selfspec_threshold_tau0"] = {"tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+                                      "ms_per_forward": dt * 1e3 / st.forwards,
+                                      "equals_ar": toks == res["ar"][:len(toks)]}
     wb = weight_bytes_8b(c)
     out["weight_bytes_per_forward"] = wb
     out["ar"]["weight_stream_gbs"] = wb / (out["ar"]["ms_per_forward"] * 1e-3) / 1e9

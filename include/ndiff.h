@@ -206,6 +206,28 @@ NDIFF_API ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int 
  * Shapes: draft, target, commit int32 [B][T]; accept_len, n_commit, kv_len
  * int32 [B]. 1 <= T <= 32. B == 0 is a no-op.
  * ------------------------------------------------------------------------ */
+/* ------------------------------------------------------------------------ *
+ * Threshold unmask round with revision (the sampler variant of
+ * NDIFF_SAMPLER_THRESHOLD; [HFB]: refinement rounds are a budget and earlier
+ * tokens can be revised). For each sequence b, with M the masked slots (bits
+ * of mask_bits[b]) and E the slots i < T fixed in earlier rounds:
+ *   revise: every i in E with pred[b][i] != draft[b][i] and
+ *           conf[b][i] >= tau_revise:  draft[b][i] = pred[b][i] and, if
+ *           i <= T-2, block_in[b][i+1] = pred[b][i];
+ *   fix:    F = { i in M : conf[b][i] >= tau }, or, if F is empty and M is
+ *           not, the slot of M with the largest conf (lowest slot on ties);
+ *           for i in F: draft[b][i] = pred[b][i], clear bit i, and
+ *           block_in[b][i+1] = pred[b][i] if i <= T-2;
+ *   n_fixed[b] = |F|, n_revised[b] = revised count (either may be NULL).
+ * Comparisons are made on the fp32 values as given. Shapes as in
+ * ndiff_unmask; 1 <= T <= 32; tau, tau_revise >= 0 (tau_revise > 1 never
+ * revises). B == 0 is a no-op. conf must not be NaN.
+ * ------------------------------------------------------------------------ */
+NDIFF_API ndiff_status ndiff_unmask_threshold(const float* conf, const int32_t* pred, int B, int T,
+                                              float tau, float tau_revise, uint32_t* mask_bits,
+                                              int32_t* block_in, int32_t* draft, int32_t* n_fixed,
+                                              int32_t* n_revised, cudaStream_t stream);
+
 NDIFF_API ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                  int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                  int32_t* kv_len, cudaStream_t stream);
@@ -296,7 +318,32 @@ typedef struct {
     int32_t last_accept_len; /* L of the last SELFSPEC verification (-1 otherwise) */
     int32_t last_n_commit;   /* tokens committed by the last decode step */
     int64_t accept_hist[33]; /* histogram of L over SELFSPEC verifications */
+    int64_t revisions;       /* earlier draft tokens replaced (threshold sampler) */
+    int32_t last_rounds;     /* drafting forwards of the last decode step */
+    int32_t reserved;
 } ndiff_stats;
+
+/* How a DIFF or SELFSPEC block is drafted ([FFI] "三种生成模式": a block is
+ * denoised over several rounds; [HFB]: the number of rounds is a budget the
+ * user sets, and the model can revise tokens it already produced; [AIF]
+ * 核心洞察: the sampler decides how many tokens a forward yields).
+ *   NDIFF_SAMPLER_TOPK:      `steps` rounds, each fixing the k = 32/steps most
+ *                            confident masked slots (ndiff_unmask).
+ *   NDIFF_SAMPLER_THRESHOLD: rounds until no slot is masked (at most 32), each
+ *                            fixing every masked slot with confidence >= tau
+ *                            or else the most confident one, after replacing
+ *                            earlier slots' tokens whose new prediction differs
+ *                            with confidence >= tau_revise (> 1: no revision)
+ *                            (ndiff_unmask_threshold). */
+typedef enum { NDIFF_SAMPLER_TOPK = 0, NDIFF_SAMPLER_THRESHOLD = 1 } ndiff_sampler;
+
+typedef struct {
+    ndiff_mode mode;
+    ndiff_sampler sampler;
+    int steps;          /* TOPK: 1 <= steps <= 32, 32 % steps == 0 */
+    float tau;          /* THRESHOLD: fix threshold, 0 <= tau */
+    float tau_revise;   /* THRESHOLD: revision threshold, 0 <= tau_revise (> 1: off) */
+} ndiff_decode_opts;
 
 NDIFF_API ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out);
 NDIFF_API ndiff_status ndiff_model_destroy(ndiff_model* m);
@@ -323,6 +370,15 @@ NDIFF_API ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host,
 NDIFF_API ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,
                                int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
                                cudaStream_t stream);
+
+/* ndiff_decode_step with a choice of draft sampler (see ndiff_decode_opts).
+ * With NDIFF_SAMPLER_THRESHOLD the rounds run one after another with a 4-byte
+ * read of the block's mask word between them (the round count depends on the
+ * model's confidence); every round and the final forward are CUDA graphs.
+ * AR ignores the sampler. Synchronous on return. */
+NDIFF_API ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
+                                            int32_t* out_tokens_host, int* n_out,
+                                            ndiff_stats* stats, cudaStream_t stream);
 
 /* Runs one forward of `T` block tokens (host ids) at the model's current
  * position with the given mask, writes fp32 logits [T][vocab] to the host

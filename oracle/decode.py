@@ -12,6 +12,17 @@ Plain definitions in Python/NumPy, float64 where floating point is involved.
   rounds of iterative denoising per block). Reading: among still-masked slots,
   the k highest-confidence ones are fixed (ties to the lower slot), without
   remasking.
+- Threshold unmask with revision (sampler variants): "NVIDIA 发布
+  Nemotron-Labs Diffusion：三模态语言模型统一 AR 与扩散解码" (aimodeling.com
+  digest of the Hugging Face blog): the refinement steps are a budget the user
+  can lower, and the diffusion model can revise tokens it already produced;
+  "Nemotron-Labs-Diffusion: 一种统一自回归、扩散和自推测解码的三模式语言模型"
+  (ai-feeds.com), 核心洞察: the sampler decides the tokens per forward.
+  Reading: a round fixes every masked slot whose confidence reaches tau (at
+  least the single most confident one, ties to the lower slot, so each round
+  makes progress), and, before that, replaces the token of every slot fixed in
+  an earlier round whose current prediction differs with confidence at least
+  tau_revise (tau_revise > 1 turns revision off).
 - Verify/accept: gsyq.cn explainer, §2.3 "自推测解码": the verifier accepts the
   agreeing prefix, rejects the first mismatching draft and everything after it,
   and supplies its own token at that position.
@@ -64,6 +75,47 @@ def unmask(conf, pred, mask_bits, block_in, draft, k: int):
             if i <= T - 2:
                 block_in[b, i + 1] = pred[b, i]
     return mask_bits.astype(np.uint32), block_in, draft, chosen
+
+
+def unmask_threshold(conf, pred, mask_bits, block_in, draft, tau: float, tau_revise: float = 2.0):
+    """One threshold round over [B][T] slots. Returns updated copies
+    (mask_bits, block_in, draft) and per sequence the number of slots fixed
+    and the number of earlier slots revised."""
+    conf = np.asarray(conf, dtype=np.float64)
+    pred = np.asarray(pred)
+    B, T = conf.shape
+    mask_bits = np.array(mask_bits, dtype=np.int64) & ((1 << T) - 1)
+    block_in = np.array(block_in, dtype=np.int32)
+    draft = np.array(draft, dtype=np.int32)
+    n_fixed = np.zeros(B, dtype=np.int32)
+    n_revised = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        mask = int(mask_bits[b])
+        masked = [i for i in range(T) if (mask >> i) & 1]
+        earlier = [i for i in range(T) if not (mask >> i) & 1]
+        # revision of slots fixed in earlier rounds
+        for i in earlier:
+            if pred[b, i] != draft[b, i] and conf[b, i] >= tau_revise:
+                draft[b, i] = pred[b, i]
+                if i <= T - 2:
+                    block_in[b, i + 1] = pred[b, i]
+                n_revised[b] += 1
+        # every masked slot at or above tau; else the most confident one
+        chosen = [i for i in masked if conf[b, i] >= tau]
+        if not chosen and masked:
+            best = masked[0]
+            for i in masked[1:]:
+                if conf[b, i] > conf[b, best]:
+                    best = i
+            chosen = [best]
+        for i in chosen:
+            draft[b, i] = pred[b, i]
+            mask &= ~(1 << i)
+            if i <= T - 2:
+                block_in[b, i + 1] = pred[b, i]
+        mask_bits[b] = mask
+        n_fixed[b] = len(chosen)
+    return mask_bits.astype(np.uint32), block_in, draft, n_fixed, n_revised
 
 
 def verify_accept(draft, target, kv_len=None):

@@ -24,6 +24,11 @@ Readings where the pages are silent (each is listed in the design notes):
   BIDIR forward of [last, d0..d30] that writes the block's KV (counted).
 - SELFSPEC: the same drafting forwards, then one CAUSAL forward of
   [last, d0..d30]; accept the longest agreeing prefix plus the correction.
+- Threshold sampler (either mode): BIDIR drafting rounds until no slot is
+  masked, each fixing the masked slots whose confidence reaches tau (else the
+  most confident one) after revising earlier slots (oracle.decode.
+  unmask_threshold); tau and tau_revise are compared in float32, the
+  precision the confidences come in.
 - Architecture: pre-norm, RMSNorm with unit gain and eps, rotate-half RoPE
   (pairs (i, i+D/2), base 10000, absolute positions), SwiGLU FFN, untied LM
   head, all weights N(0, 0.02^2) from the Philox stream of oracle.philox.
@@ -159,6 +164,8 @@ class Session:
         self.tokens: list[int] = []
         self.forwards = 0
         self.accept_lens: list[int] = []
+        self.revisions = 0
+        self.rounds = 0
 
     def _rb(self, x: np.ndarray) -> np.ndarray:
         return round_to_bf16(x) if self.cfg.dtype == "bf16" else x
@@ -234,16 +241,36 @@ class Session:
         assert int(mask[0]) == 0
         return draft[0]
 
-    def step_diff(self, steps: int) -> list[int]:
-        d = self.draft(steps)
+    def draft_threshold(self, tau: float, tau_revise: float = 2.0) -> np.ndarray:
+        block_in = np.full((1, BLOCK), self.cfg.mask_id, dtype=np.int32)
+        block_in[0, 0] = self.last
+        mask = np.array([(1 << BLOCK) - 1], dtype=np.int64)
+        draft = np.full((1, BLOCK), -1, dtype=np.int32)
+        tau32, taur32 = float(np.float32(tau)), float(np.float32(tau_revise))
+        self.rounds = 0
+        while int(mask[0]) != 0:
+            logits = self.forward(block_in[0], attention.BIDIR)
+            ids, conf = self._argmax(logits)
+            conf32 = conf.astype(np.float32).astype(np.float64)
+            mask, block_in, draft, _, nr = decode.unmask_threshold(conf32[None], ids[None], mask,
+                                                                   block_in, draft, tau32, taur32)
+            self.revisions += int(nr[0])
+            self.rounds += 1
+        return draft[0]
+
+    def _draft_any(self, steps: int, tau):
+        return self.draft(steps) if tau is None else self.draft_threshold(*tau)
+
+    def step_diff(self, steps: int, tau=None) -> list[int]:
+        d = self._draft_any(steps, tau)
         self.forward([self.last] + [int(t) for t in d[:BLOCK - 1]], attention.BIDIR)
         self.kv_len += BLOCK
         self.last = int(d[BLOCK - 1])
         self.tokens.extend(int(t) for t in d)
         return [int(t) for t in d]
 
-    def step_selfspec(self, steps: int) -> list[int]:
-        d = self.draft(steps)
+    def step_selfspec(self, steps: int, tau=None) -> list[int]:
+        d = self._draft_any(steps, tau)
         logits = self.forward([self.last] + [int(t) for t in d[:BLOCK - 1]], attention.CAUSAL)
         a = self._argmax(logits)[0]
         L, commit, n, _ = decode.verify_accept(d[None], a[None])
@@ -255,15 +282,17 @@ class Session:
         self.tokens.extend(out)
         return out
 
-    def generate(self, mode: str, n_new: int, steps: int = 1) -> list[int]:
-        """Decode until n_new tokens (extra committed tokens are cut)."""
+    def generate(self, mode: str, n_new: int, steps: int = 1, tau=None) -> list[int]:
+        """Decode until n_new tokens (extra committed tokens are cut). `tau`:
+        None for the top-k draft of `steps` rounds, or (tau, tau_revise) for
+        the threshold sampler."""
         while len(self.tokens) < n_new:
             if mode == "ar":
                 self.step_ar()
             elif mode == "diff":
-                self.step_diff(steps)
+                self.step_diff(steps, tau)
             elif mode == "selfspec":
-                self.step_selfspec(steps)
+                self.step_selfspec(steps, tau)
             else:
                 raise ValueError(mode)
         return self.tokens[:n_new]

@@ -267,6 +267,22 @@ ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int B, int T, 
   return launch_unmask(conf, pred, B, T, k, mask_bits, block_in, draft, chosen, stream);
 }
 
+ndiff_status ndiff_unmask_threshold(const float* conf, const int32_t* pred, int B, int T, float tau,
+                                    float tau_revise, uint32_t* mask_bits, int32_t* block_in,
+                                    int32_t* draft, int32_t* n_fixed, int32_t* n_revised,
+                                    cudaStream_t stream) {
+  if (B < 0 || T < 1 || T > 32 || !(tau >= 0.f) || !(tau_revise >= 0.f))
+    return set_error(NDIFF_ERR_INVALID_ARG,
+                     "ndiff_unmask_threshold: need B>=0, 1<=T<=32, tau>=0, tau_revise>=0 "
+                     "(B=%d T=%d tau=%g tau_revise=%g)",
+                     B, T, (double)tau, (double)tau_revise);
+  if (B == 0) return NDIFF_OK;
+  if (!conf || !pred || !mask_bits || !block_in || !draft)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_unmask_threshold: null pointer");
+  return launch_unmask_threshold(conf, pred, B, T, tau, tau_revise, mask_bits, block_in, draft,
+                                 n_fixed, n_revised, stream);
+}
+
 ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                  int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                  int32_t* kv_len, cudaStream_t stream) {

@@ -34,6 +34,10 @@ ndiff_status launch_logits_reduce(ndiff_dtype dt, const void* logits, int R, int
 ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T, int k,
                            uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                            int32_t* chosen, cudaStream_t stream);
+ndiff_status launch_unmask_threshold(const float* conf, const int32_t* pred, int B, int T, float tau,
+                                     float tau_revise, uint32_t* mask_bits, int32_t* block_in,
+                                     int32_t* draft, int32_t* n_fixed, int32_t* n_revised,
+                                     cudaStream_t stream);
 ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                   int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                   int32_t* kv_len, cudaStream_t stream);

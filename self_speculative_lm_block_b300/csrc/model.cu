@@ -29,7 +29,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <functional>
 #include <map>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -88,7 +90,8 @@ struct ndiff_model {
   float* conf = nullptr;        // [32]
   int32_t* draft = nullptr;     // [32]
   int32_t* block_in = nullptr;  // [32]
-  int32_t* res = nullptr;       // [34]: commit[32], n_commit, accept_len
+  int32_t* res = nullptr;       // [64]: commit[32], n_commit, accept_len; [40..41] the threshold
+                                //   round's fixed and revised counts
   int32_t* kv_len = nullptr;    // [1]
   uint32_t* mask = nullptr;     // [1]
   int32_t* chosen = nullptr;    // [32]
@@ -105,7 +108,8 @@ struct ndiff_model {
   int32_t* pin = nullptr;       // pinned host staging [64]
   int32_t* last_dev = nullptr;  // [1] pending last token (device copy of `last`)
   cudaStream_t ms = nullptr;    // the model's own stream (decode graphs run here)
-  std::map<int, cudaGraphExec_t> graphs;  // decode cycles by (mode, steps)
+  // decode graphs by (part, mode, steps, tau bits, tau_revise bits)
+  std::map<std::tuple<int, int, int, uint32_t, uint32_t>, cudaGraphExec_t> graphs;
   std::vector<void*> allocs;
   int P = 0;
   int32_t last = -1;
@@ -293,15 +297,8 @@ ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
   return NDIFF_OK;
 }
 
-// Enqueues one decode cycle; every input it reads (pending token, committed
-// prefix) lives on the device, so the same launches can be replayed.
-ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStream_t s) {
-  if (mode == NDIFF_MODE_AR) {
-    // AR: one causal forward of [last]; commit its argmax.
-    TRY(forward(m, m->last_dev, 1, 1, FWD_TOKENS, s));
-    return launch_commit(m->pred, nullptr, 1, 1, m->last_dev, m->kv_len, s);
-  }
-  TRY(draft_block(m, steps, s));
+// The end of a DIFF or SELFSPEC cycle, once the draft is complete.
+ndiff_status enqueue_tail(ndiff_model* m, ndiff_mode mode, cudaStream_t s) {
   if (mode == NDIFF_MODE_DIFF) {
     // the finished block enters the cache through one bidirectional forward
     TRY(forward(m, m->block_in, kBlock, 0, FWD_NONE, s));
@@ -314,16 +311,32 @@ ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStrea
   return launch_commit(m->res, m->res + 32, 0, 0, m->last_dev, m->kv_len, s);
 }
 
-// The decode cycle as an instantiated CUDA graph (captured on first use).
-ndiff_status cycle_graph(ndiff_model* m, ndiff_mode mode, int steps, cudaGraphExec_t* out) {
-  const int key = (int)mode * 64 + (mode == NDIFF_MODE_AR ? 0 : steps);
+// Enqueues one decode cycle; every input it reads (pending token, committed
+// prefix) lives on the device, so the same launches can be replayed.
+ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStream_t s) {
+  if (mode == NDIFF_MODE_AR) {
+    // AR: one causal forward of [last]; commit its argmax.
+    TRY(forward(m, m->last_dev, 1, 1, FWD_TOKENS, s));
+    return launch_commit(m->pred, nullptr, 1, 1, m->last_dev, m->kv_len, s);
+  }
+  TRY(draft_block(m, steps, s));
+  return enqueue_tail(m, mode, s);
+}
+
+enum { PART_CYCLE = 0, PART_INIT = 1, PART_ROUND = 2, PART_TAIL = 3 };
+
+// The launches `fn` enqueues, as an instantiated CUDA graph captured on the
+// model's stream on first use and kept under `key`.
+ndiff_status cached_graph(ndiff_model* m, const std::tuple<int, int, int, uint32_t, uint32_t>& key,
+                          const std::function<ndiff_status(cudaStream_t)>& fn,
+                          cudaGraphExec_t* out) {
   auto it = m->graphs.find(key);
   if (it != m->graphs.end()) {
     *out = it->second;
     return NDIFF_OK;
   }
   NDIFF_CUDA_TRY(cudaStreamBeginCapture(m->ms, cudaStreamCaptureModeThreadLocal));
-  ndiff_status st = enqueue_cycle(m, mode, steps, m->ms);
+  ndiff_status st = fn(m->ms);
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaStreamEndCapture(m->ms, &g);
   if (st != NDIFF_OK) {
@@ -338,6 +351,13 @@ ndiff_status cycle_graph(ndiff_model* m, ndiff_mode mode, int steps, cudaGraphEx
   m->graphs[key] = ge;
   *out = ge;
   return NDIFF_OK;
+}
+
+// The decode cycle of a fixed schedule (AR, or a top-k draft of `steps` rounds).
+ndiff_status cycle_graph(ndiff_model* m, ndiff_mode mode, int steps, cudaGraphExec_t* out) {
+  const int st = mode == NDIFF_MODE_AR ? 0 : steps;
+  return cached_graph(m, std::make_tuple((int)PART_CYCLE, (int)mode, st, 0u, 0u),
+                      [&](cudaStream_t s) { return enqueue_cycle(m, mode, steps, s); }, out);
 }
 
 // Waits for the stream and reports device-side timeouts recorded meanwhile.
@@ -602,43 +622,25 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cu
   return NDIFF_OK;
 }
 
-ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32_t* out_tokens_host,
-                               int* n_out, ndiff_stats* stats, cudaStream_t stream) {
-  if (!m || !out_tokens_host || !n_out)
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: null pointer");
-  *n_out = 0;
-  if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
-  if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC)
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad mode %d", (int)mode);
-  if (mode != NDIFF_MODE_AR && (steps < 1 || steps > kBlock || kBlock % steps != 0))
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: steps must divide 32 (got %d)", steps);
-  const int need = mode == NDIFF_MODE_AR ? 1 : kBlock;
-  if (m->P + need > m->Lmax)
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)", m->P, m->Lmax);
-  TRY(set_device(m));
-  // the cycle runs on the model's stream, after the caller's earlier work
-  NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
-  cudaGraphExec_t ge = nullptr;
-  TRY(cycle_graph(m, mode, steps, &ge));
-  NDIFF_CUDA_TRY(cudaGraphLaunch(ge, m->ms));
+// Reads the committed tokens of the cycle just enqueued on the model's stream
+// and advances the host view of the session.
+static ndiff_status collect(ndiff_model* m, ndiff_mode mode, int64_t forwards, int rounds,
+                            int64_t revisions, int32_t* out_tokens_host, int* n_out,
+                            ndiff_stats* stats) {
   int n = 0, L = -1;
-  int64_t forwards = 0;
   if (mode == NDIFF_MODE_AR) {
     NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, 4, cudaMemcpyDeviceToHost, m->ms));
     TRY(finish(m->ms));
     n = 1;
-    forwards = 1;
   } else if (mode == NDIFF_MODE_DIFF) {
     NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, kBlock * 4, cudaMemcpyDeviceToHost, m->ms));
     TRY(finish(m->ms));
     n = kBlock;
-    forwards = steps + 1;
   } else {
     NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, 34 * 4, cudaMemcpyDeviceToHost, m->ms));
     TRY(finish(m->ms));
     n = m->pin[32];
     L = m->pin[33];
-    forwards = steps + 1;
   }
   for (int i = 0; i < n; ++i) out_tokens_host[i] = m->pin[i];
   *n_out = n;
@@ -649,9 +651,98 @@ ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32
     stats->tokens += n;
     stats->last_accept_len = L;
     stats->last_n_commit = n;
+    stats->revisions += revisions;
+    stats->last_rounds = rounds;
     if (L >= 0 && L <= kBlock) stats->accept_hist[L] += 1;
   }
   return NDIFF_OK;
+}
+
+ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
+                                  int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
+                                  cudaStream_t stream) {
+  if (!m || !opts || !out_tokens_host || !n_out)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: null pointer");
+  *n_out = 0;
+  const ndiff_mode mode = opts->mode;
+  if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
+  if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad mode %d", (int)mode);
+  const bool thr = mode != NDIFF_MODE_AR && opts->sampler == NDIFF_SAMPLER_THRESHOLD;
+  if (mode != NDIFF_MODE_AR) {
+    if (opts->sampler != NDIFF_SAMPLER_TOPK && opts->sampler != NDIFF_SAMPLER_THRESHOLD)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad sampler %d", (int)opts->sampler);
+    if (!thr && (opts->steps < 1 || opts->steps > kBlock || kBlock % opts->steps != 0))
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: steps must divide 32 (got %d)",
+                       opts->steps);
+    if (thr && !(opts->tau >= 0.f && opts->tau_revise >= 0.f))
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "ndiff_decode_step: tau and tau_revise must be >= 0 (got %g, %g)",
+                       (double)opts->tau, (double)opts->tau_revise);
+  }
+  const int need = mode == NDIFF_MODE_AR ? 1 : kBlock;
+  if (m->P + need > m->Lmax)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)", m->P, m->Lmax);
+  TRY(set_device(m));
+  // the cycle runs on the model's stream, after the caller's earlier work
+  NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
+  if (!thr) {
+    cudaGraphExec_t ge = nullptr;
+    TRY(cycle_graph(m, mode, opts->steps, &ge));
+    NDIFF_CUDA_TRY(cudaGraphLaunch(ge, m->ms));
+    const int rounds = mode == NDIFF_MODE_AR ? 0 : opts->steps;
+    return collect(m, mode, rounds + 1, rounds, 0, out_tokens_host, n_out, stats);
+  }
+  // Threshold sampler: rounds until the block's mask word is empty.
+  uint32_t tb, rb;
+  memcpy(&tb, &opts->tau, 4);
+  memcpy(&rb, &opts->tau_revise, 4);
+  const float tau = opts->tau, taur = opts->tau_revise;
+  cudaGraphExec_t g_init = nullptr, g_round = nullptr, g_tail = nullptr;
+  TRY(cached_graph(m, std::make_tuple((int)PART_INIT, 0, 0, 0u, 0u),
+                   [&](cudaStream_t s) {
+                     return launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev,
+                                              m->mask_id, s);
+                   },
+                   &g_init));
+  TRY(cached_graph(m, std::make_tuple((int)PART_ROUND, 0, 0, tb, rb),
+                   [&](cudaStream_t s) {
+                     TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, s));
+                     return launch_unmask_threshold(m->conf, m->pred, 1, kBlock, tau, taur, m->mask,
+                                                    m->block_in, m->draft, m->res + 40,
+                                                    m->res + 41, s);
+                   },
+                   &g_round));
+  TRY(cached_graph(m, std::make_tuple((int)PART_TAIL, (int)mode, 0, 0u, 0u),
+                   [&](cudaStream_t s) { return enqueue_tail(m, mode, s); }, &g_tail));
+  NDIFF_CUDA_TRY(cudaGraphLaunch(g_init, m->ms));
+  int rounds = 0;
+  int64_t revisions = 0;
+  for (;;) {
+    NDIFF_CUDA_TRY(cudaGraphLaunch(g_round, m->ms));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin + 40, m->mask, 4, cudaMemcpyDeviceToHost, m->ms));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin + 41, m->res + 40, 8, cudaMemcpyDeviceToHost, m->ms));
+    TRY(finish(m->ms));
+    ++rounds;
+    revisions += m->pin[42];
+    if (m->pin[40] == 0) break;
+    // every round fixes at least one of the 32 slots
+    if (rounds >= kBlock || m->pin[41] < 1)
+      return set_error(NDIFF_ERR_CUDA, "ndiff_decode_step: threshold round fixed no slot");
+  }
+  NDIFF_CUDA_TRY(cudaGraphLaunch(g_tail, m->ms));
+  return collect(m, mode, rounds + 1, rounds, revisions, out_tokens_host, n_out, stats);
+}
+
+ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32_t* out_tokens_host,
+                               int* n_out, ndiff_stats* stats, cudaStream_t stream) {
+  ndiff_decode_opts o;
+  o.mode = mode;
+  o.sampler = NDIFF_SAMPLER_TOPK;
+  o.steps = steps;
+  o.tau = 0.f;
+  o.tau_revise = 2.f;
+  return ndiff_decode_step_ex(m, &o, out_tokens_host, n_out, stats, stream);
 }
 
 ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T, ndiff_mask mode,

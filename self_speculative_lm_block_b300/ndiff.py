@@ -39,7 +39,17 @@ class ModelConfig(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [("forwards", ctypes.c_int64), ("tokens", ctypes.c_int64),
                 ("last_accept_len", ctypes.c_int32), ("last_n_commit", ctypes.c_int32),
-                ("accept_hist", ctypes.c_int64 * 33)]
+                ("accept_hist", ctypes.c_int64 * 33), ("revisions", ctypes.c_int64),
+                ("last_rounds", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+NDIFF_SAMPLER_TOPK = 0
+NDIFF_SAMPLER_THRESHOLD = 1
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("sampler", ctypes.c_int), ("steps", ctypes.c_int),
+                ("tau", ctypes.c_float), ("tau_revise", ctypes.c_float)]
 
 
 _P = ctypes.c_void_p
@@ -65,6 +75,8 @@ _SIGS = {
     "ndiff_lm_head_argmax_workspace_size": (_SZ, [_I, _I, _I]),
     "ndiff_lm_head_argmax": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "ndiff_unmask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "ndiff_unmask_threshold": (_I, [_P, _P, _I, _I, _F, _F, _P, _P, _P, _P, _P, _P]),
+    "ndiff_decode_step_ex": (_I, [_P, _P, _P, _P, _P, _P]),
     "ndiff_verify_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.c_uint64, ctypes.POINTER(_P)]),
     "ndiff_model_destroy": (_I, [_P]),
@@ -184,6 +196,13 @@ def ndiff_lm_head_argmax(x, w, M, N, K, exclude_id, argmax, conf, ws, ws_bytes, 
                  _ptr(conf), _ptr(ws), ws_bytes, _stream(stream))
 
 
+def ndiff_unmask_threshold(conf, pred, B, T, tau, tau_revise, mask_bits, block_in, draft,
+                           n_fixed=None, n_revised=None, stream=None):
+    return _call("ndiff_unmask_threshold", _ptr(conf), _ptr(pred), B, T, tau, tau_revise,
+                 _ptr(mask_bits), _ptr(block_in), _ptr(draft), _ptr(n_fixed), _ptr(n_revised),
+                 _stream(stream))
+
+
 def ndiff_unmask(conf, pred, B, T, k, mask_bits, block_in, draft, chosen, stream=None):
     return _call("ndiff_unmask", _ptr(conf), _ptr(pred), B, T, k, _ptr(mask_bits), _ptr(block_in),
                  _ptr(draft), _ptr(chosen), _stream(stream))
@@ -212,6 +231,14 @@ def ndiff_decode_step(m: int, mode: int, steps: int, out_tokens_host, stats: Sta
                       stream=None) -> int:
     n = _I(0)
     _call("ndiff_decode_step", m, mode, steps, _ptr(out_tokens_host), ctypes.byref(n),
+          ctypes.byref(stats) if stats is not None else None, _stream(stream))
+    return n.value
+
+
+def ndiff_decode_step_ex(m: int, opts: DecodeOpts, out_tokens_host, stats: Stats | None = None,
+                         stream=None) -> int:
+    n = _I(0)
+    _call("ndiff_decode_step_ex", m, ctypes.byref(opts), _ptr(out_tokens_host), ctypes.byref(n),
           ctypes.byref(stats) if stats is not None else None, _stream(stream))
     return n.value
 
@@ -310,15 +337,21 @@ class Model:
         arr = np.ascontiguousarray(np.asarray(prompt, dtype=np.int32))
         ndiff_prefill(self.handle, arr.ctypes.data, int(arr.shape[0]))
 
-    def step(self, mode: int, steps: int = 1):
+    def step(self, mode: int, steps: int = 1, tau: float | None = None, tau_revise: float = 2.0):
+        """One decode cycle; with `tau` the draft uses the threshold sampler."""
         buf = (ctypes.c_int32 * 32)()
-        n = ndiff_decode_step(self.handle, mode, steps, ctypes.addressof(buf), self.stats)
+        if tau is None:
+            n = ndiff_decode_step(self.handle, mode, steps, ctypes.addressof(buf), self.stats)
+        else:
+            o = DecodeOpts(mode, NDIFF_SAMPLER_THRESHOLD, steps, tau, tau_revise)
+            n = ndiff_decode_step_ex(self.handle, o, ctypes.addressof(buf), self.stats)
         return list(buf[:n])
 
-    def generate(self, mode: int, n_new: int, steps: int = 1):
+    def generate(self, mode: int, n_new: int, steps: int = 1, tau: float | None = None,
+                 tau_revise: float = 2.0):
         out = []
         while len(out) < n_new:
-            out.extend(self.step(mode, steps))
+            out.extend(self.step(mode, steps, tau, tau_revise))
         return out[:n_new]
 
     def forward(self, ids, mode: int):

@@ -322,6 +322,40 @@ def test_tiny_selfspec_equals_ar_on_gpu(nd, steps):
     m.close()
 
 
+def test_tiny_threshold_sampler_on_gpu(nd):
+    """Threshold sampler through the decode loop: tau above 1 gives the
+    top-k draft with 32 rounds and tau 0 the one-round draft, token for token
+    and forward for forward; self-speculation with any threshold emits the AR
+    tokens; revision rounds run and are counted."""
+    c = synth.TINY
+    pr = synth.prompt(c["prompt"], c["vocab"], c["seed"])
+    m = _gpu_model(nd, c, "f32", max_seq=260)
+    m.prefill(pr)
+    ar = m.generate(0, 64)
+    for steps, tau in ((32, 1.5), (1, 0.0)):
+        m.prefill(pr)
+        m.stats = type(m.stats)()
+        a = m.generate(1, 64, steps)
+        fa = m.stats.forwards
+        m.prefill(pr)
+        m.stats = type(m.stats)()
+        b = m.generate(1, 64, tau=tau)
+        assert a == b and fa == m.stats.forwards == 2 * (steps + 1), (steps, tau)
+        assert m.stats.last_rounds == steps
+    for tau, taur in ((0.00345, 2.0), (1.5, 0.0), (0.0, 0.0)):
+        m.prefill(pr)
+        m.stats = type(m.stats)()
+        assert m.generate(2, 64, tau=tau, tau_revise=taur) == ar, (tau, taur)
+        assert 1 <= m.stats.last_rounds <= 32
+    # revision on: the oracle's and the GPU's diffusion drafts agree wherever
+    # they have been compared so far; here only that revisions are counted
+    m.prefill(pr)
+    m.stats = type(m.stats)()
+    m.generate(1, 64, tau=1.5, tau_revise=0.0)
+    assert m.stats.revisions > 0
+    m.close()
+
+
 # ---------------------------------------------------------------- bf16 model
 def test_bf16_forward_logits_match_oracle(nd):
     c = MID_BF16
@@ -378,6 +412,20 @@ def test_bf16_selfspec_equals_ar_and_tracks_oracle(nd):
     ref, gaps = _oracle_ar(cfg, OM.Weights(cfg), pr, 24)
     n = _compare_tokens(ar[:24], ref, gaps)
     print(f"GPU AR tokens compared with the oracle: {n} of 24")
+    m.close()
+
+
+def test_bf16_threshold_selfspec_equals_ar(nd):
+    """bf16 model: self-speculation with the threshold sampler (with and
+    without revision) emits the AR tokens."""
+    c = MID_BF16
+    pr = synth.prompt(48, c["vocab"], c["seed"])
+    m = _gpu_model(nd, c, "bf16", max_seq=256)
+    m.prefill(pr)
+    ar = m.generate(0, 40)
+    for tau, taur in ((0.002, 2.0), (0.002, 0.0)):
+        m.prefill(pr)
+        assert m.generate(2, 40, tau=tau, tau_revise=taur) == ar, (tau, taur)
     m.close()
 
 

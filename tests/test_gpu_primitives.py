@@ -206,6 +206,42 @@ def test_unmask(nd, T, ties, allm):
         assert np.array_equal(ch.cpu().numpy(), rch)
 
 
+@pytest.mark.parametrize("T,ties,allm", [(32, False, False), (32, True, False), (32, True, True),
+                                         (7, True, False), (1, False, True)])
+def test_unmask_threshold(nd, T, ties, allm):
+    """Threshold rounds with revision against the oracle, bit for bit, with
+    drafts that partly disagree with the predictions (so revision has work)
+    and thresholds at and between the tie-heavy confidence values."""
+    B = 257
+    conf, pred, mask = synth.unmask_inputs(B, T, 151936, 91 + T, ties=ties, all_masked=allm)
+    rng = np.random.default_rng(T)
+    dr0 = np.where(rng.random((B, T)) < 0.5, pred.numpy(), rng.integers(0, 151936, size=(B, T)))
+    dr0 = np.where((mask.numpy().view(np.uint32)[:, None] >> np.arange(T)) & 1, -1, dr0).astype(np.int32)
+    for tau, taur in ((0.5, 2.0), (0.8125, 0.5), (0.0, 0.0), (1.0, 1.0), (1.5, 0.9375)):
+        blk = torch.full((B, T), 7, dtype=torch.int32)
+        dr = torch.from_numpy(dr0.copy())
+        m_d, b_d, d_d = mask.cuda(), blk.cuda(), dr.cuda()
+        nf = torch.empty(B, dtype=torch.int32, device="cuda")
+        nr = torch.empty(B, dtype=torch.int32, device="cuda")
+        nd.ndiff_unmask_threshold(conf.cuda(), pred.cuda(), B, T, tau, taur, m_d, b_d, d_d, nf, nr)
+        rm, rb, rd, rnf, rnr = OD.unmask_threshold(conf.numpy(), pred.numpy(),
+                                                   mask.numpy().view(np.uint32), blk.numpy(),
+                                                   dr.numpy(), tau, taur)
+        assert np.array_equal(m_d.cpu().numpy().view(np.uint32), rm), (tau, taur)
+        assert np.array_equal(b_d.cpu().numpy(), rb), (tau, taur)
+        assert np.array_equal(d_d.cpu().numpy(), rd), (tau, taur)
+        assert np.array_equal(nf.cpu().numpy(), rnf) and np.array_equal(nr.cpu().numpy(), rnr)
+
+
+def test_unmask_threshold_rejects_bad_arguments(nd):
+    z = torch.zeros((1, 32), device="cuda")
+    zi = torch.zeros((1, 32), dtype=torch.int32, device="cuda")
+    m = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for tau, taur in ((-0.1, 2.0), (0.5, -1.0), (float("nan"), 2.0)):
+        with pytest.raises(nd.NdiffError):
+            nd.ndiff_unmask_threshold(z, zi, 1, 32, tau, taur, m, zi, zi)
+
+
 # ---------------------------------------------------------------- verify/accept
 @pytest.mark.parametrize("B,T", [(64, 32), (5, 1), (33, 7), (1000, 32)])
 def test_verify_accept(nd, B, T):

@@ -111,3 +111,85 @@ def test_verify_accept_bruteforce():
         assert (commit[b, n[b]:] == -1).all()
         if L[b] < T:
             assert commit[b, L[b]] == target[b, L[b]] and draft[b, L[b]] != target[b, L[b]]
+
+
+# ---------------------------------------------------------------- threshold sampler
+def _round(conf, pred, mask, tau, tau_rev=2.0, T=None, draft=None):
+    conf = np.asarray(conf, dtype=np.float64)[None]
+    T = conf.shape[1]
+    blk = np.full((1, T), 7, dtype=np.int32)
+    dr = np.full((1, T), -1, dtype=np.int32) if draft is None else np.asarray(draft)[None].astype(np.int32)
+    return Dd.unmask_threshold(conf, np.asarray(pred)[None], [mask], blk, dr, tau, tau_rev)
+
+
+@pytest.mark.parametrize("T", [1, 4, 6])
+def test_threshold_above_one_is_the_top1_rule(T):
+    """tau > 1 (no confidence reaches it) fixes exactly the slot the fixed-k
+    rule with k = 1 fixes, for every mask."""
+    rng = np.random.default_rng(20 + T)
+    conf = rng.integers(1, 4, size=(1, T)) / 4.0
+    pred = rng.integers(0, 1000, size=(1, T))
+    for mask in range(1, 1 << T):
+        blk = np.full((1, T), 7, dtype=np.int32)
+        dr = np.full((1, T), -1, dtype=np.int32)
+        a = Dd.unmask(conf, pred, [mask], blk, dr, 1)
+        b = Dd.unmask_threshold(conf, pred, [mask], blk, dr, 1.5)
+        assert int(a[0][0]) == int(b[0][0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+        assert b[3][0] == 1
+
+
+@pytest.mark.parametrize("T", [1, 5, 32])
+def test_threshold_at_zero_fixes_every_masked_slot(T):
+    """tau <= min conf fixes all masked slots at once: the fixed-k rule with k = T."""
+    rng = np.random.default_rng(30 + T)
+    conf = rng.random((1, T)) + 1e-3
+    pred = rng.integers(0, 1000, size=(1, T))
+    mask = int(rng.integers(1, 1 << T))
+    blk = np.full((1, T), 7, dtype=np.int32)
+    dr = np.full((1, T), -1, dtype=np.int32)
+    a = Dd.unmask(conf, pred, [mask], blk, dr, T)
+    b = Dd.unmask_threshold(conf, pred, [mask], blk, dr, 0.0)
+    assert int(b[0][0]) == 0 and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert b[3][0] == bin(mask).count("1")
+
+
+def test_threshold_counts_and_inputs_bruteforce():
+    """Random rounds: the fixed set is {masked, conf >= tau} or the first
+    maximiser; block_in[i+1] carries draft[i] for every fixed slot."""
+    rng = np.random.default_rng(41)
+    T = 32
+    for trial in range(300):
+        conf = np.round(rng.random(T) * 8) / 8
+        pred = rng.integers(0, 100, size=T)
+        mask = int(rng.integers(0, 1 << T))
+        tau = float(rng.choice([0.25, 0.5, 0.875, 1.0, 1.5]))
+        m2, b2, d2, nf, nr = _round(conf, pred, mask, tau)
+        masked = [i for i in range(T) if (mask >> i) & 1]
+        want = [i for i in masked if conf[i] >= tau]
+        if not want and masked:
+            top = max(conf[i] for i in masked)
+            want = [min(i for i in masked if conf[i] == top)]
+        assert nf[0] == len(want) and nr[0] == 0
+        assert int(m2[0]) == mask & ~sum(1 << i for i in want)
+        for i in range(T):
+            assert d2[0, i] == (pred[i] if i in want else -1)
+            if i >= 1:
+                assert b2[0, i] == (pred[i - 1] if i - 1 in want else 7)
+
+
+def test_revision_replaces_disagreeing_earlier_slots():
+    """Slots fixed in earlier rounds are replaced exactly when the new
+    prediction differs and its confidence reaches tau_revise; slots fixed
+    in this round are not revised; tau_revise > 1 never revises."""
+    T = 8
+    draft = np.array([5, 6, 7, 8, -1, -1, -1, -1])
+    pred = np.array([5, 60, 70, 80, 1, 2, 3, 4])
+    conf = np.array([0.9, 0.9, 0.3, 0.6, 0.1, 0.95, 0.2, 0.2])
+    mask = 0b11110000
+    m2, b2, d2, nf, nr = _round(conf, pred, mask, 0.9, 0.5, draft=draft)
+    assert nr[0] == 2                       # slots 1 (0.9) and 3 (0.6); slot 2 below 0.5; slot 0 agrees
+    assert list(d2[0, :4]) == [5, 60, 7, 80]
+    assert b2[0, 2] == 60 and b2[0, 4] == 80 and b2[0, 3] == 7
+    assert nf[0] == 1 and d2[0, 5] == 2 and int(m2[0]) == 0b11010000
+    m3, b3, d3, nf3, nr3 = _round(conf, pred, mask, 0.9, 1.5, draft=draft)
+    assert nr3[0] == 0 and list(d3[0, :4]) == [5, 6, 7, 8]

@@ -116,3 +116,43 @@ def test_golden_tiny_tokens():
     for key, (mode, steps) in {"ar": ("ar", 1), "diff_k4": ("diff", 8), "selfspec_s1": ("selfspec", 1)}.items():
         s = model.Session(cfg, w, max_seq=200); s.prefill(pr)
         assert s.generate(mode, 64, steps) == g[key], key
+
+
+# ---------------------------------------------------------------- threshold sampler
+def test_threshold_sampler_special_cases_reduce_to_topk():
+    """tau above 1 fixes one slot per round: the top-k draft with 32 rounds;
+    tau 0 fixes every slot in the first round: the top-k draft with 1 round."""
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    for steps, tau in ((32, (1.5, 2.0)), (1, (0.0, 2.0))):
+        a = model.Session(cfg, w, max_seq=200); a.prefill(pr)
+        b = model.Session(cfg, w, max_seq=200); b.prefill(pr)
+        assert a.generate("diff", 64, steps) == b.generate("diff", 64, tau=tau)
+        assert a.forwards == b.forwards == 2 * (steps + 1)
+
+
+@pytest.mark.parametrize("tau", [(0.05, 2.0), (0.02, 0.5), (0.3, 0.0)])
+def test_threshold_selfspec_equals_ar(tau):
+    """Whatever the draft sampler, verification makes self-speculation emit
+    the AR tokens."""
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, w, max_seq=200); s.prefill(pr)
+    ar = s.generate("ar", 48)
+    s2 = model.Session(cfg, w, max_seq=200); s2.prefill(pr)
+    assert s2.generate("selfspec", 48, tau=tau) == ar
+
+
+def test_threshold_diff_rounds_and_revisions():
+    """A mid threshold takes between 1 and 32 rounds per block; tau_revise 0
+    revises every earlier slot whose prediction changed, so revisions happen;
+    every committed id is a real token."""
+    cfg = tiny_cfg()
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, max_seq=200); s.prefill(pr)
+    toks = s.generate("diff", 64, tau=(0.05, 0.0))
+    assert len(toks) == 64 and all(0 <= t < cfg.vocab - 1 for t in toks)
+    assert 2 * 2 <= s.forwards <= 2 * 33
+    assert s.revisions > 0
