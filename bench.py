@@ -45,7 +45,7 @@ METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward
 # DRAM bytes (read + write) of one attention launch, from ncu captures of the
 # current attention kernel on these workloads (summaries under profiles/);
 # None where no capture exists.
-ATTN_TRAFFIC = {"attn-batched": 1016151040 + 17371904, "attn-long": 539035904 + 3553024,
+ATTN_TRAFFIC = {"attn-batched": 1016157440 + 9754880, "attn-long": 539045120 + 72704,
                 "attn-single": None}
 SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126e6
