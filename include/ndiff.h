@@ -238,11 +238,15 @@ NDIFF_API ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* 
  * on at most one 32-token block at a time ([FFI] "三种生成模式"; [HFB]:
  * decode is bound by memory traffic, i.e. by streaming w).
  * x: bf16 [M][K] row-major, w: bf16 [N][K] row-major (both 16-byte aligned),
- * y: fp32 [M][ldy] (ldy >= N). 1 <= M <= 32, N >= 1, K a positive multiple of
- * 64. fp32 accumulation on the tensor cores; a row's result does not depend on
- * M (the same row computed alone or inside a block is bit-identical).
+ * y: fp32 [M][ldy] (ldy >= N). M >= 1, N >= 1, K a positive multiple of 64.
+ * fp32 accumulation on the tensor cores. M <= 32 runs the weight-streaming
+ * kernel of single-sequence decode (MMA N = 32); larger M, a batch of
+ * sequences, runs the wide kernel (MMA N = 256, 256-row token chunks). Within
+ * each of the two ranges a row's result does not depend on M (the same row
+ * computed alone or inside a larger block is bit-identical).
  * ws/ws_bytes: device scratch of at least ndiff_gemm_bf16_workspace_size()
- *   bytes; its contents need no initialisation (the call clears what it needs).
+ *   bytes (0 for M > 32; ws may then be NULL); its contents need no
+ *   initialisation (the call clears what it needs).
  * ------------------------------------------------------------------------ */
 NDIFF_API size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K);
 NDIFF_API ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, float* y,
@@ -259,11 +263,12 @@ NDIFF_API ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int 
  * ([FFI] "三种生成模式"; [HFB]: decode is bound by memory traffic, and this
  * removes the write and re-read of the [M][N] logits).
  * x: bf16 [M][K] row-major, w: bf16 [N][K] row-major (16-byte aligned);
- * 1 <= M <= 32, N >= 1, K a positive multiple of 64, -1 <= exclude_id < N.
+ * M >= 1 (M > 32: the wide kernel, as in ndiff_gemm_bf16), N >= 1, K a
+ * positive multiple of 64, -1 <= exclude_id < N.
  * argmax int32 [M], conf float [M] (device). The logits are the fp32 values
  * ndiff_gemm_bf16 produces, so argmax equals ndiff_gemm_bf16 followed by
  * ndiff_logits_reduce exactly; conf agrees to fp32 rounding. A row's results
- * do not depend on M.
+ * do not depend on M within M <= 32, nor within M > 32.
  * ws/ws_bytes: device scratch of at least ndiff_lm_head_argmax_workspace_size()
  *   bytes; contents need no initialisation.
  * ------------------------------------------------------------------------ */

@@ -307,6 +307,7 @@ ndiff_status ndiff_selftest_timeout(int limit_us, cudaStream_t stream) {
 
 size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 64) return 0;
+  if (M > 32) return 0;  // the wide kernel needs no scratch
   const GemmPlan pl = gemm_plan(N, K);
   const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
   return cnt + gemm_partials_bytes(pl);
@@ -314,38 +315,49 @@ size_t ndiff_gemm_bf16_workspace_size(int M, int N, int K) {
 
 ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, float* y,
                              int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0 || ldy < N)
+  if (M < 1 || N < 1 || K < 64 || K % 64 != 0 || ldy < N)
     return set_error(NDIFF_ERR_INVALID_ARG,
-                     "ndiff_gemm_bf16: need 1<=M<=32, N>=1, K a positive multiple of 64, ldy>=N "
+                     "ndiff_gemm_bf16: need M>=1, N>=1, K a positive multiple of 64, ldy>=N "
                      "(M=%d N=%d K=%d ldy=%lld)",
                      M, N, K, (long long)ldy);
   if (!x || !w || !y) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_gemm_bf16: null pointer");
   if (!aligned16(x) || !aligned16(w))
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_gemm_bf16: x and w must be 16-byte aligned");
   const size_t need = ndiff_gemm_bf16_workspace_size(M, N, K);
-  if (!ws || ws_bytes < need)
+  if (need > 0 && (!ws || ws_bytes < need))
     return set_error(NDIFF_ERR_WORKSPACE, "ndiff_gemm_bf16: workspace of %zu bytes needed, %zu given",
                      need, ws_bytes);
-  const GemmPlan pl = gemm_plan(N, K);
-  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
-  CUtensorMap tw, tx;
-  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
-  if (s != NDIFF_OK) return s;
-  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.N = N;
   p.T = M;
   p.mode = GEMM_EPI_F32;
-  p.counters = static_cast<int*>(ws);
-  p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt);
   p.out = y;
   p.ldo = ldy;
+  CUtensorMap tw, tx;
+  if (M > 32) {
+    ndiff_status s = gemm_make_maps(w, N, K, false, nullptr, 0, &tw, nullptr);
+    if (s != NDIFF_OK) return s;
+    s = gemm_wide_make_xmap(x, M, K, &tx);
+    if (s != NDIFF_OK) return s;
+    return launch_gemm_wide(tw, tx, gemm_wide_plan(N, K, M), p, stream);
+  }
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
+  if (s != NDIFF_OK) return s;
+  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
+  p.counters = static_cast<int*>(ws);
+  p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt);
   return launch_gemm_bf16(tw, tx, pl, p, stream);
 }
 
 size_t ndiff_lm_head_argmax_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 64) return 0;
+  if (M > 32) {
+    const GemmPlan pl = gemm_wide_plan(N, K, M);
+    return (size_t)pl.ntiles * M * sizeof(float4);
+  }
   const GemmPlan pl = gemm_plan(N, K);
   const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
   const size_t part = (gemm_partials_bytes(pl) + 255) & ~(size_t)255;
@@ -355,9 +367,9 @@ size_t ndiff_lm_head_argmax_workspace_size(int M, int N, int K) {
 ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M, int N, int K, int exclude_id,
                                   int32_t* argmax, float* conf, void* ws, size_t ws_bytes,
                                   cudaStream_t stream) {
-  if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0 || exclude_id < -1 || exclude_id >= N)
+  if (M < 1 || N < 1 || K < 64 || K % 64 != 0 || exclude_id < -1 || exclude_id >= N)
     return set_error(NDIFF_ERR_INVALID_ARG,
-                     "ndiff_lm_head_argmax: need 1<=M<=32, N>=1, K a positive multiple of 64, "
+                     "ndiff_lm_head_argmax: need M>=1, N>=1, K a positive multiple of 64, "
                      "-1<=exclude_id<N (M=%d N=%d K=%d exclude_id=%d)",
                      M, N, K, exclude_id);
   if (!x || !w || !argmax || !conf)
@@ -368,25 +380,36 @@ ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M, int N, in
   if (!ws || ws_bytes < need)
     return set_error(NDIFF_ERR_WORKSPACE,
                      "ndiff_lm_head_argmax: workspace of %zu bytes needed, %zu given", need, ws_bytes);
-  const GemmPlan pl = gemm_plan(N, K);
-  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
-  const size_t part = (gemm_partials_bytes(pl) + 255) & ~(size_t)255;
-  CUtensorMap tw, tx;
-  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
-  if (s != NDIFF_OK) return s;
-  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.N = N;
   p.T = M;
   p.mode = GEMM_EPI_ARGMAX;
+  p.excl = exclude_id;
+  CUtensorMap tw, tx;
+  if (M > 32) {
+    const GemmPlan pl = gemm_wide_plan(N, K, M);
+    ndiff_status s = gemm_make_maps(w, N, K, false, nullptr, 0, &tw, nullptr);
+    if (s != NDIFF_OK) return s;
+    s = gemm_wide_make_xmap(x, M, K, &tx);
+    if (s != NDIFF_OK) return s;
+    p.red = static_cast<float4*>(ws);
+    s = launch_gemm_wide(tw, tx, pl, p, stream);
+    if (s != NDIFF_OK) return s;
+    return launch_argmax_merge(p.red, pl.ntiles, M, M, argmax, conf, stream);
+  }
+  const GemmPlan pl = gemm_plan(N, K);
+  const size_t cnt = (((size_t)pl.ntiles * 4) + 255) & ~(size_t)255;
+  const size_t part = (gemm_partials_bytes(pl) + 255) & ~(size_t)255;
+  ndiff_status s = gemm_make_maps(w, N, K, false, x, M, &tw, &tx);
+  if (s != NDIFF_OK) return s;
+  NDIFF_CUDA_TRY(cudaMemsetAsync(ws, 0, (size_t)pl.ntiles * 4, stream));
   p.counters = static_cast<int*>(ws);
   p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt);
   p.red = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + cnt + part);
-  p.excl = exclude_id;
   s = launch_gemm_bf16(tw, tx, pl, p, stream);
   if (s != NDIFF_OK) return s;
-  return launch_argmax_merge(p.red, pl.ntiles, M, argmax, conf, stream);
+  return launch_argmax_merge(p.red, pl.ntiles, M, 32, argmax, conf, stream);
 }
 
 }  // extern "C"

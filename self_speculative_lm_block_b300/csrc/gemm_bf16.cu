@@ -518,14 +518,14 @@ __global__ void __launch_bounds__(THREADS, 2)
 constexpr int MERGE_THREADS = 256;
 
 __global__ void __launch_bounds__(MERGE_THREADS)
-    argmax_merge_kernel(const float4* __restrict__ red, int ntiles, int32_t* __restrict__ argmax,
-                        float* __restrict__ conf) {
+    argmax_merge_kernel(const float4* __restrict__ red, int ntiles, int stride,
+                        int32_t* __restrict__ argmax, float* __restrict__ conf) {
   griddep_launch();
   griddep_wait();
   const int t = blockIdx.x;
   Red a{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
   for (int i = threadIdx.x; i < ntiles; i += MERGE_THREADS) {
-    const float4 f = __ldcg(red + (size_t)i * MT + t);
+    const float4 f = __ldcg(red + (size_t)i * stride + t);
     red_merge(a, Red{f.x, f.y, f.z, __float_as_int(f.w)});
   }
 #pragma unroll
@@ -548,11 +548,11 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 
 }  // namespace gemm
 
-ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int32_t* argmax, float* conf,
-                                 cudaStream_t stream) {
+ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int stride, int32_t* argmax,
+                                 float* conf, cudaStream_t stream) {
   if (T <= 0) return NDIFF_OK;
   NDIFF_CUDA_TRY(launch_k(gemm::argmax_merge_kernel, dim3(T), dim3(gemm::MERGE_THREADS), 0, stream,
-                          red, ntiles, argmax, conf));
+                          red, ntiles, stride, argmax, conf));
   return NDIFF_OK;
 }
 
@@ -580,6 +580,7 @@ GemmPlan gemm_plan(int N, int K) {
     }
   }
   pl.S = bestS;
+  pl.nchunks = 1;
   pl.items = pl.ntiles * pl.S;
   pl.grid = pl.items < sms ? pl.items : sms;
   return pl;

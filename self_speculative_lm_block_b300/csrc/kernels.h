@@ -65,10 +65,13 @@ struct GemmParams {
   float4* red;             // ARGMAX: per (tile, token row) (max, sum of exp(y - max),
                            // best allowed value, its id as int bits) [tiles][32]
   int excl;                // ARGMAX: id left out of the argmax (-1: none)
+  int Tb;                  // wide kernel, QKV: tokens per sequence (token m is slot m % Tb
+                           // of sequence m / Tb; caches [B][Hkv][Lmax][128], kv_len [B])
 };
 
 struct GemmPlan {
   int ntiles, nks, S, items, grid;
+  int nchunks;             // wide kernel: 256-row token chunks (1 for the skinny kernel)
 };
 
 GemmPlan gemm_plan(int N, int K);
@@ -77,9 +80,18 @@ ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const voi
                             CUtensorMap* tmW, CUtensorMap* tmX);
 ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
                               GemmParams p, cudaStream_t stream);
-// Merges the per-tile partials of a GEMM_EPI_ARGMAX launch: argmax[t] and the
-// softmax probability conf[t] of that id for token rows t < T.
-ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int32_t* argmax, float* conf,
-                                 cudaStream_t stream);
+// Merges the per-tile partials of a GEMM_EPI_ARGMAX launch (red[tile * stride
+// + t]): argmax[t] and the softmax probability conf[t] of that id for token
+// rows t < T.
+ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int stride, int32_t* argmax,
+                                 float* conf, cudaStream_t stream);
+
+// The projection for any number of token rows M (several sequences): items of
+// (128-row weight tile, 256-row token chunk), tcgen05 M128 N256, no K split.
+// The X map has 256-row boxes (gemm_wide_make_xmap); W maps as gemm_make_maps.
+GemmPlan gemm_wide_plan(int N, int K, int M);
+ndiff_status gemm_wide_make_xmap(const void* x, int M, int K, CUtensorMap* tmX);
+ndiff_status launch_gemm_wide(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                              GemmParams p, cudaStream_t stream);
 
 }  // namespace ndiff

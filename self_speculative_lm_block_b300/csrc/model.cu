@@ -269,7 +269,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     p.red = m->red;
     p.excl = m->mask_id;
     TRY(launch_gemm_bf16(m->tm_lm, m->tm_h, m->pl_lm, p, s));
-    return launch_argmax_merge(m->red, m->pl_lm.ntiles, T, m->pred, m->conf, s);
+    return launch_argmax_merge(m->red, m->pl_lm.ntiles, T, 32, m->pred, m->conf, s);
   }
   if (m->bf16) {
     GemmParams p = gp;

@@ -139,11 +139,27 @@ def test_gemm_lm_head_shape_sampled(nd):
     assert (np.abs(y[:, cols] - ref) <= bound).all()
 
 
+@pytest.mark.parametrize("M,N,K", [(33, 300, 128), (256, 4096, 512), (300, 1000, 4096),
+                                   (2048, 6144, 4096)])
+def test_gemm_wide_within_fp32_bound(nd, M, N, K):
+    """More than 32 token rows (a batch of sequences) run the wide kernel."""
+    _gemm_check(nd, M, N, K, seed=M * 3 + N + K)
+
+
+def test_gemm_wide_rows_do_not_depend_on_batch(nd):
+    x = synth.normal_bf16((700, 2048), 1.0, 15, 1)
+    w = synth.normal_bf16((3000, 2048), 0.02, 15, 2)
+    y = nd.gemm_bf16(x.cuda(), w.cuda())
+    for M in (33, 300, 513):
+        ym = nd.gemm_bf16(x[:M].cuda(), w.cuda())
+        assert torch.equal(ym, y[:M]), M
+
+
 def test_gemm_rejects_bad_shapes(nd):
-    x = torch.zeros((33, 64), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(nd.NdiffError):
-        nd.gemm_bf16(x, w)
+        nd.ndiff_gemm_bf16(torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda"), w, 0, 128, 64,
+                           torch.zeros((1, 128), device="cuda"), 128, None, 0)
     with pytest.raises(nd.NdiffError):
         nd.gemm_bf16(torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda"),
                      torch.zeros((8, 96), dtype=torch.bfloat16, device="cuda"))
@@ -192,6 +208,14 @@ def test_lm_head_argmax_matches_unfused_and_oracle(nd, M, N, K, excl):
     _lm_head_check(nd, M, N, K, excl, seed=M + N + K)
 
 
+@pytest.mark.parametrize("M,N,K,excl", [(33, 4173, 512, 4172), (300, 20000, 1024, 0)])
+def test_lm_head_argmax_wide(nd, M, N, K, excl):
+    """Batches of more than 32 token rows (the wide kernel), every row against
+    the unfused path and 48 rows against the oracle."""
+    rows = np.random.default_rng(M).choice(M, min(M, 48), replace=False)
+    _lm_head_check(nd, M, N, K, excl, seed=M + N, oracle_rows=rows)
+
+
 def test_lm_head_argmax_8b_shape(nd):
     """The 8B LM head (151936 x 4096) at a 32-token block, every row against
     the oracle's float64 logits."""
@@ -235,7 +259,7 @@ def test_lm_head_argmax_rejects_bad_arguments(nd):
     with pytest.raises(nd.NdiffError):
         nd.lm_head_argmax(x, w, 128)          # exclude_id >= N
     with pytest.raises(nd.NdiffError):
-        nd.lm_head_argmax(torch.zeros((33, 64), dtype=torch.bfloat16, device="cuda"), w, -1)
+        nd.lm_head_argmax(x, w, -2)
 
 
 # ---------------------------------------------------------------- weights
