@@ -298,7 +298,12 @@ NDIFF_API ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M,
  * dtype NDIFF_BF16: bf16 weights, bf16 GEMM inputs, fp32 residual stream and
  *   accumulators; requires head_dim == 128, d_model % 128 == 0, ffn % 128 == 0,
  *   n_heads/n_kv_heads * 32 <= 128.
- * Batch 1 only (batch must be 1).
+ * batch: sequences decoded together. 1 serves the single-sequence calls
+ *   (ndiff_prefill, ndiff_decode_step[_ex], ndiff_model_forward); B > 1 (bf16
+ *   models only) serves the batch calls (ndiff_prefill_batch,
+ *   ndiff_decode_step_batch), which run every projection on the wide kernel
+ *   over B*T token rows and attention over B ragged sequences ([TRI] Abstract:
+ *   the modes serve different deployment settings and concurrency levels).
  * ------------------------------------------------------------------------ */
 typedef struct {
     int layers;
@@ -312,7 +317,7 @@ typedef struct {
     float rope_base;
     float eps;
     int max_seq; /* KV cache capacity in tokens (prompt + generated + 32) */
-    int batch;   /* must be 1 */
+    int batch;   /* sequences decoded together (1 .. 4096; > 1 needs bf16) */
 } ndiff_model_config;
 
 typedef struct ndiff_model ndiff_model;
@@ -384,6 +389,33 @@ NDIFF_API ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int st
 NDIFF_API ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
                                             int32_t* out_tokens_host, int* n_out,
                                             ndiff_stats* stats, cudaStream_t stream);
+
+/* Batched sessions (cfg.batch = B > 1). Prefill: prompt b is
+ * prompts_host[sum_{c<b} lengths_host[c] ..] of lengths_host[b] tokens
+ * (1 <= n_b, n_b + 32 <= max_seq); each sequence's cache takes its prompt but
+ * the last token, which becomes its pending token. The prompts advance 32
+ * tokens per forward together; a sequence whose prompt is used up runs filler
+ * tokens past its prefix (scratch cache rows that the next block overwrites).
+ * Synchronous on return. */
+NDIFF_API ndiff_status ndiff_prefill_batch(ndiff_model* m, const int32_t* prompts_host,
+                                           const int32_t* lengths_host, cudaStream_t stream);
+
+/* One decode cycle of all B sequences in opts->mode (as ndiff_decode_step_ex):
+ * every forward runs the B blocks (or B pending tokens in AR) together, and
+ * unmasking, verification and commits are per sequence, so accept lengths
+ * differ from sequence to sequence. out_tokens_host [B][32] receives sequence
+ * b's committed tokens in row b, n_out_host [B] their counts. stats counts
+ * batch forwards and the tokens of all sequences; accept_hist counts every
+ * sequence's verification. The fixed-schedule cycle is one CUDA graph.
+ * Synchronous on return. */
+NDIFF_API ndiff_status ndiff_decode_step_batch(ndiff_model* m, const ndiff_decode_opts* opts,
+                                               int32_t* out_tokens_host, int32_t* n_out_host,
+                                               ndiff_stats* stats, cudaStream_t stream);
+
+/* Per-sequence committed prefix lengths and pending tokens ([B] host arrays,
+ * either may be NULL). */
+NDIFF_API ndiff_status ndiff_model_state_batch(const ndiff_model* m, int32_t* kv_len_host,
+                                               int32_t* last_host);
 
 /* Runs one forward of `T` block tokens (host ids) at the model's current
  * position with the given mask, writes fp32 logits [T][vocab] to the host

@@ -82,6 +82,7 @@ struct ndiff_model {
   void* ob = nullptr;        // attention output [32][Hq D]
   void* ab = nullptr;        // SwiGLU output [32][ffn]
   float* y = nullptr;        // fp32 path projection scratch [32][ymax]
+  int B = 1;                 // sequences decoded together; activations hold B * 32 rows
   float* logits = nullptr;   // [32][ldl] fp32 (rows 16-byte aligned)
   int ldl = 0;
   // decode-cycle state
@@ -90,10 +91,16 @@ struct ndiff_model {
   float* conf = nullptr;        // [32]
   int32_t* draft = nullptr;     // [32]
   int32_t* block_in = nullptr;  // [32]
-  int32_t* res = nullptr;       // [64]: commit[32], n_commit, accept_len; [40..41] the threshold
-                                //   round's fixed and revised counts
-  int32_t* kv_len = nullptr;    // [1]
-  uint32_t* mask = nullptr;     // [1]
+  // per-sequence results, one contiguous block for the host read:
+  // commit [B][32] | n_commit [B] | accept_len [B] | fixed [B] | revised [B]
+  int32_t* res = nullptr;
+  int32_t* commit = nullptr;
+  int32_t* ncommit = nullptr;
+  int32_t* acclen = nullptr;
+  int32_t* nfixed = nullptr;
+  int32_t* nrevised = nullptr;
+  int32_t* kv_len = nullptr;    // [B]
+  uint32_t* mask = nullptr;     // [B]
   int32_t* chosen = nullptr;    // [32]
   int32_t* prompt = nullptr;    // [Lmax]
   float2* rope = nullptr;       // [Lmax][D/2]
@@ -104,15 +111,17 @@ struct ndiff_model {
   size_t aws_bytes = 0;
   int attn_split = 0;
   CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
+  CUtensorMap tm_h_w, tm_oact_w, tm_a_w;  // 256-row boxes for the wide kernel (B > 1)
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
-  int32_t* pin = nullptr;       // pinned host staging [64]
-  int32_t* last_dev = nullptr;  // [1] pending last token (device copy of `last`)
+  int32_t* pin = nullptr;       // pinned host staging [pin_n]
+  size_t pin_n = 0;
+  int32_t* last_dev = nullptr;  // [B] pending last token per sequence
   cudaStream_t ms = nullptr;    // the model's own stream (decode graphs run here)
   // decode graphs by (part, mode, steps, tau bits, tau_revise bits)
   std::map<std::tuple<int, int, int, uint32_t, uint32_t>, cudaGraphExec_t> graphs;
   std::vector<void*> allocs;
-  int P = 0;
-  int32_t last = -1;
+  std::vector<int> P;          // committed prefix per sequence (host view)
+  std::vector<int32_t> last;   // pending token per sequence (host view)
   bool ready = false;
 };
 
@@ -158,8 +167,10 @@ ndiff_status check_config(const ndiff_model_config* c) {
       c->ffn < 1 || c->vocab < 2 || c->max_seq < kBlock + 1 || !(c->eps > 0.f) ||
       !(c->rope_base > 1.f))
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: bad sizes in config");
-  if (c->batch != 1)
-    return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_create: batch must be 1 (got %d)", c->batch);
+  if (c->batch < 1 || c->batch > 4096)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: batch in [1, 4096] (got %d)", c->batch);
+  if (c->batch > 1 && c->dtype != NDIFF_BF16)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_create: batch > 1 needs a bf16 model");
   if (c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_create: n_heads %% n_kv_heads and head_dim %% 2 must be 0");
   if (c->dtype == NDIFF_BF16) {
@@ -168,7 +179,7 @@ ndiff_status check_config(const ndiff_model_config* c) {
       return set_error(NDIFF_ERR_UNSUPPORTED,
                        "ndiff_model_create: bf16 models need head_dim 128, d_model and ffn multiples "
                        "of 128, and n_heads/n_kv_heads <= 4");
-    if ((long long)c->n_kv_heads * c->max_seq >= (1LL << 31))
+    if ((long long)c->batch * c->n_kv_heads * c->max_seq >= (1LL << 31))
       return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_create: KV cache too large");
   } else if (c->dtype == NDIFF_F32) {
     if (c->head_dim > 64 || c->d_model > 4096 || c->vocab > (1 << 20))
@@ -188,22 +199,35 @@ ndiff_status check_config(const ndiff_model_config* c) {
 // folds the tiles.
 enum { FWD_NONE = 0, FWD_TOKENS = 1, FWD_LOGITS = 2 };
 
-// Runs the T (<= 32) tokens `ids` (device) at positions kv_len .. kv_len+T-1
-// and writes their K/V into the cache there.
+// Runs T (<= 32) tokens of each of the B sequences (`ids` [B][T], device) at
+// positions kv_len[b] .. kv_len[b]+T-1 and writes their K/V into each
+// sequence's cache there. A single sequence uses the weight-streaming kernel
+// (MMA N = 32); a batch uses the wide kernel (MMA N = 256) for every
+// projection, so a row's arithmetic is the same in AR (T = 1) and block
+// (T = 32) forwards either way.
 ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int out,
                      cudaStream_t s) {
   PdlScope pdl(m->bf16);
   const float scale = 1.f / sqrtf((float)m->D);
-  TRY(launch_embed(m->embed, m->bf16, ids, T, m->V, m->d, m->x, s));
+  const int B = m->B, M = B * T;
+  const bool wide = B > 1;
+  TRY(launch_embed(m->embed, m->bf16, ids, M, m->V, m->d, m->x, s));
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
-  gp.T = T;
+  gp.T = M;
+  gp.Tb = T;
   gp.w_tiled = 1;
   gp.ws = m->gws;
   gp.counters = m->gcnt;
+  // one projection: W [N][K] against the activation behind tx (skinny) / txw (wide)
+  auto proj = [&](const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& txw,
+                  const GemmPlan& pl, int N, int K, const GemmParams& p) -> ndiff_status {
+    if (wide) return launch_gemm_wide(tw, txw, gemm_wide_plan(N, K, M), p, s);
+    return launch_gemm_bf16(tw, tx, pl, p, s);
+  };
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
-    TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, m->bf16, s));
+    TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s));
     if (m->bf16) {
       GemmParams p = gp;
       p.N = m->NQKV;
@@ -216,28 +240,28 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.Lmax = m->Lmax;
       p.kv_len = m->kv_len;
       p.rope = m->rope;
-      TRY(launch_gemm_bf16(ly.tm_qkv, m->tm_h, m->pl_qkv, p, s));
-      TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, 1, T, m->Hq, m->Hkv, m->Lmax, causal,
+      TRY(proj(ly.tm_qkv, m->tm_h, m->tm_h_w, m->pl_qkv, m->NQKV, m->d, p));
+      TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, B, T, m->Hq, m->Hkv, m->Lmax, causal,
                            scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s));
       p = gp;
       p.N = m->d;
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(launch_gemm_bf16(ly.tm_o, m->tm_oact, m->pl_o, p, s));
-      TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, true, s));
+      TRY(proj(ly.tm_o, m->tm_oact, m->tm_oact_w, m->pl_o, m->d, m->HD, p));
+      TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, true, s));
       p = gp;
       p.N = 2 * m->ffn;
       p.mode = GEMM_EPI_SWIGLU;
       p.act = static_cast<__nv_bfloat16*>(m->ab);
       p.lda = m->ffn;
-      TRY(launch_gemm_bf16(ly.tm_gu, m->tm_h, m->pl_gu, p, s));
+      TRY(proj(ly.tm_gu, m->tm_h, m->tm_h_w, m->pl_gu, 2 * m->ffn, m->d, p));
       p = gp;
       p.N = m->d;
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(launch_gemm_bf16(ly.tm_d, m->tm_a, m->pl_d, p, s));
+      TRY(proj(ly.tm_d, m->tm_a, m->tm_a_w, m->pl_d, m->d, m->ffn, p));
     } else {
       const float* h = static_cast<const float*>(m->h);
       TRY(launch_linear_f32(h, m->d, static_cast<const float*>(ly.wqkv), m->NQKV, m->d, m->y,
@@ -261,16 +285,18 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     }
   }
   if (out == FWD_NONE) return NDIFF_OK;
-  TRY(launch_rmsnorm(m->x, T, m->d, m->eps, m->h, m->bf16, s));
+  TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s));
   if (m->bf16 && out == FWD_TOKENS) {
     GemmParams p = gp;
     p.N = m->V;
     p.mode = GEMM_EPI_ARGMAX;
     p.red = m->red;
     p.excl = m->mask_id;
-    TRY(launch_gemm_bf16(m->tm_lm, m->tm_h, m->pl_lm, p, s));
-    return launch_argmax_merge(m->red, m->pl_lm.ntiles, T, 32, m->pred, m->conf, s);
+    TRY(proj(m->tm_lm, m->tm_h, m->tm_h_w, m->pl_lm, m->V, m->d, p));
+    return launch_argmax_merge(m->red, m->pl_lm.ntiles, M, wide ? M : 32, m->pred, m->conf, s);
   }
+  if (wide)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "model logits are available for batch 1 only");
   if (m->bf16) {
     GemmParams p = gp;
     p.N = m->V;
@@ -289,10 +315,11 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
 // each fixing the k = 32/steps most confident masked slots.
 ndiff_status draft_block(ndiff_model* m, int steps, cudaStream_t s) {
   const int k = kBlock / steps;
-  TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev, m->mask_id, s));
+  TRY(launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev, m->mask_id, m->B, s));
   for (int i = 0; i < steps; ++i) {
     TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, s));
-    TRY(launch_unmask(m->conf, m->pred, 1, kBlock, k, m->mask, m->block_in, m->draft, m->chosen, s));
+    TRY(launch_unmask(m->conf, m->pred, m->B, kBlock, k, m->mask, m->block_in, m->draft, m->chosen,
+                      s));
   }
   return NDIFF_OK;
 }
@@ -302,13 +329,13 @@ ndiff_status enqueue_tail(ndiff_model* m, ndiff_mode mode, cudaStream_t s) {
   if (mode == NDIFF_MODE_DIFF) {
     // the finished block enters the cache through one bidirectional forward
     TRY(forward(m, m->block_in, kBlock, 0, FWD_NONE, s));
-    return launch_commit(m->draft, nullptr, kBlock, kBlock, m->last_dev, m->kv_len, s);
+    return launch_commit(m->draft, kBlock, nullptr, kBlock, kBlock, m->last_dev, m->kv_len, m->B, s);
   }
   // SELFSPEC: causal verification of [last, d0..d30], accept the agreeing prefix
   TRY(forward(m, m->block_in, kBlock, 1, FWD_TOKENS, s));
-  TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->res + 33, m->res, m->res + 32, m->kv_len,
-                           s));
-  return launch_commit(m->res, m->res + 32, 0, 0, m->last_dev, m->kv_len, s);
+  TRY(launch_verify_accept(m->draft, m->pred, m->B, kBlock, m->acclen, m->commit, m->ncommit,
+                           m->kv_len, s));
+  return launch_commit(m->commit, kBlock, m->ncommit, 0, 0, m->last_dev, m->kv_len, m->B, s);
 }
 
 // Enqueues one decode cycle; every input it reads (pending token, committed
@@ -317,7 +344,7 @@ ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStrea
   if (mode == NDIFF_MODE_AR) {
     // AR: one causal forward of [last]; commit its argmax.
     TRY(forward(m, m->last_dev, 1, 1, FWD_TOKENS, s));
-    return launch_commit(m->pred, nullptr, 1, 1, m->last_dev, m->kv_len, s);
+    return launch_commit(m->pred, 1, nullptr, 1, 1, m->last_dev, m->kv_len, m->B, s);
   }
   TRY(draft_block(m, steps, s));
   return enqueue_tail(m, mode, s);
@@ -403,8 +430,12 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   m->mask_id = m->V - 1;
   m->ldl = (m->V + 3) & ~3;
   m->eps = c.eps;
+  m->B = c.batch;
+  m->P.assign(m->B, 0);
+  m->last.assign(m->B, -1);
   const size_t esz = m->esz;
   const size_t d = m->d;
+  const size_t R = (size_t)m->B * kBlock;  // activation rows
   cudaStream_t s = 0;
 
   TRY(dalloc(m, &m->embed, (size_t)m->V * d * esz));
@@ -412,7 +443,7 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(dalloc(m, &m->lm, vpad * d * esz));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->lm, 0, vpad * d * esz, s));
   m->layers.resize(m->L);
-  const size_t kv_elems = (size_t)m->Hkv * m->Lmax * m->D;
+  const size_t kv_elems = (size_t)m->B * m->Hkv * m->Lmax * m->D;
   for (Layer& ly : m->layers) {
     TRY(dalloc(m, &ly.wqkv, (size_t)m->NQKV * d * esz));
     TRY(dalloc(m, &ly.wo, d * m->HD * esz));
@@ -424,34 +455,40 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     NDIFF_CUDA_TRY(cudaMemsetAsync(ly.vc, 0, kv_elems * esz, s));
   }
   const int ymax = m->NQKV > 2 * m->ffn ? m->NQKV : 2 * m->ffn;
-  TRY(dalloc_t(m, &m->x, kBlock * d * 4));
-  TRY(dalloc(m, &m->h, kBlock * d * esz));
-  TRY(dalloc(m, &m->qb, (size_t)kBlock * m->HD * esz));
-  TRY(dalloc(m, &m->ob, (size_t)kBlock * m->HD * esz));
-  TRY(dalloc(m, &m->ab, (size_t)kBlock * m->ffn * esz));
+  TRY(dalloc_t(m, &m->x, R * d * 4));
+  TRY(dalloc(m, &m->h, R * d * esz));
+  TRY(dalloc(m, &m->qb, R * m->HD * esz));
+  TRY(dalloc(m, &m->ob, R * m->HD * esz));
+  TRY(dalloc(m, &m->ab, R * m->ffn * esz));
   TRY(dalloc_t(m, &m->y, (size_t)kBlock * (ymax > m->d ? ymax : m->d) * 4));
   TRY(dalloc_t(m, &m->logits, (size_t)kBlock * m->ldl * 4));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->x, 0, kBlock * d * 4, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->h, 0, kBlock * d * esz, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->qb, 0, (size_t)kBlock * m->HD * esz, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ob, 0, (size_t)kBlock * m->HD * esz, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ab, 0, (size_t)kBlock * m->ffn * esz, s));
-  TRY(dalloc_t(m, &m->ids, kBlock * 4));
-  TRY(dalloc_t(m, &m->pred, kBlock * 4));
-  TRY(dalloc_t(m, &m->conf, kBlock * 4));
-  TRY(dalloc_t(m, &m->draft, kBlock * 4));
-  TRY(dalloc_t(m, &m->block_in, kBlock * 4));
-  TRY(dalloc_t(m, &m->res, 64 * 4));
-  TRY(dalloc_t(m, &m->kv_len, 16));
-  TRY(dalloc_t(m, &m->mask, 16));
-  TRY(dalloc_t(m, &m->chosen, kBlock * 4));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->x, 0, R * d * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->h, 0, R * d * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->qb, 0, R * m->HD * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ob, 0, R * m->HD * esz, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ab, 0, R * m->ffn * esz, s));
+  TRY(dalloc_t(m, &m->ids, R * 4));
+  TRY(dalloc_t(m, &m->pred, R * 4));
+  TRY(dalloc_t(m, &m->conf, R * 4));
+  TRY(dalloc_t(m, &m->draft, R * 4));
+  TRY(dalloc_t(m, &m->block_in, R * 4));
+  const size_t Bn = (size_t)m->B;
+  TRY(dalloc_t(m, &m->res, (R + 4 * Bn) * 4));
+  m->commit = m->res;
+  m->ncommit = m->res + R;
+  m->acclen = m->ncommit + Bn;
+  m->nfixed = m->acclen + Bn;
+  m->nrevised = m->nfixed + Bn;
+  TRY(dalloc_t(m, &m->kv_len, Bn * 4));
+  TRY(dalloc_t(m, &m->mask, Bn * 4));
+  TRY(dalloc_t(m, &m->chosen, R * 4));
   TRY(dalloc_t(m, &m->prompt, (size_t)m->Lmax * 4));
-  TRY(dalloc_t(m, &m->last_dev, 16));
+  TRY(dalloc_t(m, &m->last_dev, Bn * 4));
   TRY(dalloc_t(m, &m->rope, (size_t)m->Lmax * (m->D / 2) * sizeof(float2)));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, kBlock * 4, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, 16, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->last_dev, 0, 16, s));
-  NDIFF_CUDA_TRY(cudaMemsetAsync(m->block_in, 0, kBlock * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, R * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, Bn * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->last_dev, 0, Bn * 4, s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->block_in, 0, R * 4, s));
 
   if (m->bf16) {
     m->pl_qkv = gemm_plan(m->NQKV, m->d);
@@ -469,14 +506,17 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     }
     TRY(dalloc_t(m, &m->gws, ws));
     TRY(dalloc_t(m, &m->gcnt, (size_t)tiles * 4));
-    TRY(dalloc_t(m, &m->red, (size_t)m->pl_lm.ntiles * kBlock * sizeof(float4)));
+    TRY(dalloc_t(m, &m->red, (size_t)m->pl_lm.ntiles * R * sizeof(float4)));
     NDIFF_CUDA_TRY(cudaMemsetAsync(m->gcnt, 0, (size_t)tiles * 4, s));
-    m->attn_split = attn_bf16_auto_split(1, m->Hkv, m->Lmax);
-    m->aws_bytes = attn_bf16_workspace(1, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
+    m->attn_split = attn_bf16_auto_split(m->B, m->Hkv, m->Lmax);
+    m->aws_bytes = attn_bf16_workspace(m->B, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
     if (m->aws_bytes) TRY(dalloc(m, &m->aws, m->aws_bytes));
     TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, kBlock, nullptr, &m->tm_h));
     TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, kBlock, nullptr, &m->tm_oact));
     TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, kBlock, nullptr, &m->tm_a));
+    TRY(gemm_wide_make_xmap(m->h, (int)R, m->d, &m->tm_h_w));
+    TRY(gemm_wide_make_xmap(m->ob, (int)R, m->HD, &m->tm_oact_w));
+    TRY(gemm_wide_make_xmap(m->ab, (int)R, m->ffn, &m->tm_a_w));
     TRY(gemm_make_maps(m->lm, m->V, m->d, true, nullptr, 0, &m->tm_lm, nullptr));
     for (Layer& ly : m->layers) {
       TRY(gemm_make_maps(ly.wqkv, m->NQKV, m->d, true, nullptr, 0, &ly.tm_qkv, nullptr));
@@ -511,7 +551,10 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(launch_init_normal(m->lm, b, 1 + 8 * m->L, m->V, m->d, 0, ROWMAP_IDENTITY, b, seed, kSigma, s));
   TRY(launch_rope_table(m->rope, m->Lmax, m->D, (double)c.rope_base, s));
 
-  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&m->pin), 64 * sizeof(int32_t));
+  // host staging: the largest read (SELFSPEC results, R + 2 B ints), a
+  // threshold round's masks and counts (3 B), a prefill chunk (R + B)
+  m->pin_n = R + 8 * Bn + 64;
+  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&m->pin), m->pin_n * sizeof(int32_t));
   if (e != cudaSuccess) {
     m->pin = nullptr;
     return set_error(NDIFF_ERR_OOM, "ndiff_model_create: pinned host buffer: %s", cudaGetErrorString(e));
@@ -521,7 +564,7 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   // One forward of each block length sets every kernel attribute and device
   // lookup up front, so that later graph captures only record launches. The
   // cache rows it writes are scratch until a prefill fills them.
-  TRY(forward(m, m->ids, 1, 1, FWD_LOGITS, m->ms));
+  TRY(forward(m, m->ids, 1, 1, m->B > 1 ? FWD_TOKENS : FWD_LOGITS, m->ms));
   TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, m->ms));
   TRY(finish(m->ms));
   NDIFF_CUDA_TRY(cudaGetLastError());
@@ -598,6 +641,8 @@ ndiff_status ndiff_model_destroy(ndiff_model* m) {
 
 ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cudaStream_t stream) {
   if (!m || !prompt_host) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: null pointer");
+  if (m->B != 1)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_prefill: batched model; use ndiff_prefill_batch");
   if (n < 1 || n + kBlock > m->Lmax)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: need 1 <= n and n + 32 <= max_seq (n=%d, max_seq=%d)",
                      n, m->Lmax);
@@ -616,54 +661,126 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cu
   m->pin[0] = prompt_host[n - 1];
   NDIFF_CUDA_TRY(cudaMemcpyAsync(m->last_dev, m->pin, 4, cudaMemcpyHostToDevice, stream));
   TRY(finish(stream));
-  m->P = n - 1;
-  m->last = prompt_host[n - 1];
+  m->P[0] = n - 1;
+  m->last[0] = prompt_host[n - 1];
+  m->ready = true;
+  return NDIFF_OK;
+}
+
+ndiff_status ndiff_prefill_batch(ndiff_model* m, const int32_t* prompts_host,
+                                 const int32_t* lengths_host, cudaStream_t stream) {
+  if (!m || !prompts_host || !lengths_host)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill_batch: null pointer");
+  const int B = m->B;
+  std::vector<int64_t> off(B + 1, 0);
+  int longest = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = lengths_host[b];
+    if (n < 1 || n + kBlock > m->Lmax)
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "ndiff_prefill_batch: sequence %d: need 1 <= n and n + 32 <= max_seq (n=%d)", b, n);
+    off[b + 1] = off[b] + n;
+    longest = n > longest ? n : longest;
+  }
+  for (int64_t i = 0; i < off[B]; ++i)
+    if (prompts_host[i] < 0 || prompts_host[i] >= m->V)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill_batch: token out of range at %lld",
+                       (long long)i);
+  TRY(set_device(m));
+  m->ready = false;
+  // All sequences advance through their prompts 32 tokens per forward. A
+  // sequence whose prompt is used up runs filler tokens at positions past its
+  // prefix; those cache rows are scratch (the next block overwrites them) and
+  // no committed row attends to them.
+  const size_t R = (size_t)B * kBlock;
+  int32_t* ids = m->pin;
+  int32_t* kv = m->pin + R;
+  for (int c = 0; c * kBlock < longest - 1; ++c) {
+    for (int b = 0; b < B; ++b) {
+      const int n1 = lengths_host[b] - 1;  // prompt[0 .. n-2] enters the cache
+      const int p0 = c * kBlock < n1 ? c * kBlock : n1;
+      kv[b] = p0;
+      for (int i = 0; i < kBlock; ++i)
+        ids[(size_t)b * kBlock + i] = (p0 + i < n1 && c * kBlock + i < n1)
+                                          ? prompts_host[off[b] + c * kBlock + i]
+                                          : 0;
+    }
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->ids, ids, R * 4, cudaMemcpyHostToDevice, stream));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->kv_len, kv, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
+    TRY(forward(m, m->ids, kBlock, 1, FWD_NONE, stream));
+    TRY(finish(stream));  // the staging buffer is rewritten for the next chunk
+  }
+  for (int b = 0; b < B; ++b) {
+    kv[b] = lengths_host[b] - 1;
+    ids[b] = prompts_host[off[b + 1] - 1];
+  }
+  NDIFF_CUDA_TRY(cudaMemcpyAsync(m->kv_len, kv, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
+  NDIFF_CUDA_TRY(cudaMemcpyAsync(m->last_dev, ids, (size_t)B * 4, cudaMemcpyHostToDevice, stream));
+  TRY(finish(stream));
+  for (int b = 0; b < B; ++b) {
+    m->P[b] = lengths_host[b] - 1;
+    m->last[b] = prompts_host[off[b + 1] - 1];
+  }
   m->ready = true;
   return NDIFF_OK;
 }
 
 // Reads the committed tokens of the cycle just enqueued on the model's stream
-// and advances the host view of the session.
+// (out_tokens_host [B][32], n_out [B]) and advances the host view of each
+// session.
 static ndiff_status collect(ndiff_model* m, ndiff_mode mode, int64_t forwards, int rounds,
-                            int64_t revisions, int32_t* out_tokens_host, int* n_out,
+                            int64_t revisions, int32_t* out_tokens_host, int32_t* n_out,
                             ndiff_stats* stats) {
-  int n = 0, L = -1;
-  if (mode == NDIFF_MODE_AR) {
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, 4, cudaMemcpyDeviceToHost, m->ms));
-    TRY(finish(m->ms));
-    n = 1;
-  } else if (mode == NDIFF_MODE_DIFF) {
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, kBlock * 4, cudaMemcpyDeviceToHost, m->ms));
-    TRY(finish(m->ms));
-    n = kBlock;
-  } else {
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, 34 * 4, cudaMemcpyDeviceToHost, m->ms));
-    TRY(finish(m->ms));
-    n = m->pin[32];
-    L = m->pin[33];
+  const int B = m->B;
+  const size_t R = (size_t)B * kBlock;
+  if (mode == NDIFF_MODE_AR)
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->pred, (size_t)B * 4, cudaMemcpyDeviceToHost, m->ms));
+  else if (mode == NDIFF_MODE_DIFF)
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->draft, R * 4, cudaMemcpyDeviceToHost, m->ms));
+  else
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin, m->res, (R + 2 * B) * 4, cudaMemcpyDeviceToHost, m->ms));
+  TRY(finish(m->ms));
+  int64_t tokens = 0;
+  for (int b = 0; b < B; ++b) {
+    int n = 0, L = -1;
+    const int32_t* src = nullptr;
+    if (mode == NDIFF_MODE_AR) {
+      n = 1;
+      src = m->pin + b;
+    } else if (mode == NDIFF_MODE_DIFF) {
+      n = kBlock;
+      src = m->pin + (size_t)b * kBlock;
+    } else {
+      n = m->pin[R + b];
+      L = m->pin[R + B + b];
+      src = m->pin + (size_t)b * kBlock;
+    }
+    for (int i = 0; i < n; ++i) out_tokens_host[(size_t)b * kBlock + i] = src[i];
+    n_out[b] = n;
+    m->P[b] += n;
+    m->last[b] = src[n - 1];
+    tokens += n;
+    if (stats) {
+      if (b == 0) {
+        stats->last_accept_len = L;
+        stats->last_n_commit = n;
+      }
+      if (L >= 0 && L <= kBlock) stats->accept_hist[L] += 1;
+    }
   }
-  for (int i = 0; i < n; ++i) out_tokens_host[i] = m->pin[i];
-  *n_out = n;
-  m->P += n;
-  m->last = m->pin[n - 1];
   if (stats) {
     stats->forwards += forwards;
-    stats->tokens += n;
-    stats->last_accept_len = L;
-    stats->last_n_commit = n;
+    stats->tokens += tokens;
     stats->revisions += revisions;
     stats->last_rounds = rounds;
-    if (L >= 0 && L <= kBlock) stats->accept_hist[L] += 1;
   }
   return NDIFF_OK;
 }
 
-ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
-                                  int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
-                                  cudaStream_t stream) {
-  if (!m || !opts || !out_tokens_host || !n_out)
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: null pointer");
-  *n_out = 0;
+// One decode cycle of every sequence of the model (see ndiff_decode_step_ex).
+static ndiff_status decode_cycle(ndiff_model* m, const ndiff_decode_opts* opts,
+                                 int32_t* out_tokens_host, int32_t* n_out, ndiff_stats* stats,
+                                 cudaStream_t stream) {
   const ndiff_mode mode = opts->mode;
   if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
   if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC)
@@ -681,8 +798,10 @@ ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
                        (double)opts->tau, (double)opts->tau_revise);
   }
   const int need = mode == NDIFF_MODE_AR ? 1 : kBlock;
-  if (m->P + need > m->Lmax)
-    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)", m->P, m->Lmax);
+  for (int b = 0; b < m->B; ++b)
+    if (m->P[b] + need > m->Lmax)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache of sequence %d full (%d of %d)",
+                       b, m->P[b], m->Lmax);
   TRY(set_device(m));
   // the cycle runs on the model's stream, after the caller's earlier work
   NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
@@ -693,24 +812,25 @@ ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
     const int rounds = mode == NDIFF_MODE_AR ? 0 : opts->steps;
     return collect(m, mode, rounds + 1, rounds, 0, out_tokens_host, n_out, stats);
   }
-  // Threshold sampler: rounds until the block's mask word is empty.
+  // Threshold sampler: rounds until every sequence's mask word is empty.
   uint32_t tb, rb;
   memcpy(&tb, &opts->tau, 4);
   memcpy(&rb, &opts->tau_revise, 4);
   const float tau = opts->tau, taur = opts->tau_revise;
+  const int B = m->B;
   cudaGraphExec_t g_init = nullptr, g_round = nullptr, g_tail = nullptr;
   TRY(cached_graph(m, std::make_tuple((int)PART_INIT, 0, 0, 0u, 0u),
                    [&](cudaStream_t s) {
                      return launch_block_init(m->block_in, m->draft, m->mask, kBlock, m->last_dev,
-                                              m->mask_id, s);
+                                              m->mask_id, B, s);
                    },
                    &g_init));
   TRY(cached_graph(m, std::make_tuple((int)PART_ROUND, 0, 0, tb, rb),
                    [&](cudaStream_t s) {
                      TRY(forward(m, m->block_in, kBlock, 0, FWD_TOKENS, s));
-                     return launch_unmask_threshold(m->conf, m->pred, 1, kBlock, tau, taur, m->mask,
-                                                    m->block_in, m->draft, m->res + 40,
-                                                    m->res + 41, s);
+                     return launch_unmask_threshold(m->conf, m->pred, B, kBlock, tau, taur, m->mask,
+                                                    m->block_in, m->draft, m->nfixed, m->nrevised,
+                                                    s);
                    },
                    &g_round));
   TRY(cached_graph(m, std::make_tuple((int)PART_TAIL, (int)mode, 0, 0u, 0u),
@@ -718,20 +838,50 @@ ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
   NDIFF_CUDA_TRY(cudaGraphLaunch(g_init, m->ms));
   int rounds = 0;
   int64_t revisions = 0;
+  int32_t* hmask = m->pin;
+  int32_t* hcnt = m->pin + B;  // fixed [B], revised [B]
   for (;;) {
     NDIFF_CUDA_TRY(cudaGraphLaunch(g_round, m->ms));
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin + 40, m->mask, 4, cudaMemcpyDeviceToHost, m->ms));
-    NDIFF_CUDA_TRY(cudaMemcpyAsync(m->pin + 41, m->res + 40, 8, cudaMemcpyDeviceToHost, m->ms));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(hmask, m->mask, (size_t)B * 4, cudaMemcpyDeviceToHost, m->ms));
+    NDIFF_CUDA_TRY(cudaMemcpyAsync(hcnt, m->nfixed, (size_t)2 * B * 4, cudaMemcpyDeviceToHost, m->ms));
     TRY(finish(m->ms));
     ++rounds;
-    revisions += m->pin[42];
-    if (m->pin[40] == 0) break;
-    // every round fixes at least one of the 32 slots
-    if (rounds >= kBlock || m->pin[41] < 1)
-      return set_error(NDIFF_ERR_CUDA, "ndiff_decode_step: threshold round fixed no slot");
+    bool open = false;
+    for (int b = 0; b < B; ++b) {
+      revisions += hcnt[B + b];
+      open = open || hmask[b] != 0;
+    }
+    if (!open) break;
+    // every round fixes at least one of each unfinished block's 32 slots
+    if (rounds >= kBlock)
+      return set_error(NDIFF_ERR_CUDA, "ndiff_decode_step: 32 threshold rounds left slots masked");
   }
   NDIFF_CUDA_TRY(cudaGraphLaunch(g_tail, m->ms));
   return collect(m, mode, rounds + 1, rounds, revisions, out_tokens_host, n_out, stats);
+}
+
+ndiff_status ndiff_decode_step_ex(ndiff_model* m, const ndiff_decode_opts* opts,
+                                  int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
+                                  cudaStream_t stream) {
+  if (!m || !opts || !out_tokens_host || !n_out)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: null pointer");
+  *n_out = 0;
+  if (m->B != 1)
+    return set_error(NDIFF_ERR_UNSUPPORTED,
+                     "ndiff_decode_step: batched model; use ndiff_decode_step_batch");
+  int32_t n = 0;
+  TRY(decode_cycle(m, opts, out_tokens_host, &n, stats, stream));
+  *n_out = n;
+  return NDIFF_OK;
+}
+
+ndiff_status ndiff_decode_step_batch(ndiff_model* m, const ndiff_decode_opts* opts,
+                                     int32_t* out_tokens_host, int32_t* n_out_host,
+                                     ndiff_stats* stats, cudaStream_t stream) {
+  if (!m || !opts || !out_tokens_host || !n_out_host)
+    return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step_batch: null pointer");
+  for (int b = 0; b < m->B; ++b) n_out_host[b] = 0;
+  return decode_cycle(m, opts, out_tokens_host, n_out_host, stats, stream);
 }
 
 ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32_t* out_tokens_host,
@@ -748,11 +898,13 @@ ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32
 ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T, ndiff_mask mode,
                                  float* logits_host, cudaStream_t stream) {
   if (!m || !ids_host) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: null pointer");
+  if (m->B != 1)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_model_forward: batch-1 models only");
   if (T < 1 || T > kBlock)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: 1 <= T <= 32 (got %d)", T);
   if (mode != NDIFF_BIDIR && mode != NDIFF_CAUSAL)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: bad mask mode %d", (int)mode);
-  if (m->P + T > m->Lmax)
+  if (m->P[0] + T > m->Lmax)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_forward: KV cache full");
   for (int i = 0; i < T; ++i)
     if (ids_host[i] < 0 || ids_host[i] >= m->V)
@@ -768,8 +920,18 @@ ndiff_status ndiff_model_forward(ndiff_model* m, const int32_t* ids_host, int T,
 
 ndiff_status ndiff_model_state(const ndiff_model* m, int* kv_len, int32_t* last_token) {
   if (!m) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_state: null model");
-  if (kv_len) *kv_len = m->P;
-  if (last_token) *last_token = m->last;
+  if (kv_len) *kv_len = m->P[0];
+  if (last_token) *last_token = m->last[0];
+  return NDIFF_OK;
+}
+
+ndiff_status ndiff_model_state_batch(const ndiff_model* m, int32_t* kv_len_host,
+                                     int32_t* last_host) {
+  if (!m) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_model_state_batch: null model");
+  for (int b = 0; b < m->B; ++b) {
+    if (kv_len_host) kv_len_host[b] = m->P[b];
+    if (last_host) last_host[b] = m->last[b];
+  }
   return NDIFF_OK;
 }
 

@@ -239,28 +239,33 @@ __global__ void resid_add_f32_kernel(float* x, const float* y, int n) {
 // ---------------------------------------------------------------- decode state
 // A fresh draft block: slot 0 holds the pending token, slots 1..T-1 [MASK];
 // every slot masked, no draft yet.
+// Start of a drafted block, one CTA per sequence b: input [last_b, MASK ...],
+// no slot fixed yet, every slot masked.
 __global__ void block_init_kernel(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
                                   const int32_t* last, int32_t mask_id) {
   griddep_launch();
   griddep_wait();
-  const int i = threadIdx.x;
+  const int b = blockIdx.x, i = threadIdx.x;
   if (i < T) {
-    block_in[i] = i == 0 ? last[0] : mask_id;
-    draft[i] = -1;
+    block_in[(size_t)b * T + i] = i == 0 ? last[b] : mask_id;
+    draft[(size_t)b * T + i] = -1;
   }
-  if (i == 0) *mask = T >= 32 ? 0xffffffffu : ((1u << T) - 1u);
+  if (i == 0) mask[b] = T >= 32 ? 0xffffffffu : ((1u << T) - 1u);
 }
 
-// End of a decode cycle: the pending token becomes the last committed one
-// (tokens[n-1], n = *n_ptr or n_const) and the committed prefix grows by
-// kv_add (0 when verification has already advanced it).
-__global__ void commit_kernel(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
-                              int32_t* last, int32_t* kv_len) {
+// End of a decode cycle, one thread per sequence b: the pending token becomes
+// the last committed one (tokens[b * stride + n - 1], n = n_ptr[b] or n_const)
+// and the committed prefix grows by kv_add (0 when verification has already
+// advanced it).
+__global__ void commit_kernel(const int32_t* tokens, int stride, const int32_t* n_ptr, int n_const,
+                              int kv_add, int32_t* last, int32_t* kv_len, int B) {
   griddep_launch();
   griddep_wait();
-  const int n = n_ptr ? *n_ptr : n_const;
-  last[0] = tokens[n > 0 ? n - 1 : 0];
-  kv_len[0] += kv_add;
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = n_ptr ? n_ptr[b] : n_const;
+  last[b] = tokens[(size_t)b * stride + (n > 0 ? n - 1 : 0)];
+  kv_len[b] += kv_add;
 }
 
 __global__ void set_token_kernel(int32_t* ids, int32_t tok) {
@@ -362,16 +367,16 @@ ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t 
   return NDIFF_OK;
 }
 
-ndiff_status launch_commit(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
-                           int32_t* last, int32_t* kv_len, cudaStream_t s) {
-  NDIFF_CUDA_TRY(launch_k(mk::commit_kernel, dim3(1), dim3(1), 0, s, tokens, n_ptr, n_const, kv_add,
-                          last, kv_len));
+ndiff_status launch_commit(const int32_t* tokens, int stride, const int32_t* n_ptr, int n_const,
+                           int kv_add, int32_t* last, int32_t* kv_len, int B, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::commit_kernel, dim3((B + 127) / 128), dim3(128), 0, s, tokens, stride,
+                          n_ptr, n_const, kv_add, last, kv_len, B));
   return NDIFF_OK;
 }
 
 ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
-                               const int32_t* last, int32_t mask_id, cudaStream_t s) {
-  NDIFF_CUDA_TRY(launch_k(mk::block_init_kernel, dim3(1), dim3(32), 0, s, block_in, draft, mask, T,
+                               const int32_t* last, int32_t mask_id, int B, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::block_init_kernel, dim3(B), dim3(32), 0, s, block_in, draft, mask, T,
                           last, mask_id));
   return NDIFF_OK;
 }

@@ -34,10 +34,12 @@ ndiff_status launch_qkv_rope_f32(const float* y, int T, int Hq, int Hkv, int D, 
                                  float* vc, cudaStream_t s);
 ndiff_status launch_swiglu_f32(const float* y, int T, int ffn, float* a, cudaStream_t s);
 ndiff_status launch_resid_add_f32(float* x, const float* y, int n, cudaStream_t s);
+// B sequences: block_in / draft [B][T], mask [B], last [B].
 ndiff_status launch_block_init(int32_t* block_in, int32_t* draft, uint32_t* mask, int T,
-                               const int32_t* last, int32_t mask_id, cudaStream_t s);
-ndiff_status launch_commit(const int32_t* tokens, const int32_t* n_ptr, int n_const, int kv_add,
-                           int32_t* last, int32_t* kv_len, cudaStream_t s);
+                               const int32_t* last, int32_t mask_id, int B, cudaStream_t s);
+// B sequences: tokens [B][stride], n_ptr [B] (or n_const), last / kv_len [B].
+ndiff_status launch_commit(const int32_t* tokens, int stride, const int32_t* n_ptr, int n_const,
+                           int kv_add, int32_t* last, int32_t* kv_len, int B, cudaStream_t s);
 ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s);
 ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s);
 

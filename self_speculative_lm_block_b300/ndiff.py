@@ -77,6 +77,9 @@ _SIGS = {
     "ndiff_unmask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_unmask_threshold": (_I, [_P, _P, _I, _I, _F, _F, _P, _P, _P, _P, _P, _P]),
     "ndiff_decode_step_ex": (_I, [_P, _P, _P, _P, _P, _P]),
+    "ndiff_prefill_batch": (_I, [_P, _P, _P, _P]),
+    "ndiff_decode_step_batch": (_I, [_P, _P, _P, _P, _P, _P]),
+    "ndiff_model_state_batch": (_I, [_P, _P, _P]),
     "ndiff_verify_accept": (_I, [_P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "ndiff_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.c_uint64, ctypes.POINTER(_P)]),
     "ndiff_model_destroy": (_I, [_P]),
@@ -313,11 +316,13 @@ class Model:
     """Owner of an ndiff_model handle (thin wrapper over the C ABI)."""
 
     def __init__(self, layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, dtype="f32",
-                 max_seq=4096, seed=0, rope_base=10000.0, eps=1e-6):
+                 max_seq=4096, seed=0, rope_base=10000.0, eps=1e-6, batch=1):
         cfg = ModelConfig(layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab,
-                          NDIFF_BF16 if dtype == "bf16" else NDIFF_F32, rope_base, eps, max_seq, 1)
+                          NDIFF_BF16 if dtype == "bf16" else NDIFF_F32, rope_base, eps, max_seq,
+                          batch)
         self.cfg = cfg
         self.vocab = vocab
+        self.batch = batch
         self.handle = ndiff_model_create(cfg, seed)
         self.stats = Stats()
 
@@ -353,6 +358,42 @@ class Model:
         while len(out) < n_new:
             out.extend(self.step(mode, steps, tau, tau_revise))
         return out[:n_new]
+
+    # ---- batched sessions (batch > 1)
+    def prefill_batch(self, prompts):
+        """prompts: a list of B token lists (ragged lengths)."""
+        import numpy as np
+        lens = np.ascontiguousarray(np.array([len(p) for p in prompts], dtype=np.int32))
+        flat = np.ascontiguousarray(np.concatenate([np.asarray(p, dtype=np.int32) for p in prompts]))
+        _call("ndiff_prefill_batch", self.handle, flat.ctypes.data, lens.ctypes.data,
+              _stream(None))
+
+    def step_batch(self, mode: int, steps: int = 1, tau: float | None = None,
+                   tau_revise: float = 2.0):
+        """One decode cycle of every sequence: a list of B token lists."""
+        B = self.batch
+        buf = (ctypes.c_int32 * (32 * B))()
+        n = (ctypes.c_int32 * B)()
+        o = DecodeOpts(mode, NDIFF_SAMPLER_TOPK if tau is None else NDIFF_SAMPLER_THRESHOLD, steps,
+                       0.0 if tau is None else tau, tau_revise)
+        _call("ndiff_decode_step_batch", self.handle, ctypes.byref(o), ctypes.addressof(buf),
+              ctypes.addressof(n), ctypes.byref(self.stats), _stream(None))
+        return [list(buf[32 * b: 32 * b + n[b]]) for b in range(B)]
+
+    def generate_batch(self, mode: int, n_new: int, steps: int = 1, tau: float | None = None,
+                       tau_revise: float = 2.0):
+        out = [[] for _ in range(self.batch)]
+        while min(len(o) for o in out) < n_new:
+            for o, t in zip(out, self.step_batch(mode, steps, tau, tau_revise)):
+                o.extend(t)
+        return [o[:n_new] for o in out]
+
+    def state_batch(self):
+        B = self.batch
+        kv = (ctypes.c_int32 * B)()
+        last = (ctypes.c_int32 * B)()
+        _call("ndiff_model_state_batch", self.handle, ctypes.addressof(kv), ctypes.addressof(last))
+        return list(kv), list(last)
 
     def forward(self, ids, mode: int):
         import numpy as np

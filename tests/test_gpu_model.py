@@ -485,3 +485,109 @@ def test_bf16_full_width_two_layer_truncation(nd):
         if rows[j] != gpu_id:
             jg = int(np.nonzero(rows == gpu_id)[0][0])
             assert ref[t, j] - ref[t, jg] < 4e-2, (t, rows[j], gpu_id)
+
+
+# ---------------------------------------------------------------- batched sessions
+def _batch_model(nd, c, B, max_seq=256):
+    return nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"],
+                    c["ffn"], c["vocab"], dtype="bf16", max_seq=max_seq, seed=c["seed"], batch=B)
+
+
+def _ragged_prompts(c, lengths, seed):
+    return [list(synth.prompt(n, c["vocab"], seed + i)) for i, n in enumerate(lengths)]
+
+
+def test_batch_prefill_state(nd):
+    c = MID_BF16
+    lengths = [40, 75, 9, 1]
+    prompts = _ragged_prompts(c, lengths, 60)
+    m = _batch_model(nd, c, len(lengths))
+    m.prefill_batch(prompts)
+    kv, last = m.state_batch()
+    assert kv == [n - 1 for n in lengths]
+    assert last == [p[-1] for p in prompts]
+    m.close()
+
+
+def test_batch_ar_tracks_oracle_and_selfspec_equals_ar(nd):
+    """Three ragged sequences decoded together: each sequence's AR tokens follow
+    the oracle's AR run of that sequence alone (divergence only at a near-tie);
+    self-speculation, with top-k and threshold drafts, emits each sequence's AR
+    tokens exactly (every row's arithmetic is the same in the T = 1 and T = 32
+    forwards of the wide kernel and the batched attention)."""
+    c = MID_BF16
+    cfg = _ocfg(c, "bf16")
+    w = OM.Weights(cfg)
+    lengths = [40, 75, 9]
+    prompts = _ragged_prompts(c, lengths, 70)
+    m = _batch_model(nd, c, len(lengths), max_seq=512)
+    m.prefill_batch(prompts)
+    ar = m.generate_batch(0, 40)
+    for b, pr in enumerate(prompts):
+        ref, gaps = _oracle_ar(cfg, w, pr, 20)
+        n = _compare_tokens(ar[b][:20], ref, gaps)
+        print(f"sequence {b}: {n} of 20 AR tokens equal the oracle's")
+    for steps, tau in ((1, None), (4, None), (1, 0.002)):
+        m.prefill_batch(prompts)
+        m.stats = type(m.stats)()
+        ss = m.generate_batch(2, 40, steps, tau=tau)
+        assert ss == ar, (steps, tau)
+        assert m.stats.forwards > 0 and sum(m.stats.accept_hist) >= len(prompts)
+    m.close()
+
+
+def test_batch_diff_first_block_matches_oracle(nd):
+    """Block diffusion with one drafting forward: each sequence's first 32
+    tokens are the argmaxes of one bidirectional forward of [last, MASK x 31]
+    over its own prefix (oracle), divergence only at a near-tie; the prefixes
+    grow by 32 per cycle."""
+    c = MID_BF16
+    cfg = _ocfg(c, "bf16")
+    w = OM.Weights(cfg)
+    lengths = [33, 64, 5]
+    prompts = _ragged_prompts(c, lengths, 80)
+    m = _batch_model(nd, c, len(lengths))
+    m.prefill_batch(prompts)
+    out = m.step_batch(1, 1)
+    kv, _ = m.state_batch()
+    assert kv == [n - 1 + 32 for n in lengths]
+    for b, pr in enumerate(prompts):
+        s = OM.Session(cfg, w, max_seq=256)
+        s.prefill(pr)
+        blk = [s.last] + [cfg.mask_id] * 31
+        logits = s.forward(blk, OA.BIDIR)
+        ids = OD.logits_reduce(logits, exclude_id=cfg.mask_id)[0]
+        gaps = [_gap(logits[i], cfg.mask_id) for i in range(32)]
+        for i in range(32):
+            if out[b][i] != ids[i]:
+                assert gaps[i] < 1e-3, (b, i, out[b][i], ids[i], gaps[i])
+    m.close()
+
+
+def test_batch_of_forty_selfspec_equals_ar(nd):
+    """Forty sequences: the block forwards have 1280 token rows (five 256-row
+    chunks of the wide kernel) and the AR forwards 40; attention runs the
+    ragged batch longest first."""
+    c = MID_BF16
+    rng = np.random.default_rng(5)
+    lengths = [int(x) for x in rng.integers(1, 120, size=40)]
+    prompts = _ragged_prompts(c, lengths, 90)
+    m = _batch_model(nd, c, 40, max_seq=512)
+    m.prefill_batch(prompts)
+    ar = m.generate_batch(0, 12)
+    m.prefill_batch(prompts)
+    assert m.generate_batch(2, 12, 1) == ar
+    m.close()
+
+
+def test_single_sequence_calls_reject_a_batched_model(nd):
+    c = MID_BF16
+    mb = _batch_model(nd, c, 2, max_seq=128)
+    with pytest.raises(nd.NdiffError):
+        mb.prefill(synth.prompt(8, c["vocab"], 3))
+    mb.prefill_batch([list(synth.prompt(8, c["vocab"], 3))] * 2)
+    with pytest.raises(nd.NdiffError):
+        mb.step(0)
+    with pytest.raises(nd.NdiffError):
+        mb.forward([1, 2], 1)
+    mb.close()
