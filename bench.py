@@ -21,6 +21,12 @@ generate --model-tokens tokens through the C ABI's decode step; reported as
 tokens/s, tokens per forward and whether the self-speculation tokens equal
 the AR tokens.
 
+Unless --batch-model 0, the same 8B-shaped model also decodes a batch of 64
+sequences together (ragged prompts uniform in [512, 2048] tokens; every
+projection on the wide tensor-core kernel over 64 x 32 token rows): AR and
+self-speculation, --batch-tokens tokens per sequence, reported as tokens/s of
+the whole batch, tokens per batch forward and the forward's tensor FLOP rate.
+
 Under torchrun (N > 1) each rank runs an independent replica of the workload
 (sequences are independent: no collective on the data path); value is the
 work of all ranks divided by the slowest rank's time.
@@ -421,6 +427,48 @@ def run_lm_head(reps=20):
     return out
 
 
+def run_model_batched(rank, B, n_tokens):
+    """AR and self-speculative decoding of B ragged sequences together."""
+    import numpy as np
+    import torch
+    from self_speculative_lm_block_b300 import ndiff as nd
+    from self_speculative_lm_block_b300 import synth
+    c = synth.MODEL_8B
+    seed = c["seed"] + 1000 * rank
+    lengths = [int(x) for x in np.random.default_rng(seed).integers(512, 2049, size=B)]
+    prompts = [list(synth.prompt(n, c["vocab"], seed + i)) for i, n in enumerate(lengths)]
+    m = nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
+                 c["vocab"], dtype="bf16", max_seq=max(lengths) + 32 * n_tokens + 64, seed=seed,
+                 batch=B)
+    out = {"batch": B, "prompt_lengths": "uniform in [512, 2048]", "tokens_per_sequence": n_tokens}
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    m.prefill_batch(prompts)
+    out["prefill_s"] = time.perf_counter() - t0
+    out["prefill_tokens"] = int(sum(lengths) - B)
+    res = {}
+    for name, mode in (("ar", nd.NDIFF_MODE_AR), ("selfspec", nd.NDIFF_MODE_SELFSPEC)):
+        m.prefill_batch(prompts)
+        m.step_batch(mode, 1)                    # warm-up cycle (graph capture)
+        m.prefill_batch(prompts)
+        m.stats = nd.Stats()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        toks = m.generate_batch(mode, n_tokens, 1)
+        dt = time.perf_counter() - t0
+        st = m.stats
+        res[name] = toks
+        out[name] = {"tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+                     "tokens_per_forward": st.tokens / st.forwards,
+                     "ms_per_forward": dt * 1e3 / st.forwards, "seconds": dt}
+    # a block forward multiplies 64 x 32 token rows with every weight once
+    flops = 2.0 * B * 32 * (weight_bytes_8b(c) / 2)
+    out["selfspec"]["block_forward_tflops"] = flops / (out["selfspec"]["ms_per_forward"] * 1e-3) / 1e12
+    out["selfspec_equals_ar"] = all(a == b for a, b in zip(res["selfspec"], res["ar"]))
+    m.close()
+    return out
+
+
 def make_workload(name, rank):
     if name.startswith("attn-"):
         return AttnWorkload(name, rank)
@@ -473,6 +521,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--model-tokens", type=int, default=512,
                     help="tokens generated per mode by the 8B-shaped model (0: skip)")
+    ap.add_argument("--batch-model", type=int, default=64,
+                    help="sequences of the batched 8B-shaped decode (0: skip)")
+    ap.add_argument("--batch-tokens", type=int, default=32,
+                    help="tokens generated per sequence and mode by the batched decode")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -551,6 +603,8 @@ def main():
 
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
     lm_head = run_lm_head() if args.model_tokens > 0 else None
+    batched = run_model_batched(rank, args.batch_model, args.batch_tokens) \
+        if args.batch_model > 0 else None
     if model is not None and world > 1:
         for k in ("ar", "selfspec"):
             t = torch.tensor([model[k]["tokens_per_s"]], device="cuda", dtype=torch.float64)
@@ -578,6 +632,8 @@ def main():
             out["model_8b"] = model
         if lm_head is not None:
             out["lm_head_8b"] = lm_head
+        if batched is not None:
+            out["model_8b_batched"] = batched
         if not args.no_cpu_baseline:
             cv, desc, dt = wl.oracle_sample()
             out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": _oracle_threads(),
