@@ -74,7 +74,12 @@ typedef enum { NDIFF_BF16 = 0, NDIFF_F32 = 1 } ndiff_dtype;
 typedef enum { NDIFF_BIDIR = 0, NDIFF_CAUSAL = 1 } ndiff_mask;
 
 /* The three decode modes of one checkpoint ([FFI] "三种生成模式"). */
-typedef enum { NDIFF_MODE_AR = 0, NDIFF_MODE_DIFF = 1, NDIFF_MODE_SELFSPEC = 2 } ndiff_mode;
+typedef enum {
+    NDIFF_MODE_AR = 0,
+    NDIFF_MODE_DIFF = 1,
+    NDIFF_MODE_SELFSPEC = 2,
+    NDIFF_MODE_SELFSPEC_FUSED = 3  /* verification of a block and the draft of the next in one forward */
+} ndiff_mode;
 
 NDIFF_API const char* ndiff_last_error(void);
 NDIFF_API const char* ndiff_status_string(ndiff_status s);

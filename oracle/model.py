@@ -24,6 +24,15 @@ Readings where the pages are silent (each is listed in the design notes):
   BIDIR forward of [last, d0..d30] that writes the block's KV (counted).
 - SELFSPEC: the same drafting forwards, then one CAUSAL forward of
   [last, d0..d30]; accept the longest agreeing prefix plus the correction.
+- Fused self-speculation ("NVIDIA 发布 Nemotron-Labs Diffusion 语言模型系列"
+  (fintech-frontier-insights), 吞吐量数据: linear and quadratic
+  self-speculation; the linear one is read as one forward that verifies a
+  block and drafts the next): a forward of [last, d0..d30] (CAUSAL) followed
+  by [d31, MASK x 31] at the next 32 positions (BIDIR, over the prefix plus
+  the block under verification). The agreeing prefix plus the correction is
+  committed; when all 32 drafts were accepted, the second half's argmaxes are
+  the next block's draft, otherwise the next cycle drafts afresh (one BIDIR
+  forward). Each fused forward counts as one forward.
 - Threshold sampler (either mode): BIDIR drafting rounds until no slot is
   masked, each fixing the masked slots whose confidence reaches tau (else the
   most confident one) after revising earlier slots (oracle.decode.
@@ -166,6 +175,7 @@ class Session:
         self.accept_lens: list[int] = []
         self.revisions = 0
         self.rounds = 0
+        self.pending_draft = None
 
     def _rb(self, x: np.ndarray) -> np.ndarray:
         return round_to_bf16(x) if self.cfg.dtype == "bf16" else x
@@ -215,6 +225,7 @@ class Session:
         self.forwards = 0
         self.kv_len = len(prompt) - 1
         self.last = prompt[-1]
+        self.pending_draft = None
 
     def _argmax(self, logits):
         return decode.logits_reduce(logits, exclude_id=self.cfg.mask_id)
@@ -282,6 +293,29 @@ class Session:
         self.tokens.extend(out)
         return out
 
+    def step_selfspec_fused(self) -> list[int]:
+        P = self.kv_len
+        d = self.pending_draft
+        if d is None:
+            d = self.draft(1)
+        blk = [self.last] + [int(t) for t in d[:BLOCK - 1]]
+        a = self._argmax(self.forward(blk, attention.CAUSAL))[0]       # writes KV of [P, P+32)
+        # the draft half sees the prefix and the block under verification
+        self.kv_len = P + BLOCK
+        nxt = self._argmax(self.forward([int(d[BLOCK - 1])] + [self.cfg.mask_id] * (BLOCK - 1),
+                                        attention.BIDIR))[0]
+        self.kv_len = P
+        self.forwards -= 1                      # the two halves are one forward
+        L, commit, n, _ = decode.verify_accept(np.asarray(d)[None], a[None])
+        n0 = int(n[0])
+        self.accept_lens.append(int(L[0]))
+        self.kv_len += n0
+        out = [int(t) for t in commit[0, :n0]]
+        self.last = out[-1]
+        self.tokens.extend(out)
+        self.pending_draft = nxt if int(L[0]) == BLOCK else None
+        return out
+
     def generate(self, mode: str, n_new: int, steps: int = 1, tau=None) -> list[int]:
         """Decode until n_new tokens (extra committed tokens are cut). `tau`:
         None for the top-k draft of `steps` rounds, or (tau, tau_revise) for
@@ -293,6 +327,8 @@ class Session:
                 self.step_diff(steps, tau)
             elif mode == "selfspec":
                 self.step_selfspec(steps, tau)
+            elif mode == "selfspec-fused":
+                self.step_selfspec_fused()
             else:
                 raise ValueError(mode)
         return self.tokens[:n_new]

@@ -48,22 +48,31 @@ namespace gemm {
 
 constexpr int BM = 128;                    // weight rows per tile (MMA M)
 constexpr int BK = 64;                     // K per stage (one 128-byte swizzle atom)
-constexpr int MT = 32;                     // token rows (MMA N)
-constexpr int NST = 5;                     // pipeline stages
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
-constexpr int B_BYTES = MT * BK * 2;       // 4 KB
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NST * A_BYTES;
-constexpr int OFF_RED = OFF_B + NST * B_BYTES;   // ARGMAX: [4 warps][32 tokens] float4
-constexpr int RED_BYTES = 4 * MT * 16;
-constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-constexpr int N_BARS = 2 * NST + 4 + 1;
-constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
-constexpr int TMEM_COLS = 64;              // two 32-column accumulators
 constexpr int THREADS = 192;
 
-static_assert(OFF_B % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(2 * SMEM_BYTES <= 227 * 1024, "two CTAs per SM");
+// Shared-memory and TMEM geometry for MT token rows (the MMA's N): 32 for a
+// block or one token, 64 for the fused verify + draft forward of two blocks.
+template <int MT_>
+struct Geo {
+  static constexpr int MT = MT_;
+  static constexpr int NST = MT_ == 32 ? 5 : 4;          // pipeline stages
+  static constexpr int B_BYTES = MT_ * BK * 2;           // 4 KB / 8 KB
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + NST * A_BYTES;
+  static constexpr int OFF_RED = OFF_B + NST * B_BYTES;  // ARGMAX: [4 warps][32 tokens] float4
+  static constexpr int RED_BYTES = 4 * 32 * 16;
+  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr int N_BARS = 2 * NST + 4 + 1;
+  static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
+  static constexpr int TMEM_COLS = 2 * MT_;              // two accumulators
+  static constexpr int MIN_BLOCKS = MT_ == 32 ? 2 : 1;
+};
+
+static_assert(Geo<32>::OFF_B % 1024 == 0 && Geo<64>::OFF_B % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(2 * Geo<32>::SMEM_BYTES <= 227 * 1024, "two CTAs per SM at 32 token rows");
+static_assert(Geo<64>::SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ bool bar_and(bool pred) {
   uint32_t r;
@@ -96,6 +105,7 @@ __device__ __forceinline__ void split_range(int s, int S, int nks, int& lo, int&
 // Epilogue of one finished 128-row tile. Thread r holds y[m] for storage row
 // tile*128 + r and token rows m < T. Loads are issued before stores so that
 // the 32 token rows do not serialise on memory latency.
+template <int MT>
 __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[MT]) {
   const int n = tile * BM + r;
   switch (p.mode) {
@@ -235,8 +245,10 @@ __device__ __forceinline__ void red_halve(Red (&a)[W], Red (&o)[W / 2], int lane
 }
 
 // Thread r of the epilogue holds y[vocab n = tile*128 + r][token m] in v[m].
+// Token columns m0 .. m0+31 of the tile; the states go to red[tile * stride + m].
 __device__ __forceinline__ void epilogue_argmax(const GemmParams& p, int tile, int r, int lane,
-                                                int quarter, const float (&v)[MT], float4* sred) {
+                                                int quarter, const float* v, float4* sred,
+                                                int stride, int m0) {
   const int n = tile * BM + r;
   const bool valid = n < p.N;
   const bool allowed = valid && n != p.excl;
@@ -272,17 +284,18 @@ __device__ __forceinline__ void epilogue_argmax(const GemmParams& p, int tile, i
   red_halve<4>(a4, a2, lane, 2);
   red_halve<2>(a2, a1, lane, 1);
   // lane l now holds token column l over this warp's 32 vocabulary rows
-  sred[quarter * MT + lane] = make_float4(a1[0].m, a1[0].s, a1[0].bv, __int_as_float(a1[0].bi));
+  sred[quarter * 32 + lane] = make_float4(a1[0].m, a1[0].s, a1[0].bv, __int_as_float(a1[0].bi));
   bar_sync128();
-  if (quarter == 0 && lane < p.T) {
+  if (quarter == 0 && m0 + lane < p.T) {
     float4 f = sred[lane];
     Red acc{f.x, f.y, f.z, __float_as_int(f.w)};
 #pragma unroll
     for (int q = 1; q < 4; ++q) {
-      f = sred[q * MT + lane];
+      f = sred[q * 32 + lane];
       red_merge(acc, Red{f.x, f.y, f.z, __float_as_int(f.w)});
     }
-    __stcg(p.red + (size_t)tile * MT + lane, make_float4(acc.m, acc.s, acc.bv, __int_as_float(acc.bi)));
+    __stcg(p.red + (size_t)tile * stride + m0 + lane,
+           make_float4(acc.m, acc.s, acc.bv, __int_as_float(acc.bi)));
   }
   bar_sync128();
 }
@@ -290,10 +303,14 @@ __device__ __forceinline__ void epilogue_argmax(const GemmParams& p, int tile, i
 // ARGMAX selects the LM-head epilogue at compile time: a separate
 // instantiation keeps that epilogue's registers and code out of the
 // projections' kernel (measured 7% slower decode when both shared one body).
-template <bool ARGMAX>
-__global__ void __launch_bounds__(THREADS, 2)
+template <int MT, bool ARGMAX>
+__global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const GemmParams p) {
+  using G = Geo<MT>;
+  constexpr int NST = G::NST, B_BYTES = G::B_BYTES, OFF_A = G::OFF_A, OFF_B = G::OFF_B;
+  constexpr int OFF_RED = G::OFF_RED, OFF_BAR = G::OFF_BAR, N_BARS = G::N_BARS;
+  constexpr int TMEM_COLS = G::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -442,7 +459,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (!bar_and(ok)) break;
       tc_fence_after();
       float v[MT];
-      tmem_ld32(tl + buf * MT, v);
+#pragma unroll
+      for (int c = 0; c < MT; c += 32) tmem_ld32(tl + buf * MT + c, v + c);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
@@ -497,10 +515,12 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int m = 0; m < MT; ++m) v[m] = acc[m];
         if (tid == 0) p.counters[tile] = 0;
       }
-      if constexpr (ARGMAX)
-        epilogue_argmax(p, tile, r, lane, quarter, v, sred);
-      else
-        epilogue(p, tile, r, v);
+      if constexpr (ARGMAX) {
+#pragma unroll
+        for (int c = 0; c < MT; c += 32) epilogue_argmax(p, tile, r, lane, quarter, v + c, sred, MT, c);
+      } else {
+        epilogue<MT>(p, tile, r, v);
+      }
     }
   }
 
@@ -586,12 +606,12 @@ GemmPlan gemm_plan(int N, int K) {
   return pl;
 }
 
-size_t gemm_partials_bytes(const GemmPlan& pl) {
-  return pl.S > 1 ? (size_t)pl.items * gemm::MT * gemm::BM * sizeof(float) : 0;
+size_t gemm_partials_bytes(const GemmPlan& pl, int mt) {
+  return pl.S > 1 ? (size_t)pl.items * mt * gemm::BM * sizeof(float) : 0;
 }
 
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
-                            CUtensorMap* tmW, CUtensorMap* tmX) {
+                            CUtensorMap* tmW, CUtensorMap* tmX, int mt) {
   if (tmW) {
     const uint32_t box[2] = {gemm::BK, gemm::BM};
     ndiff_status s;
@@ -611,38 +631,45 @@ ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const voi
   if (tmX) {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
     const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {gemm::BK, gemm::MT};
+    const uint32_t box[2] = {gemm::BK, (uint32_t)mt};
     ndiff_status s = make_tmap_bf16(tmX, x, 2, dims, strides, box);
     if (s != NDIFF_OK) return s;
   }
   return NDIFF_OK;
 }
 
-ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
-                              GemmParams p, cudaStream_t stream) {
+template <int MT, bool ARGMAX>
+static ndiff_status launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                                   const GemmParams& p, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   NDIFF_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 64 && !attr_set[dev]) {
-    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel<false>,
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel<MT, ARGMAX>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        gemm::SMEM_BYTES));
-    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm::gemm_bf16_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        gemm::SMEM_BYTES));
+                                        gemm::Geo<MT>::SMEM_BYTES));
     attr_set[dev] = true;
   }
+  NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel<MT, ARGMAX>, dim3(pl.grid), dim3(gemm::THREADS),
+                          (size_t)gemm::Geo<MT>::SMEM_BYTES, stream, tmW, tmX, p));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                              GemmParams p, cudaStream_t stream, int mt) {
+  if (mt != 32 && mt != 64)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "projection kernel: 32 or 64 token rows (got %d)", mt);
+  if (p.T > mt) return set_error(NDIFF_ERR_INVALID_ARG, "projection kernel: %d rows > %d", p.T, mt);
   p.S = pl.S;
   p.nks = pl.nks;
   p.items = pl.items;
   p.status = device_status_word();
-  if (p.mode == GEMM_EPI_ARGMAX)
-    NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel<true>, dim3(pl.grid), dim3(gemm::THREADS),
-                            (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
-  else
-    NDIFF_CUDA_TRY(launch_k(gemm::gemm_bf16_kernel<false>, dim3(pl.grid), dim3(gemm::THREADS),
-                            (size_t)gemm::SMEM_BYTES, stream, tmW, tmX, p));
-  return NDIFF_OK;
+  const bool am = p.mode == GEMM_EPI_ARGMAX;
+  if (mt == 32)
+    return am ? launch_variant<32, true>(tmW, tmX, pl, p, stream)
+              : launch_variant<32, false>(tmW, tmX, pl, p, stream);
+  return am ? launch_variant<64, true>(tmW, tmX, pl, p, stream)
+            : launch_variant<64, false>(tmW, tmX, pl, p, stream);
 }
 
 }  // namespace ndiff

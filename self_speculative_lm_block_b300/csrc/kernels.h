@@ -74,12 +74,16 @@ struct GemmPlan {
   int nchunks;             // wide kernel: 256-row token chunks (1 for the skinny kernel)
 };
 
+// The weight-streaming projection for mt = 32 token rows (a block, or one
+// token) or mt = 64 (two blocks: the fused verify + draft forward). The K
+// split depends on (N, K) only, so a row's arithmetic is the same for every
+// row count and both mt.
 GemmPlan gemm_plan(int N, int K);
-size_t gemm_partials_bytes(const GemmPlan& pl);
+size_t gemm_partials_bytes(const GemmPlan& pl, int mt = 32);
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
-                            CUtensorMap* tmW, CUtensorMap* tmX);
+                            CUtensorMap* tmW, CUtensorMap* tmX, int mt = 32);
 ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
-                              GemmParams p, cudaStream_t stream);
+                              GemmParams p, cudaStream_t stream, int mt = 32);
 // Merges the per-tile partials of a GEMM_EPI_ARGMAX launch (red[tile * stride
 // + t]): argmax[t] and the softmax probability conf[t] of that id for token
 // rows t < T.

@@ -112,6 +112,11 @@ struct ndiff_model {
   int attn_split = 0;
   CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
   CUtensorMap tm_h_w, tm_oact_w, tm_a_w;  // 256-row boxes for the wide kernel (B > 1)
+  CUtensorMap tm_h64, tm_oact64, tm_a64;  // 64-row boxes: the fused verify + draft forward
+  int32_t* fin = nullptr;       // [64] fused forward input
+  int32_t* kv_len2 = nullptr;   // [1] prefix of the fused forward's draft half
+  bool have_draft = false;      // the last fused forward left a draft of the next block
+  int last_L0 = -1;             // accept length of sequence 0 in the last verification
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
   int32_t* pin = nullptr;       // pinned host staging [pin_n]
   size_t pin_n = 0;
@@ -205,12 +210,22 @@ enum { FWD_NONE = 0, FWD_TOKENS = 1, FWD_LOGITS = 2 };
 // (MMA N = 32); a batch uses the wide kernel (MMA N = 256) for every
 // projection, so a row's arithmetic is the same in AR (T = 1) and block
 // (T = 32) forwards either way.
+//
+// T = 64 (one bf16 sequence) is the fused forward of two blocks: rows 0..31
+// are a block under verification (CAUSAL at prefix kv_len) and rows 32..63 the
+// next block to draft (BIDIR at prefix kv_len + 32, read from kv_len2); the
+// projections run the 64-column kernel, whose per-row arithmetic is that of
+// the 32-column one.
 ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int out,
                      cudaStream_t s) {
   PdlScope pdl(m->bf16);
   const float scale = 1.f / sqrtf((float)m->D);
   const int B = m->B, M = B * T;
   const bool wide = B > 1;
+  const bool fused = T == 2 * kBlock;
+  if (fused && (wide || !m->bf16))
+    return set_error(NDIFF_ERR_UNSUPPORTED, "fused verify + draft forward: one bf16 sequence only");
+  const int mt = fused ? 2 * kBlock : kBlock;
   TRY(launch_embed(m->embed, m->bf16, ids, M, m->V, m->d, m->x, s));
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
@@ -221,8 +236,10 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
   gp.counters = m->gcnt;
   // one projection: W [N][K] against the activation behind tx (skinny) / txw (wide)
   auto proj = [&](const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& txw,
-                  const GemmPlan& pl, int N, int K, const GemmParams& p) -> ndiff_status {
+                  const CUtensorMap& tx64, const GemmPlan& pl, int N, int K,
+                  const GemmParams& p) -> ndiff_status {
     if (wide) return launch_gemm_wide(tw, txw, gemm_wide_plan(N, K, M), p, s);
+    if (fused) return launch_gemm_bf16(tw, tx64, pl, p, s, mt);
     return launch_gemm_bf16(tw, tx, pl, p, s);
   };
   for (int l = 0; l < m->L; ++l) {
@@ -240,28 +257,38 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.Lmax = m->Lmax;
       p.kv_len = m->kv_len;
       p.rope = m->rope;
-      TRY(proj(ly.tm_qkv, m->tm_h, m->tm_h_w, m->pl_qkv, m->NQKV, m->d, p));
-      TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, B, T, m->Hq, m->Hkv, m->Lmax, causal,
-                           scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s));
+      TRY(proj(ly.tm_qkv, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_qkv, m->NQKV, m->d, p));
+      if (fused) {
+        const size_t half = (size_t)kBlock * m->HD;  // elements of one block's q / output rows
+        __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(m->ob);
+        TRY(launch_attn_bf16(qb, ly.kc, ly.vc, m->kv_len, 1, kBlock, m->Hq, m->Hkv, m->Lmax, 1,
+                             scale, m->attn_split, ob, m->aws, m->aws_bytes, s));
+        TRY(launch_attn_bf16(qb + half, ly.kc, ly.vc, m->kv_len2, 1, kBlock, m->Hq, m->Hkv,
+                             m->Lmax, 0, scale, m->attn_split, ob + half, m->aws, m->aws_bytes, s));
+      } else {
+        TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, B, T, m->Hq, m->Hkv, m->Lmax, causal,
+                             scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s));
+      }
       p = gp;
       p.N = m->d;
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(proj(ly.tm_o, m->tm_oact, m->tm_oact_w, m->pl_o, m->d, m->HD, p));
+      TRY(proj(ly.tm_o, m->tm_oact, m->tm_oact_w, m->tm_oact64, m->pl_o, m->d, m->HD, p));
       TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, true, s));
       p = gp;
       p.N = 2 * m->ffn;
       p.mode = GEMM_EPI_SWIGLU;
       p.act = static_cast<__nv_bfloat16*>(m->ab);
       p.lda = m->ffn;
-      TRY(proj(ly.tm_gu, m->tm_h, m->tm_h_w, m->pl_gu, 2 * m->ffn, m->d, p));
+      TRY(proj(ly.tm_gu, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_gu, 2 * m->ffn, m->d, p));
       p = gp;
       p.N = m->d;
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(proj(ly.tm_d, m->tm_a, m->tm_a_w, m->pl_d, m->d, m->ffn, p));
+      TRY(proj(ly.tm_d, m->tm_a, m->tm_a_w, m->tm_a64, m->pl_d, m->d, m->ffn, p));
     } else {
       const float* h = static_cast<const float*>(m->h);
       TRY(launch_linear_f32(h, m->d, static_cast<const float*>(ly.wqkv), m->NQKV, m->d, m->y,
@@ -292,11 +319,11 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     p.mode = GEMM_EPI_ARGMAX;
     p.red = m->red;
     p.excl = m->mask_id;
-    TRY(proj(m->tm_lm, m->tm_h, m->tm_h_w, m->pl_lm, m->V, m->d, p));
-    return launch_argmax_merge(m->red, m->pl_lm.ntiles, M, wide ? M : 32, m->pred, m->conf, s);
+    TRY(proj(m->tm_lm, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_lm, m->V, m->d, p));
+    return launch_argmax_merge(m->red, m->pl_lm.ntiles, M, wide ? M : mt, m->pred, m->conf, s);
   }
-  if (wide)
-    return set_error(NDIFF_ERR_UNSUPPORTED, "model logits are available for batch 1 only");
+  if (wide || fused)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "model logits: one block of one sequence only");
   if (m->bf16) {
     GemmParams p = gp;
     p.N = m->V;
@@ -350,7 +377,23 @@ ndiff_status enqueue_cycle(ndiff_model* m, ndiff_mode mode, int steps, cudaStrea
   return enqueue_tail(m, mode, s);
 }
 
-enum { PART_CYCLE = 0, PART_INIT = 1, PART_ROUND = 2, PART_TAIL = 3 };
+// One cycle of fused self-speculation (one sequence): unless the previous
+// fused forward left a draft of this block, a drafting forward first; then one
+// forward verifies the block (rows 0..31, CAUSAL) and drafts the next
+// (rows 32..63, BIDIR, as if the whole block is accepted); the agreeing
+// prefix plus the correction is committed, and when all 32 drafts were
+// accepted the draft half becomes the next block's draft.
+ndiff_status enqueue_fused(ndiff_model* m, bool need_draft, cudaStream_t s) {
+  if (need_draft) TRY(draft_block(m, 1, s));
+  TRY(launch_fused_input(m->fin, m->block_in, m->draft, m->mask_id, m->kv_len, m->kv_len2, s));
+  TRY(forward(m, m->fin, 2 * kBlock, 1, FWD_TOKENS, s));
+  TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->acclen, m->commit, m->ncommit,
+                           m->kv_len, s));
+  TRY(launch_commit(m->commit, kBlock, m->ncommit, 0, 0, m->last_dev, m->kv_len, 1, s));
+  return launch_fused_stash(m->pred + kBlock, m->acclen, m->last_dev, m->draft, m->block_in, s);
+}
+
+enum { PART_CYCLE = 0, PART_INIT = 1, PART_ROUND = 2, PART_TAIL = 3, PART_FUSED = 4 };
 
 // The launches `fn` enqueues, as an instantiated CUDA graph captured on the
 // model's stream on first use and kept under `key`.
@@ -435,7 +478,8 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   m->last.assign(m->B, -1);
   const size_t esz = m->esz;
   const size_t d = m->d;
-  const size_t R = (size_t)m->B * kBlock;  // activation rows
+  // activation rows: B blocks, or the two blocks of a fused forward
+  const size_t R = (size_t)(m->B > 1 ? m->B * kBlock : 2 * kBlock);
   cudaStream_t s = 0;
 
   TRY(dalloc(m, &m->embed, (size_t)m->V * d * esz));
@@ -473,9 +517,10 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(dalloc_t(m, &m->draft, R * 4));
   TRY(dalloc_t(m, &m->block_in, R * 4));
   const size_t Bn = (size_t)m->B;
-  TRY(dalloc_t(m, &m->res, (R + 4 * Bn) * 4));
+  const size_t RC = Bn * kBlock;  // commit rows
+  TRY(dalloc_t(m, &m->res, (RC + 4 * Bn) * 4));
   m->commit = m->res;
-  m->ncommit = m->res + R;
+  m->ncommit = m->res + RC;
   m->acclen = m->ncommit + Bn;
   m->nfixed = m->acclen + Bn;
   m->nrevised = m->nfixed + Bn;
@@ -484,6 +529,8 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(dalloc_t(m, &m->chosen, R * 4));
   TRY(dalloc_t(m, &m->prompt, (size_t)m->Lmax * 4));
   TRY(dalloc_t(m, &m->last_dev, Bn * 4));
+  TRY(dalloc_t(m, &m->fin, 2 * kBlock * 4));
+  TRY(dalloc_t(m, &m->kv_len2, 16));
   TRY(dalloc_t(m, &m->rope, (size_t)m->Lmax * (m->D / 2) * sizeof(float2)));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, R * 4, s));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, Bn * 4, s));
@@ -500,7 +547,7 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     size_t ws = 16;
     int tiles = 1;
     for (const GemmPlan* pl : pls) {
-      const size_t b = gemm_partials_bytes(*pl);
+      const size_t b = gemm_partials_bytes(*pl, 2 * kBlock);
       if (b > ws) ws = b;
       if (pl->ntiles > tiles) tiles = pl->ntiles;
     }
@@ -514,6 +561,11 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, kBlock, nullptr, &m->tm_h));
     TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, kBlock, nullptr, &m->tm_oact));
     TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, kBlock, nullptr, &m->tm_a));
+    TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, 2 * kBlock, nullptr, &m->tm_h64, 2 * kBlock));
+    TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, 2 * kBlock, nullptr, &m->tm_oact64,
+                       2 * kBlock));
+    TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, 2 * kBlock, nullptr, &m->tm_a64,
+                       2 * kBlock));
     TRY(gemm_wide_make_xmap(m->h, (int)R, m->d, &m->tm_h_w));
     TRY(gemm_wide_make_xmap(m->ob, (int)R, m->HD, &m->tm_oact_w));
     TRY(gemm_wide_make_xmap(m->ab, (int)R, m->ffn, &m->tm_a_w));
@@ -651,6 +703,7 @@ ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host, int n, cu
       return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_prefill: token %d at %d out of range", prompt_host[i], i);
   TRY(set_device(m));
   m->ready = false;
+  m->have_draft = false;
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->kv_len, 0, sizeof(int32_t), stream));
   NDIFF_CUDA_TRY(cudaMemcpyAsync(m->prompt, prompt_host, (size_t)n * 4, cudaMemcpyHostToDevice, stream));
   for (int off = 0; off < n - 1; off += kBlock) {
@@ -688,6 +741,7 @@ ndiff_status ndiff_prefill_batch(ndiff_model* m, const int32_t* prompts_host,
                        (long long)i);
   TRY(set_device(m));
   m->ready = false;
+  m->have_draft = false;
   // All sequences advance through their prompts 32 tokens per forward. A
   // sequence whose prompt is used up runs filler tokens at positions past its
   // prefix; those cache rows are scratch (the next block overwrites them) and
@@ -757,6 +811,7 @@ static ndiff_status collect(ndiff_model* m, ndiff_mode mode, int64_t forwards, i
     }
     for (int i = 0; i < n; ++i) out_tokens_host[(size_t)b * kBlock + i] = src[i];
     n_out[b] = n;
+    if (b == 0) m->last_L0 = L;
     m->P[b] += n;
     m->last[b] = src[n - 1];
     tokens += n;
@@ -783,8 +838,28 @@ static ndiff_status decode_cycle(ndiff_model* m, const ndiff_decode_opts* opts,
                                  cudaStream_t stream) {
   const ndiff_mode mode = opts->mode;
   if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
-  if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC)
+  if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC &&
+      mode != NDIFF_MODE_SELFSPEC_FUSED)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad mode %d", (int)mode);
+  if (mode == NDIFF_MODE_SELFSPEC_FUSED) {
+    if (m->B != 1 || !m->bf16)
+      return set_error(NDIFF_ERR_UNSUPPORTED,
+                       "ndiff_decode_step: fused self-speculation needs one bf16 sequence");
+    for (int b = 0; b < m->B; ++b)
+      if (m->P[b] + 2 * kBlock > m->Lmax)
+        return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache full (%d of %d)",
+                         m->P[b], m->Lmax);
+    TRY(set_device(m));
+    NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
+    const bool need = !m->have_draft;
+    cudaGraphExec_t ge = nullptr;
+    TRY(cached_graph(m, std::make_tuple((int)PART_FUSED, (int)mode, need ? 1 : 0, 0u, 0u),
+                     [&](cudaStream_t s2) { return enqueue_fused(m, need, s2); }, &ge));
+    NDIFF_CUDA_TRY(cudaGraphLaunch(ge, m->ms));
+    TRY(collect(m, mode, need ? 2 : 1, need ? 1 : 0, 0, out_tokens_host, n_out, stats));
+    m->have_draft = m->last_L0 == kBlock;
+    return NDIFF_OK;
+  }
   const bool thr = mode != NDIFF_MODE_AR && opts->sampler == NDIFF_SAMPLER_THRESHOLD;
   if (mode != NDIFF_MODE_AR) {
     if (opts->sampler != NDIFF_SAMPLER_TOPK && opts->sampler != NDIFF_SAMPLER_THRESHOLD)

@@ -280,6 +280,33 @@ __global__ void kv_add_kernel(int32_t* kv_len, int add) {
   kv_len[0] += add;
 }
 
+// Fused verify + draft forward of one sequence. fused_input: the 64 input
+// tokens [last, d0..d30] (the block under verification, from block_in) and
+// [d31, MASK x 31] (the next block to draft), and the draft half's prefix
+// kv_len + 32. fused_stash: when the whole block was accepted, the draft
+// half's argmaxes become the next block's draft and its verification input
+// [d31, d'0..d'30].
+__global__ void fused_input_kernel(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                                   int32_t mask_id, const int32_t* kv_len, int32_t* kv_len2) {
+  griddep_launch();
+  griddep_wait();
+  const int i = threadIdx.x;
+  if (i < 32) fin[i] = block_in[i];
+  else if (i < 64) fin[i] = i == 32 ? draft[31] : mask_id;
+  if (i == 0) kv_len2[0] = kv_len[0] + 32;
+}
+
+__global__ void fused_stash_kernel(const int32_t* pred2, const int32_t* acclen, const int32_t* last,
+                                   int32_t* draft, int32_t* block_in) {
+  griddep_launch();
+  griddep_wait();
+  const int i = threadIdx.x;
+  if (acclen[0] != 32 || i >= 32) return;
+  draft[i] = pred2[i];
+  if (i == 0) block_in[0] = last[0];
+  if (i <= 30) block_in[i + 1] = pred2[i];
+}
+
 }  // namespace mk
 
 // ---------------------------------------------------------------- launchers
@@ -388,6 +415,21 @@ ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s) {
 
 ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s) {
   NDIFF_CUDA_TRY(launch_k(mk::kv_add_kernel, dim3(1), dim3(1), 0, s, kv_len, add));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_fused_input(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                                int32_t mask_id, const int32_t* kv_len, int32_t* kv_len2,
+                                cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::fused_input_kernel, dim3(1), dim3(64), 0, s, fin, block_in, draft,
+                          mask_id, kv_len, kv_len2));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_fused_stash(const int32_t* pred2, const int32_t* acclen, const int32_t* last,
+                                int32_t* draft, int32_t* block_in, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::fused_stash_kernel, dim3(1), dim3(32), 0, s, pred2, acclen, last,
+                          draft, block_in));
   return NDIFF_OK;
 }
 

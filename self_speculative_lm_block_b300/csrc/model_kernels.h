@@ -42,5 +42,13 @@ ndiff_status launch_commit(const int32_t* tokens, int stride, const int32_t* n_p
                            int kv_add, int32_t* last, int32_t* kv_len, int B, cudaStream_t s);
 ndiff_status launch_set_token(int32_t* ids, int32_t tok, cudaStream_t s);
 ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s);
+// Fused verify + draft forward (one sequence): its 64 input tokens and the
+// draft half's prefix; after verification, the next draft when all 32 drafts
+// were accepted.
+ndiff_status launch_fused_input(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                                int32_t mask_id, const int32_t* kv_len, int32_t* kv_len2,
+                                cudaStream_t s);
+ndiff_status launch_fused_stash(const int32_t* pred2, const int32_t* acclen, const int32_t* last,
+                                int32_t* draft, int32_t* block_in, cudaStream_t s);
 
 }  // namespace ndiff

@@ -19,7 +19,7 @@ NDIFF_OK, NDIFF_ERR_INVALID_ARG, NDIFF_ERR_UNSUPPORTED = 0, 1, 2
 NDIFF_ERR_CUDA, NDIFF_ERR_OOM, NDIFF_ERR_WORKSPACE, NDIFF_ERR_TIMEOUT = 3, 4, 5, 6
 NDIFF_BF16, NDIFF_F32 = 0, 1
 NDIFF_BIDIR, NDIFF_CAUSAL = 0, 1
-NDIFF_MODE_AR, NDIFF_MODE_DIFF, NDIFF_MODE_SELFSPEC = 0, 1, 2
+NDIFF_MODE_AR, NDIFF_MODE_DIFF, NDIFF_MODE_SELFSPEC, NDIFF_MODE_SELFSPEC_FUSED = 0, 1, 2, 3
 NDIFF_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 

@@ -591,3 +591,69 @@ def test_single_sequence_calls_reject_a_batched_model(nd):
     with pytest.raises(nd.NdiffError):
         mb.forward([1, 2], 1)
     mb.close()
+
+
+# ---------------------------------------------------------------- fused self-speculation
+SMALL_BF16 = dict(layers=2, d_model=128, n_heads=1, n_kv_heads=1, head_dim=128, ffn=256, vocab=16,
+                  seed=21)
+
+
+def _small_model(nd, vocab, seed=21, max_seq=600):
+    c = dict(SMALL_BF16, vocab=vocab, seed=seed)
+    return c, _gpu_model(nd, c, "bf16", max_seq=max_seq)
+
+
+def test_fused_selfspec_equals_ar_and_reuses_drafts(nd):
+    """Fused self-speculation emits the AR tokens exactly (the verify rows of
+    the 64-row forward are computed as in a 32-row or one-token forward); with
+    a 16-id vocabulary some blocks are accepted whole, and the next cycle then
+    runs no drafting forward. The oracle's fused run of the same model and its
+    AR tokens agree with the GPU's."""
+    c, m = _small_model(nd, 16)
+    cfg = _ocfg(c, "bf16")
+    pr = [int(x) for x in synth.prompt(24, c["vocab"], 5)]
+    m.prefill(pr)
+    ar = m.generate(0, 160)
+    m.prefill(pr)
+    m.stats = type(m.stats)()
+    fu = m.generate(3, 160)
+    assert fu == ar
+    hist = list(m.stats.accept_hist)
+    cycles = sum(hist)
+    assert hist[32] >= 1 and cycles > hist[32]
+    # a cycle that follows a whole block runs no drafting forward
+    skipped = hist[32] - (1 if m.stats.last_accept_len == 32 else 0)
+    assert m.stats.forwards == 2 * cycles - skipped
+    ref, gaps = _oracle_ar(cfg, OM.Weights(cfg), pr, 160)
+    n = _compare_tokens(ar, ref, gaps)
+    s = OM.Session(cfg, OM.Weights(cfg), max_seq=600)
+    s.prefill(pr)
+    of = s.generate("selfspec-fused", 160)
+    assert of[:n] == ar[:n]
+    print(f"GPU fused: {m.stats.forwards} forwards, {cycles} cycles, {hist[32]} whole blocks; "
+          f"oracle: {s.forwards} forwards; AR equal to the oracle for {n} of 160 tokens")
+    m.close()
+
+
+def test_fused_full_acceptance_one_forward_per_block(nd):
+    """Two ids: every draft is accepted, so after the first drafting forward
+    each fused forward commits 32 tokens."""
+    c, m = _small_model(nd, 2)
+    m.prefill([0] * 20)
+    m.stats = type(m.stats)()
+    toks = m.generate(3, 96)
+    assert toks == [0] * 96
+    assert m.stats.forwards == 1 + 3 and m.stats.accept_hist[32] == 3
+    assert m.state()[0] == 19 + 96
+    m.close()
+
+
+def test_fused_selfspec_equals_ar_8b_like_width(nd):
+    c = MID_BF16
+    pr = synth.prompt(40, c["vocab"], 17)
+    m = _gpu_model(nd, c, "bf16", max_seq=256)
+    m.prefill(pr)
+    ar = m.generate(0, 48)
+    m.prefill(pr)
+    assert m.generate(3, 48) == ar
+    m.close()

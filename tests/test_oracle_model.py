@@ -156,3 +156,58 @@ def test_threshold_diff_rounds_and_revisions():
     assert len(toks) == 64 and all(0 <= t < cfg.vocab - 1 for t in toks)
     assert 2 * 2 <= s.forwards <= 2 * 33
     assert s.revisions > 0
+
+
+# ---------------------------------------------------------------- fused self-speculation
+def _cfg_vocab(V, seed=7):
+    t = synth.TINY
+    return model.Config(layers=t["layers"], d_model=t["d_model"], n_heads=t["n_heads"],
+                        n_kv_heads=t["n_kv_heads"], head_dim=t["head_dim"], ffn=t["ffn"],
+                        vocab=V, dtype="f32", seed=seed)
+
+
+def test_fused_selfspec_equals_ar():
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, w, max_seq=260); s.prefill(pr)
+    ar = s.generate("ar", 64)
+    s2 = model.Session(cfg, w, max_seq=260); s2.prefill(pr)
+    assert s2.generate("selfspec-fused", 64) == ar
+
+
+def test_fused_full_acceptance_takes_one_forward_per_block():
+    """With two ids ([MASK] and one token) every draft is accepted: one drafting
+    forward, then one fused forward per 32 tokens."""
+    cfg = _cfg_vocab(2)
+    w = model.Weights(cfg)
+    s = model.Session(cfg, w, max_seq=260); s.prefill([0] * 20)
+    toks = s.generate("selfspec-fused", 96)
+    assert toks == [0] * 96
+    assert s.forwards == 1 + 3 and s.accept_lens == [32, 32, 32]
+    assert s.kv_len == 19 + 96
+
+
+def test_fused_next_draft_is_the_draft_of_the_new_state():
+    """After a fully accepted block, the draft the fused forward leaves is the
+    one a fresh drafting forward computes from the committed tokens (same
+    positions and prefix: the shifted block layout holds across the two halves);
+    with eight ids full acceptances happen and mix with partial ones, and the
+    tokens stay the AR tokens."""
+    cfg = _cfg_vocab(8, seed=11)
+    w = model.Weights(cfg)
+    pr = [int(x) for x in synth.prompt(24, cfg.vocab, 5)]
+    s = model.Session(cfg, w, max_seq=600); s.prefill(pr)
+    ar = s.generate("ar", 160)
+    f = model.Session(cfg, w, max_seq=600); f.prefill(pr)
+    checked = 0
+    while len(f.tokens) < 160:
+        f.step_selfspec_fused()
+        if f.pending_draft is not None and checked < 3:
+            fresh = model.Session(cfg, w, max_seq=600)
+            fresh.prefill(pr + f.tokens)
+            assert np.array_equal(fresh.draft(1), f.pending_draft)
+            checked += 1
+    assert f.tokens[:160] == ar
+    assert 32 in f.accept_lens and min(f.accept_lens) < 32
+    assert checked >= 1
