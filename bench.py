@@ -15,11 +15,13 @@ Workloads (seeded synthetic inputs, shapes of the 8B-like configurations):
 
 Every run also decodes with the 8B-shaped random-init model (36 layers,
 d_model 4096, 32/8 heads x 128, SwiGLU 12288, vocab 151936, bf16 weights; batch
-1, 1024-token prompt) unless --model-tokens 0: AR and temperature-0
-self-speculation (32-token diffusion drafts, one drafting forward) each
+1, 1024-token prompt) unless --model-tokens 0: AR, temperature-0
+self-speculation (32-token diffusion drafts, one drafting forward) and fused
+self-speculation (one forward verifies a block and drafts the next) each
 generate --model-tokens tokens through the C ABI's decode step; reported as
 tokens/s, tokens per forward and whether the self-speculation tokens equal
-the AR tokens.
+the AR tokens. A labelled forced-acceptance run (the same body with a two-id
+vocabulary, so every draft is accepted) shows the machinery's L = 32 ceiling.
 
 Unless --batch-model 0, the same 8B-shaped model also decodes a batch of 64
 sequences together (ragged prompts uniform in [512, 2048] tokens; every
@@ -329,7 +331,8 @@ def run_model(rank, n_tokens, steps=1):
     out = {"model": "8B-shaped random init (36L, d4096, 32/8x128, ffn 12288, V151936, bf16)",
            "prompt": c["prompt"], "tokens": n_tokens}
     res = {}
-    for name, mode in (("ar", nd.NDIFF_MODE_AR), ("selfspec", nd.NDIFF_MODE_SELFSPEC)):
+    for name, mode in (("ar", nd.NDIFF_MODE_AR), ("selfspec", nd.NDIFF_MODE_SELFSPEC),
+                       ("selfspec_fused", nd.NDIFF_MODE_SELFSPEC_FUSED)):
         m.prefill(prompt)
         m.step(mode, steps)                      # warm-up cycle (graph capture)
         m.prefill(prompt)
@@ -343,7 +346,7 @@ def run_model(rank, n_tokens, steps=1):
         out[name] = {"tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
                      "tokens_per_forward": st.tokens / st.forwards,
                      "ms_per_forward": dt * 1e3 / st.forwards, "seconds": dt}
-        if name == "selfspec":
+        if name.startswith("selfspec"):
             hist = [int(x) for x in st.accept_hist]
             out[name]["accept_len_hist"] = {str(i): v for i, v in enumerate(hist) if v}
             out[name]["draft_forwards_per_block"] = steps
@@ -366,6 +369,7 @@ def run_model(rank, n_tokens, steps=1):
     out["weight_bytes_per_forward"] = wb
     out["ar"]["weight_stream_gbs"] = wb / (out["ar"]["ms_per_forward"] * 1e-3) / 1e9
     out["selfspec_equals_ar"] = res["selfspec"] == res["ar"]
+    out["selfspec_fused_equals_ar"] = res["selfspec_fused"] == res["ar"]
     out["note"] = ("random-init weights: tokens per forward is not the trained model's; "
                    "decode steps are host-synchronous calls (host buffers in and out)")
     m.close()
@@ -424,6 +428,33 @@ def run_lm_head(reps=20):
         tf, tu = time_graph(fused), time_graph(unfused)
         out[f"tokens_{M}"] = {"fused_us": tf, "unfused_us": tu,
                               "fused_weight_gbs": V * d * 2 / (tf * 1e-6) / 1e9}
+    return out
+
+
+def run_forced_accept(rank, n_tokens=256):
+    """The fused self-speculation machinery with every draft accepted: the
+    8B-shaped body with a two-id vocabulary ([MASK] and one token), so each
+    fused forward commits 32 tokens. Labelled as the L = 32 ceiling of the
+    machinery; the LM head is 2 ids instead of 151936."""
+    import torch
+    from self_speculative_lm_block_b300 import ndiff as nd
+    from self_speculative_lm_block_b300 import synth
+    c = synth.MODEL_8B
+    m = nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
+                 2, dtype="bf16", max_seq=1024 + n_tokens + 96, seed=c["seed"] + 1000 * rank)
+    m.prefill([0] * 1024)
+    m.step(nd.NDIFF_MODE_SELFSPEC_FUSED)
+    m.prefill([0] * 1024)
+    m.stats = nd.Stats()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    m.generate(nd.NDIFF_MODE_SELFSPEC_FUSED, n_tokens)
+    dt = time.perf_counter() - t0
+    st = m.stats
+    out = {"label": "L = 32 machinery ceiling (vocabulary of 2: every draft accepted)",
+           "tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+           "tokens_per_forward": st.tokens / st.forwards, "ms_per_forward": dt * 1e3 / st.forwards}
+    m.close()
     return out
 
 
@@ -603,6 +634,7 @@ def main():
 
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
     lm_head = run_lm_head() if args.model_tokens > 0 else None
+    forced = run_forced_accept(rank) if args.model_tokens > 0 else None
     batched = run_model_batched(rank, args.batch_model, args.batch_tokens) \
         if args.batch_model > 0 else None
     if model is not None and world > 1:
@@ -632,6 +664,8 @@ def main():
             out["model_8b"] = model
         if lm_head is not None:
             out["lm_head_8b"] = lm_head
+        if forced is not None:
+            out["model_8b"]["forced_accept_fused"] = forced
         if batched is not None:
             out["model_8b_batched"] = batched
         if not args.no_cpu_baseline:
