@@ -488,6 +488,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  // Each warp reconverges (warps 0 and 1 ran their roles on one lane) before
+  // the CTA barrier that orders every TMEM access before the release.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

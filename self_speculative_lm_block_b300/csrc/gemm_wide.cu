@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  __syncwarp();  // warps 0 and 1 reconverge before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
