@@ -56,7 +56,7 @@ constexpr int THREADS = 192;
 template <int MT_>
 struct Geo {
   static constexpr int MT = MT_;
-  static constexpr int NST = MT_ == 32 ? 5 : 4;          // pipeline stages
+  static constexpr int NST = MT_ == 32 ? 5 : 7;          // pipeline stages
   static constexpr int B_BYTES = MT_ * BK * 2;           // 4 KB / 8 KB
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NST * A_BYTES;
