@@ -529,6 +529,24 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def reduce_over_ranks(x: float, op: str, world: int, device) -> float:
+    """A per-rank number combined over the replicas: "max" (the slowest
+    rank's time, which bounds the job) or "sum" (all ranks' throughput)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(
+        t, op=torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every replica processes step_bytes per step, the job
+    takes the slowest replica's time."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
 def capture(torch, fn, n):
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -607,13 +625,9 @@ def main():
         a1.record()
         barrier()
     steps_done = reps * per_graph
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_over_ranks(e0.elapsed_time(e1), "max", world, "cuda")
     ms_step = ms_total / steps_done
-    value = wl.step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = job_gbs(wl.step_bytes, world, ms_step)
     attn_ms = a0.elapsed_time(a1) / steps_done
     attn_gbs = wl.attn_bytes / (attn_ms * 1e-3) / 1e9
 
@@ -629,8 +643,8 @@ def main():
         h2d, d2h = wl.e2e_step(pinned)
     f1.record()
     barrier()
-    e2e_ms = f0.elapsed_time(f1) / n_e2e
-    e2e_val = wl.step_bytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = reduce_over_ranks(f0.elapsed_time(f1), "max", world, "cuda") / n_e2e
+    e2e_val = job_gbs(wl.step_bytes, world, e2e_ms)
 
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
     lm_head = run_lm_head() if args.model_tokens > 0 else None
@@ -638,10 +652,9 @@ def main():
     batched = run_model_batched(rank, args.batch_model, args.batch_tokens) \
         if args.batch_model > 0 else None
     if model is not None and world > 1:
-        for k in ("ar", "selfspec"):
-            t = torch.tensor([model[k]["tokens_per_s"]], device="cuda", dtype=torch.float64)
-            torch.distributed.all_reduce(t)
-            model[k]["tokens_per_s_all_ranks"] = float(t.item())
+        for k in ("ar", "selfspec", "selfspec_fused"):
+            model[k]["tokens_per_s_all_ranks"] = reduce_over_ranks(model[k]["tokens_per_s"], "sum",
+                                                                   world, "cuda")
 
     hbm, _, _, src = _peaks()
     if rank == 0:
