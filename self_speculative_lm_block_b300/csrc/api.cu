@@ -338,7 +338,7 @@ ndiff_status ndiff_gemm_bf16(const void* x, const void* w, int M, int N, int K, 
   if (M > 32) {
     ndiff_status s = gemm_make_maps(w, N, K, false, nullptr, 0, &tw, nullptr);
     if (s != NDIFF_OK) return s;
-    s = gemm_wide_make_xmap(x, M, K, &tx);
+    s = gemm_wide_make_xmap(x, M, K, &tx, gemm_wide_box_rows(M));
     if (s != NDIFF_OK) return s;
     return launch_gemm_wide(tw, tx, gemm_wide_plan(N, K, M), p, stream);
   }
@@ -391,7 +391,7 @@ ndiff_status ndiff_lm_head_argmax(const void* x, const void* w, int M, int N, in
     const GemmPlan pl = gemm_wide_plan(N, K, M);
     ndiff_status s = gemm_make_maps(w, N, K, false, nullptr, 0, &tw, nullptr);
     if (s != NDIFF_OK) return s;
-    s = gemm_wide_make_xmap(x, M, K, &tx);
+    s = gemm_wide_make_xmap(x, M, K, &tx, gemm_wide_box_rows(M));
     if (s != NDIFF_OK) return s;
     p.red = static_cast<float4*>(ws);
     s = launch_gemm_wide(tw, tx, pl, p, stream);

@@ -39,23 +39,34 @@ namespace gemm_wide {
 
 constexpr int BM = 128;                     // weight rows per tile (MMA M)
 constexpr int BK = 64;                      // K per stage (one 128-byte swizzle atom)
-constexpr int MT = 256;                     // token rows per item (MMA N)
-constexpr int NST = 4;                      // pipeline stages
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = MT * BK * 2;        // 32 KB
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NST * A_BYTES;
-constexpr int OFF_RED = OFF_B + NST * B_BYTES;   // ARGMAX: [4 warps][32 tokens] float4
-constexpr int RED_BYTES = 4 * 32 * 16;
-constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-constexpr int N_BARS = 2 * NST + 4 + 1;
-constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
-constexpr int TMEM_COLS = 2 * MT;           // two 256-column accumulators
 constexpr int THREADS = 192;
 constexpr float L2E = 1.4426950408889634f;
 
-static_assert(OFF_B % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+// Geometry for MT token rows per item (the MMA's N): 256 for block forwards
+// of a batch (4 stages of 48 KB), 64 for the AR forward of up to 64
+// sequences (8 stages of 24 KB: twice the weight bytes in flight per SM, for
+// the short projections that have fewer weight tiles than SMs). Both run the
+// same K loop with no split, so a row's arithmetic is the same in either.
+template <int MT_>
+struct Geo {
+  static constexpr int MT = MT_;
+  static constexpr int NST = MT_ == 256 ? 4 : 8;
+  static constexpr int B_BYTES = MT_ * BK * 2;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + NST * A_BYTES;
+  static constexpr int OFF_RED = OFF_B + NST * B_BYTES;  // ARGMAX: [4 warps][32 tokens] float4
+  static constexpr int RED_BYTES = 4 * 32 * 16;
+  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr int N_BARS = 2 * NST + 4 + 1;
+  static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
+  static constexpr int TMEM_COLS = 2 * MT_;             // two accumulators
+};
+
+static_assert(Geo<256>::OFF_B % 1024 == 0 && Geo<64>::OFF_B % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(Geo<256>::SMEM_BYTES <= 227 * 1024 && Geo<64>::SMEM_BYTES <= 227 * 1024,
+              "shared memory per CTA");
 
 __device__ __forceinline__ void bar_sync128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -259,10 +270,14 @@ __device__ __forceinline__ void epilogue_argmax(const GemmParams& p, int tile, i
 }
 
 // ---------------------------------------------------------------- kernel
-template <bool ARGMAX>
+template <int MT, bool ARGMAX>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const GemmParams p, int nchunks) {
+  using G = Geo<MT>;
+  constexpr int NST = G::NST, B_BYTES = G::B_BYTES, OFF_A = G::OFF_A, OFF_B = G::OFF_B;
+  constexpr int OFF_RED = G::OFF_RED, OFF_BAR = G::OFF_BAR, N_BARS = G::N_BARS;
+  constexpr int TMEM_COLS = G::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -413,53 +428,60 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace gemm_wide
 
+static int wide_mt(int M) { return gemm_wide_box_rows(M); }
+
 GemmPlan gemm_wide_plan(int N, int K, int M) {
   GemmPlan pl;
+  const int mt = wide_mt(M);
   pl.ntiles = (N + gemm_wide::BM - 1) / gemm_wide::BM;
   pl.nks = K / gemm_wide::BK;
   pl.S = 1;
-  pl.nchunks = (M + gemm_wide::MT - 1) / gemm_wide::MT;
+  pl.nchunks = (M + mt - 1) / mt;
   pl.items = pl.ntiles * pl.nchunks;
   const int sms = num_sms();
   pl.grid = pl.items < sms ? pl.items : sms;
   return pl;
 }
 
-ndiff_status gemm_wide_make_xmap(const void* x, int M, int K, CUtensorMap* tmX) {
+ndiff_status gemm_wide_make_xmap(const void* x, int M, int K, CUtensorMap* tmX, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
   const uint64_t strides[1] = {(uint64_t)K * 2};
-  const uint32_t box[2] = {gemm_wide::BK, gemm_wide::MT};
+  const uint32_t box[2] = {gemm_wide::BK, (uint32_t)box_rows};
   return make_tmap_bf16(tmX, x, 2, dims, strides, box);
 }
 
-ndiff_status launch_gemm_wide(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
-                              GemmParams p, cudaStream_t stream) {
+template <int MT, bool ARGMAX>
+static ndiff_status launch_wide_variant(const CUtensorMap& tmW, const CUtensorMap& tmX,
+                                        const GemmPlan& pl, const GemmParams& p,
+                                        cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   NDIFF_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 64 && !attr_set[dev]) {
-    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm_wide::gemm_wide_kernel<false>,
+    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm_wide::gemm_wide_kernel<MT, ARGMAX>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        gemm_wide::SMEM_BYTES));
-    NDIFF_CUDA_TRY(cudaFuncSetAttribute(gemm_wide::gemm_wide_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        gemm_wide::SMEM_BYTES));
+                                        gemm_wide::Geo<MT>::SMEM_BYTES));
     attr_set[dev] = true;
   }
+  NDIFF_CUDA_TRY(launch_k(gemm_wide::gemm_wide_kernel<MT, ARGMAX>, dim3(pl.grid),
+                          dim3(gemm_wide::THREADS), (size_t)gemm_wide::Geo<MT>::SMEM_BYTES, stream,
+                          tmW, tmX, p, pl.nchunks));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_gemm_wide(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
+                              GemmParams p, cudaStream_t stream) {
   if (p.T <= 0) return NDIFF_OK;
   p.S = 1;
   p.nks = pl.nks;
   p.items = pl.items;
   p.status = device_status_word();
-  if (p.mode == GEMM_EPI_ARGMAX)
-    NDIFF_CUDA_TRY(launch_k(gemm_wide::gemm_wide_kernel<true>, dim3(pl.grid),
-                            dim3(gemm_wide::THREADS), (size_t)gemm_wide::SMEM_BYTES, stream, tmW,
-                            tmX, p, pl.nchunks));
-  else
-    NDIFF_CUDA_TRY(launch_k(gemm_wide::gemm_wide_kernel<false>, dim3(pl.grid),
-                            dim3(gemm_wide::THREADS), (size_t)gemm_wide::SMEM_BYTES, stream, tmW,
-                            tmX, p, pl.nchunks));
-  return NDIFF_OK;
+  const bool am = p.mode == GEMM_EPI_ARGMAX;
+  if (wide_mt(p.T) == 64)
+    return am ? launch_wide_variant<64, true>(tmW, tmX, pl, p, stream)
+              : launch_wide_variant<64, false>(tmW, tmX, pl, p, stream);
+  return am ? launch_wide_variant<256, true>(tmW, tmX, pl, p, stream)
+            : launch_wide_variant<256, false>(tmW, tmX, pl, p, stream);
 }
 
 }  // namespace ndiff

@@ -91,10 +91,13 @@ ndiff_status launch_argmax_merge(const float4* red, int ntiles, int T, int strid
                                  float* conf, cudaStream_t stream);
 
 // The projection for any number of token rows M (several sequences): items of
-// (128-row weight tile, 256-row token chunk), tcgen05 M128 N256, no K split.
-// The X map has 256-row boxes (gemm_wide_make_xmap); W maps as gemm_make_maps.
+// (128-row weight tile, token chunk), no K split; chunks of 64 rows (tcgen05
+// M128 N64) when M <= 64, else of 256 rows (M128 N256). The X map's box must
+// have that many rows (gemm_wide_make_xmap with box_rows = 64 or 256); W maps
+// as gemm_make_maps.
 GemmPlan gemm_wide_plan(int N, int K, int M);
-ndiff_status gemm_wide_make_xmap(const void* x, int M, int K, CUtensorMap* tmX);
+inline int gemm_wide_box_rows(int M) { return M <= 64 ? 64 : 256; }
+ndiff_status gemm_wide_make_xmap(const void* x, int M, int K, CUtensorMap* tmX, int box_rows = 256);
 ndiff_status launch_gemm_wide(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
                               GemmParams p, cudaStream_t stream);
 

@@ -112,6 +112,7 @@ struct ndiff_model {
   int attn_split = 0;
   CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
   CUtensorMap tm_h_w, tm_oact_w, tm_a_w;  // 256-row boxes for the wide kernel (B > 1)
+  CUtensorMap tm_h_w64, tm_oact_w64, tm_a_w64;  // 64-row boxes: its AR forwards (B <= 64 rows)
   CUtensorMap tm_h64, tm_oact64, tm_a64;  // 64-row boxes: the fused verify + draft forward
   int32_t* fin = nullptr;       // [64] fused forward input
   int32_t* kv_len2 = nullptr;   // [1] prefix of the fused forward's draft half
@@ -235,12 +236,21 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
   gp.ws = m->gws;
   gp.counters = m->gcnt;
   // one projection: W [N][K] against the activation behind tx (skinny) / txw (wide)
-  auto proj = [&](const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& txw,
-                  const CUtensorMap& tx64, const GemmPlan& pl, int N, int K,
+  // the activation maps of one projection input: 32-row boxes (one block),
+  // 64-row boxes (fused forward), and the wide kernel's 256- and 64-row boxes
+  struct XMaps {
+    const CUtensorMap &x32, &x64, &w256, &w64;
+  };
+  const XMaps xh{m->tm_h, m->tm_h64, m->tm_h_w, m->tm_h_w64};
+  const XMaps xo{m->tm_oact, m->tm_oact64, m->tm_oact_w, m->tm_oact_w64};
+  const XMaps xa{m->tm_a, m->tm_a64, m->tm_a_w, m->tm_a_w64};
+  auto proj = [&](const CUtensorMap& tw, const XMaps& xm, const GemmPlan& pl, int N, int K,
                   const GemmParams& p) -> ndiff_status {
-    if (wide) return launch_gemm_wide(tw, txw, gemm_wide_plan(N, K, M), p, s);
-    if (fused) return launch_gemm_bf16(tw, tx64, pl, p, s, mt);
-    return launch_gemm_bf16(tw, tx, pl, p, s);
+    if (wide)
+      return launch_gemm_wide(tw, gemm_wide_box_rows(M) == 64 ? xm.w64 : xm.w256,
+                              gemm_wide_plan(N, K, M), p, s);
+    if (fused) return launch_gemm_bf16(tw, xm.x64, pl, p, s, mt);
+    return launch_gemm_bf16(tw, xm.x32, pl, p, s);
   };
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
@@ -257,7 +267,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.Lmax = m->Lmax;
       p.kv_len = m->kv_len;
       p.rope = m->rope;
-      TRY(proj(ly.tm_qkv, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_qkv, m->NQKV, m->d, p));
+      TRY(proj(ly.tm_qkv, xh, m->pl_qkv, m->NQKV, m->d, p));
       if (fused) {
         const size_t half = (size_t)kBlock * m->HD;  // elements of one block's q / output rows
         __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
@@ -275,20 +285,20 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(proj(ly.tm_o, m->tm_oact, m->tm_oact_w, m->tm_oact64, m->pl_o, m->d, m->HD, p));
+      TRY(proj(ly.tm_o, xo, m->pl_o, m->d, m->HD, p));
       TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, true, s));
       p = gp;
       p.N = 2 * m->ffn;
       p.mode = GEMM_EPI_SWIGLU;
       p.act = static_cast<__nv_bfloat16*>(m->ab);
       p.lda = m->ffn;
-      TRY(proj(ly.tm_gu, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_gu, 2 * m->ffn, m->d, p));
+      TRY(proj(ly.tm_gu, xh, m->pl_gu, 2 * m->ffn, m->d, p));
       p = gp;
       p.N = m->d;
       p.mode = GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
-      TRY(proj(ly.tm_d, m->tm_a, m->tm_a_w, m->tm_a64, m->pl_d, m->d, m->ffn, p));
+      TRY(proj(ly.tm_d, xa, m->pl_d, m->d, m->ffn, p));
     } else {
       const float* h = static_cast<const float*>(m->h);
       TRY(launch_linear_f32(h, m->d, static_cast<const float*>(ly.wqkv), m->NQKV, m->d, m->y,
@@ -319,7 +329,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     p.mode = GEMM_EPI_ARGMAX;
     p.red = m->red;
     p.excl = m->mask_id;
-    TRY(proj(m->tm_lm, m->tm_h, m->tm_h_w, m->tm_h64, m->pl_lm, m->V, m->d, p));
+    TRY(proj(m->tm_lm, xh, m->pl_lm, m->V, m->d, p));
     return launch_argmax_merge(m->red, m->pl_lm.ntiles, M, wide ? M : mt, m->pred, m->conf, s);
   }
   if (wide || fused)
@@ -569,6 +579,9 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     TRY(gemm_wide_make_xmap(m->h, (int)R, m->d, &m->tm_h_w));
     TRY(gemm_wide_make_xmap(m->ob, (int)R, m->HD, &m->tm_oact_w));
     TRY(gemm_wide_make_xmap(m->ab, (int)R, m->ffn, &m->tm_a_w));
+    TRY(gemm_wide_make_xmap(m->h, (int)R, m->d, &m->tm_h_w64, 64));
+    TRY(gemm_wide_make_xmap(m->ob, (int)R, m->HD, &m->tm_oact_w64, 64));
+    TRY(gemm_wide_make_xmap(m->ab, (int)R, m->ffn, &m->tm_a_w64, 64));
     TRY(gemm_make_maps(m->lm, m->V, m->d, true, nullptr, 0, &m->tm_lm, nullptr));
     for (Layer& ly : m->layers) {
       TRY(gemm_make_maps(ly.wqkv, m->NQKV, m->d, true, nullptr, 0, &ly.tm_qkv, nullptr));
