@@ -66,6 +66,32 @@ def test_host_side_validation_without_gpu(nd):
     nd.ndiff_logits_reduce(nd.NDIFF_F32, None, 0, 10, 10, -1, None, None, stream=0)
 
 
+def test_host_side_validation_of_the_later_entry_points(nd):
+    """Threshold unmask, fused LM head, plain projection and the model calls
+    reject bad arguments on the host, before any device work."""
+    for tau, taur in ((-1.0, 2.0), (0.5, -0.5), (float("nan"), 2.0)):
+        with pytest.raises(nd.NdiffError) as e:
+            nd.ndiff_unmask_threshold(16, 16, 1, 32, tau, taur, 16, 16, 16, stream=0)
+        assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_unmask_threshold(16, 16, 1, 33, 0.5, 2.0, 16, 16, 16, stream=0)   # T > 32
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    nd.ndiff_unmask_threshold(None, None, 0, 32, 0.5, 2.0, None, None, None, stream=0)  # empty batch
+    for M, N, K, ex in ((0, 128, 64, -1), (4, 128, 96, -1), (4, 128, 64, 128), (4, 128, 64, -2)):
+        with pytest.raises(nd.NdiffError) as e:
+            nd.ndiff_lm_head_argmax(16, 16, M, N, K, ex, 16, 16, 16, 1 << 20, stream=0)
+        assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError) as e:
+        nd.ndiff_gemm_bf16(16, 16, 4, 128, 64, 16, 100, 16, 1 << 20, stream=0)      # ldy < N
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    with pytest.raises(nd.NdiffError):
+        nd._call("ndiff_decode_step_ex", None, None, None, None, None, nd._stream(0))
+    with pytest.raises(nd.NdiffError):
+        nd._call("ndiff_prefill_batch", None, None, None, nd._stream(0))
+    with pytest.raises(nd.NdiffError):
+        nd._call("ndiff_decode_step_batch", None, None, None, None, None, nd._stream(0))
+
+
 def test_workspace_sizes(nd):
     # one sequence, one split: no scratch
     assert nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 1, 32, 32, 8, 128, 512, 512) == 0
