@@ -378,8 +378,17 @@ NDIFF_API ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host,
  *             tokens.
  *   SELFSPEC: the DIFF draft (steps forwards) then one CAUSAL forward of
  *             [last, d0..d30]; commits the accepted prefix plus the correction.
+ *   SELFSPEC_FUSED (bf16, one sequence): unless the previous cycle left a
+ *             draft of this block, one BIDIR drafting forward; then one
+ *             forward of 64 rows that verifies [last, d0..d30] (CAUSAL) and
+ *             drafts the next block [d31, MASK x 31] at the following 32
+ *             positions (BIDIR over the prefix and the verified block, as if
+ *             it is accepted whole). Commits the accepted prefix plus the
+ *             correction; when all 32 drafts were accepted, the second half's
+ *             argmaxes are the next cycle's draft ([FFI] 吞吐量数据: linear
+ *             self-speculation). Needs max_seq >= committed + 64.
  * steps: drafting forwards per block (1 <= steps <= 32, 32 % steps == 0);
- *   ignored for AR.
+ *   ignored for AR and SELFSPEC_FUSED (one drafting forward).
  * out_tokens_host: host buffer of >= 32 int32; *n_out receives the count.
  * stats (optional) accumulates counters. Synchronous on return. */
 NDIFF_API ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps,

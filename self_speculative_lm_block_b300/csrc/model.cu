@@ -1,5 +1,8 @@
 // model.cu — the random-init tri-mode model behind the C ABI: weights, KV
-// cache, one forward of a token block, and the three decode modes.
+// caches, one forward of a token block, and the decode modes (AR, block
+// diffusion, self-speculation with top-k or threshold drafts, fused
+// verify + draft self-speculation), for one sequence or a batch of ragged
+// sequences decoded together.
 //
 // Sources (page title, section):
 //   "NVIDIA 发布 Nemotron-Labs Diffusion 语言模型系列" (fintech-frontier-insights),
@@ -18,7 +21,9 @@
 // token after it in every mode; [MASK] = vocab-1, never predicted; a diffusion
 // block enters the cache through one bidirectional forward of the finished
 // block; the self-speculation draft is `steps` bidirectional forwards, each
-// fixing the 32/steps most confident masked slots.
+// fixing the 32/steps most confident masked slots (or, with the threshold
+// sampler, every masked slot at or above tau, with revision of earlier slots);
+// the fused mode verifies a block and drafts the next one in a 64-row forward.
 //
 // Numerics: bf16 models keep bf16 weights and round the inputs of every matrix
 // product (normed activations, attention output, SwiGLU output) and q/k/v to
