@@ -22,7 +22,9 @@
 //     4-stage TMA ring (48 KB a stage, 128-byte swizzle); warp 1 issues
 //     tcgen05.mma M128 N256 K16; warps 2-5 drain the other accumulator in
 //     32-column slices, so the epilogue of one item overlaps the next item's
-//     main loop. No K split: there are enough items to fill the SMs.
+//     main loop. Launches of at most 64 rows (a batch's AR step) use 64-row
+//     chunks (M128 N64) and an 8-stage ring of 24 KB. No K split in either, so
+//     a row's arithmetic is the same in AR and block forwards.
 //   * Fused epilogues as in the skinny kernel, for token rows of several
 //     sequences: fp32 store, residual add, SwiGLU, QKV with RoPE and the K/V
 //     write at each token's own sequence and position, and the ARGMAX
