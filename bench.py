@@ -53,7 +53,7 @@ METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward
 # DRAM bytes (read + write) of one attention launch, from ncu captures of the
 # current attention kernel on these workloads (summaries under profiles/);
 # None where no capture exists.
-ATTN_TRAFFIC = {"attn-batched": 1016157440 + 9754880, "attn-long": 539045120 + 72704,
+ATTN_TRAFFIC = {"attn-batched": 1016157440 + 9754880, "attn-long": 539051520 + 3462400,
                 "attn-single": None}
 SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126e6
@@ -431,6 +431,79 @@ def run_lm_head(reps=20):
     return out
 
 
+def run_select_batch(B=65536, T=32, k=8, usets=48, vsets=8):
+    """Unmask (top-k) and verify/accept over a batch large enough for a
+    bandwidth figure: 65536 sequences of 32 slots. Every launch in the timed
+    graph works on its own copy of the inputs (unmask: 48 copies of 34 MB, one
+    per launch, mask words reset before the replay and outside the timed
+    region; verify: 8 copies of 26 MB cycled), so each launch reads its inputs
+    from HBM rather than from the 126 MB L2. Algorithmic bytes per sequence:
+    unmask reads conf, pred and the mask word and writes the mask word, the k
+    chosen slots and k draft and next-input tokens; verify reads draft and
+    target and writes the commit row, accept length and commit count, and
+    reads and writes the prefix length."""
+    import torch
+    from self_speculative_lm_block_b300 import ndiff as nd
+    from self_speculative_lm_block_b300 import synth
+    hbm, _, _, src = _peaks()
+    conf, pred, mask = synth.unmask_inputs(B, T, 151936, 4001)
+    draft, target, _ = synth.draft_target(B, T, 151936, 4002)
+    conf, pred, mask, draft, target = (t.cuda() for t in (conf, pred, mask, draft, target))
+    z = lambda *shape: torch.zeros(shape, dtype=torch.int32, device="cuda")
+    U = [dict(conf=conf.clone(), pred=pred.clone(), mk=mask.clone(), blk=z(B, T), dr=z(B, T),
+              ch=z(B, k)) for _ in range(usets)]
+    V = [dict(draft=draft.clone(), target=target.clone(), L=z(B), n=z(B), com=z(B, T), kv=z(B))
+         for _ in range(vsets)]
+    s = torch.cuda.Stream()
+
+    def time_graph(fn, reps, nsets, reset=lambda: None):
+        with torch.cuda.stream(s):
+            reset()
+            for i in range(nsets):
+                fn(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for r in range(reps):
+                    fn(r % nsets)
+            reset()
+            g.replay()
+            torch.cuda.synchronize()
+            reset()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def reset_masks():
+        for u in U:
+            u["mk"].copy_(mask)
+
+    def unmask(i):
+        u = U[i]
+        nd.ndiff_unmask(u["conf"], u["pred"], B, T, k, u["mk"], u["blk"], u["dr"], u["ch"],
+                        s.cuda_stream)
+
+    def verify(i):
+        v = V[i]
+        nd.ndiff_verify_accept(v["draft"], v["target"], B, T, v["L"], v["com"], v["n"], v["kv"],
+                               s.cuda_stream)
+
+    t_u = time_graph(unmask, usets, usets, reset_masks)
+    t_v = time_graph(verify, 48, vsets)
+    bytes_u = B * (T * 4 * 2 + 4 + 4 + k * 4 * 3)
+    bytes_v = B * (T * 4 * 3 + 4 * 4)
+    res = {"label": f"{B} sequences x {T} slots, every launch on its own copy of the inputs "
+                    "(throughput figure; decode steps use a few sequences)"}
+    for name, t, nb in (("unmask_k8", t_u, bytes_u), ("verify_accept", t_v, bytes_v)):
+        gbs = nb / (t * 1e-6) / 1e9
+        res[name] = {"us": t, "bytes": nb, "gbs": gbs, "frac_hbm": gbs / hbm, "peak_source": src}
+    return res
+
+
 def run_forced_accept(rank, n_tokens=256):
     """The fused self-speculation machinery with every draft accepted: the
     8B-shaped body with a two-id vocabulary ([MASK] and one token), so each
@@ -649,6 +722,7 @@ def main():
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
     lm_head = run_lm_head() if args.model_tokens > 0 else None
     forced = run_forced_accept(rank) if args.model_tokens > 0 else None
+    select = run_select_batch()
     batched = run_model_batched(rank, args.batch_model, args.batch_tokens) \
         if args.batch_model > 0 else None
     if model is not None and world > 1:
@@ -679,6 +753,7 @@ def main():
             out["lm_head_8b"] = lm_head
         if forced is not None:
             out["model_8b"]["forced_accept_fused"] = forced
+        out["select_65536"] = select
         if batched is not None:
             out["model_8b_batched"] = batched
         if not args.no_cpu_baseline:

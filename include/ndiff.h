@@ -200,18 +200,6 @@ NDIFF_API ndiff_status ndiff_unmask(const float* conf, const int32_t* pred, int 
                           int32_t* chosen, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
- * Self-speculation verify / accept ([GSY] §2.3; [FFI] "三种生成模式":
- * diffusion drafts, AR verifies, temperature-0 output equals AR output).
- * For each sequence b:
- *   accept_len[b] = L = first i in [0,T) with draft[b][i] != target[b][i], or T;
- *   n_commit[b]   = n = min(L+1, T)  (the accepted drafts plus the target's
- *                                     correction token when L < T);
- *   commit[b][j]  = target[b][j] for j < n, -1 otherwise;
- *   kv_len[b]    += n   (skipped when kv_len is NULL).
- * Shapes: draft, target, commit int32 [B][T]; accept_len, n_commit, kv_len
- * int32 [B]. 1 <= T <= 32. B == 0 is a no-op.
- * ------------------------------------------------------------------------ */
-/* ------------------------------------------------------------------------ *
  * Threshold unmask round with revision (the sampler variant of
  * NDIFF_SAMPLER_THRESHOLD; [HFB]: refinement rounds are a budget and earlier
  * tokens can be revised). For each sequence b, with M the masked slots (bits
@@ -233,6 +221,18 @@ NDIFF_API ndiff_status ndiff_unmask_threshold(const float* conf, const int32_t* 
                                               int32_t* block_in, int32_t* draft, int32_t* n_fixed,
                                               int32_t* n_revised, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * Self-speculation verify / accept ([GSY] §2.3; [FFI] "三种生成模式":
+ * diffusion drafts, AR verifies, temperature-0 output equals AR output).
+ * For each sequence b:
+ *   accept_len[b] = L = first i in [0,T) with draft[b][i] != target[b][i], or T;
+ *   n_commit[b]   = n = min(L+1, T)  (the accepted drafts plus the target's
+ *                                     correction token when L < T);
+ *   commit[b][j]  = target[b][j] for j < n, -1 otherwise;
+ *   kv_len[b]    += n   (skipped when kv_len is NULL).
+ * Shapes: draft, target, commit int32 [B][T]; accept_len, n_commit, kv_len
+ * int32 [B]. 1 <= T <= 32. B == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
 NDIFF_API ndiff_status ndiff_verify_accept(const int32_t* draft, const int32_t* target, int B, int T,
                                  int32_t* accept_len, int32_t* commit, int32_t* n_commit,
                                  int32_t* kv_len, cudaStream_t stream);

@@ -206,6 +206,87 @@ def test_unmask(nd, T, ties, allm):
         assert np.array_equal(ch.cpu().numpy(), rch)
 
 
+@pytest.mark.parametrize("B", [256, 4096 + 77])
+@pytest.mark.parametrize("ties,allm", [(False, False), (True, False), (True, True)])
+def test_unmask_row_parallel_batches(nd, B, ties, allm):
+    """Batches of 32-slot blocks from 256 sequences up take the row-parallel
+    layout (one thread per sequence, ranks from pairwise key comparisons); a
+    ragged last CTA and every k in {1, 4, 8, 32}, bit for bit."""
+    T = 32
+    conf, pred, mask = synth.unmask_inputs(B, T, 151936, 301 + B, ties=ties, all_masked=allm)
+    for k in (1, 4, 8, 32):
+        blk = torch.full((B, T), 7, dtype=torch.int32)
+        dr = torch.full((B, T), -1, dtype=torch.int32)
+        m_d, b_d, d_d = mask.cuda(), blk.cuda(), dr.cuda()
+        ch = torch.empty((B, k), dtype=torch.int32, device="cuda")
+        nd.ndiff_unmask(conf.cuda(), pred.cuda(), B, T, k, m_d, b_d, d_d, ch)
+        rm, rb, rd, rch = OD.unmask(conf.numpy(), pred.numpy(), mask.numpy().view(np.uint32),
+                                    blk.numpy(), dr.numpy(), k)
+        assert np.array_equal(m_d.cpu().numpy().view(np.uint32), rm), k
+        assert np.array_equal(b_d.cpu().numpy(), rb), k
+        assert np.array_equal(d_d.cpu().numpy(), rd), k
+        assert np.array_equal(ch.cpu().numpy(), rch), k
+
+
+def test_unmask_signed_zero_and_infinite_confidence(nd):
+    """-0 ties +0 (the lower slot wins), -inf ranks below every finite value
+    and +inf above; both layouts (one warp per sequence below 256 sequences,
+    one thread per sequence from 256) against the oracle."""
+    T = 32
+    vals = np.array([0.0, -0.0, -np.inf, np.inf, 1e-30, -1e-30, 0.5, -0.5], dtype=np.float32)
+    for B in (64, 512):
+        rng = np.random.default_rng(B)
+        conf = torch.from_numpy(vals[rng.integers(0, len(vals), size=(B, T))])
+        pred = torch.from_numpy(rng.integers(0, 1000, size=(B, T)).astype(np.int32))
+        mask = torch.from_numpy(rng.integers(0, 2**32, size=B, dtype=np.uint64)
+                                .astype(np.uint32).view(np.int32))
+        for k in (3, 32):
+            blk = torch.zeros((B, T), dtype=torch.int32)
+            dr = torch.full((B, T), -1, dtype=torch.int32)
+            m_d, b_d, d_d = mask.cuda(), blk.cuda(), dr.cuda()
+            ch = torch.empty((B, k), dtype=torch.int32, device="cuda")
+            nd.ndiff_unmask(conf.cuda(), pred.cuda(), B, T, k, m_d, b_d, d_d, ch)
+            rm, rb, rd, rch = OD.unmask(conf.numpy(), pred.numpy(), mask.numpy().view(np.uint32),
+                                        blk.numpy(), dr.numpy(), k)
+            assert np.array_equal(ch.cpu().numpy(), rch), (B, k)
+            assert np.array_equal(m_d.cpu().numpy().view(np.uint32), rm), (B, k)
+            assert np.array_equal(d_d.cpu().numpy(), rd), (B, k)
+            assert np.array_equal(b_d.cpu().numpy(), rb), (B, k)
+
+
+def test_unmask_and_verify_unaligned_rows_take_the_warp_layout(nd):
+    """Row pointers that are not 16-byte aligned (a view offset by one
+    element) fall back to one warp per sequence: same results."""
+    B, T, k = 300, 32, 8
+    conf, pred, mask = synth.unmask_inputs(B, T, 151936, 17)
+    cbuf = torch.zeros(B * T + 1, device="cuda")
+    pbuf = torch.zeros(B * T + 1, dtype=torch.int32, device="cuda")
+    cbuf[1:] = conf.reshape(-1).cuda()
+    pbuf[1:] = pred.reshape(-1).cuda()
+    blk = torch.zeros((B, T), dtype=torch.int32)
+    dr = torch.full((B, T), -1, dtype=torch.int32)
+    m_d, b_d, d_d = mask.cuda(), blk.cuda(), dr.cuda()
+    ch = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    nd.ndiff_unmask(cbuf[1:], pbuf[1:], B, T, k, m_d, b_d, d_d, ch)
+    rm, rb, rd, rch = OD.unmask(conf.numpy(), pred.numpy(), mask.numpy().view(np.uint32),
+                                blk.numpy(), dr.numpy(), k)
+    assert np.array_equal(ch.cpu().numpy(), rch)
+    assert np.array_equal(m_d.cpu().numpy().view(np.uint32), rm)
+    assert np.array_equal(d_d.cpu().numpy(), rd) and np.array_equal(b_d.cpu().numpy(), rb)
+    draft, target, _ = synth.draft_target(B, T, 151936, 18)
+    dbuf = torch.zeros(B * T + 1, dtype=torch.int32, device="cuda")
+    dbuf[1:] = draft.reshape(-1).cuda()
+    kv = torch.arange(B, dtype=torch.int32)
+    L = torch.empty(B, dtype=torch.int32, device="cuda")
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    cm = torch.empty((B, T), dtype=torch.int32, device="cuda")
+    kvd = kv.cuda()
+    nd.ndiff_verify_accept(dbuf[1:], target.cuda(), B, T, L, cm, n, kvd)
+    rL, rc, rn, rkv = OD.verify_accept(draft.numpy(), target.numpy(), kv.numpy())
+    assert np.array_equal(L.cpu().numpy(), rL) and np.array_equal(n.cpu().numpy(), rn)
+    assert np.array_equal(cm.cpu().numpy(), rc) and np.array_equal(kvd.cpu().numpy(), rkv)
+
+
 @pytest.mark.parametrize("T,ties,allm", [(32, False, False), (32, True, False), (32, True, True),
                                          (7, True, False), (1, False, True)])
 def test_unmask_threshold(nd, T, ties, allm):
@@ -243,7 +324,8 @@ def test_unmask_threshold_rejects_bad_arguments(nd):
 
 
 # ---------------------------------------------------------------- verify/accept
-@pytest.mark.parametrize("B,T", [(64, 32), (5, 1), (33, 7), (1000, 32)])
+@pytest.mark.parametrize("B,T", [(64, 32), (5, 1), (33, 7), (1000, 32), (1, 32), (31, 32),
+                                 (4096 + 5, 32)])
 def test_verify_accept(nd, B, T):
     draft, target, _ = synth.draft_target(B, T, 151936, 81 + T)
     kv = torch.arange(B, dtype=torch.int32) * 3
@@ -257,3 +339,36 @@ def test_verify_accept(nd, B, T):
     assert np.array_equal(n.cpu().numpy(), rn)
     assert np.array_equal(cm.cpu().numpy(), rc)
     assert np.array_equal(kvd.cpu().numpy(), rkv)
+
+
+def test_unmask_and_verify_at_bench_batch_sampled_rows(nd):
+    """The batch size the bandwidth figure is measured at (65536 sequences x
+    32 slots): every row is independent, so 2048 sampled rows (first, last and
+    random) are checked against the oracle bit for bit."""
+    B, T, k = 65536, 32, 8
+    conf, pred, mask = synth.unmask_inputs(B, T, 151936, 4001)
+    draft, target, _ = synth.draft_target(B, T, 151936, 4002)
+    blk = torch.zeros((B, T), dtype=torch.int32)
+    dr = torch.zeros((B, T), dtype=torch.int32)
+    m_d, b_d, d_d = mask.cuda(), blk.cuda(), dr.cuda()
+    ch = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    nd.ndiff_unmask(conf.cuda(), pred.cuda(), B, T, k, m_d, b_d, d_d, ch)
+    kv = torch.zeros(B, dtype=torch.int32)
+    L = torch.empty(B, dtype=torch.int32, device="cuda")
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    cm = torch.empty((B, T), dtype=torch.int32, device="cuda")
+    kvd = kv.cuda()
+    nd.ndiff_verify_accept(draft.cuda(), target.cuda(), B, T, L, cm, n, kvd)
+    rows = np.unique(np.concatenate([[0, B - 1], np.random.default_rng(5).integers(0, B, 2046)]))
+    rm, rb, rd, rch = OD.unmask(conf.numpy()[rows], pred.numpy()[rows],
+                                mask.numpy().view(np.uint32)[rows], blk.numpy()[rows],
+                                dr.numpy()[rows], k)
+    assert np.array_equal(m_d.cpu().numpy().view(np.uint32)[rows], rm)
+    assert np.array_equal(b_d.cpu().numpy()[rows], rb)
+    assert np.array_equal(d_d.cpu().numpy()[rows], rd)
+    assert np.array_equal(ch.cpu().numpy()[rows], rch)
+    rL, rc, rn, rkv = OD.verify_accept(draft.numpy()[rows], target.numpy()[rows], kv.numpy()[rows])
+    assert np.array_equal(L.cpu().numpy()[rows], rL)
+    assert np.array_equal(n.cpu().numpy()[rows], rn)
+    assert np.array_equal(cm.cpu().numpy()[rows], rc)
+    assert np.array_equal(kvd.cpu().numpy()[rows], rkv)
