@@ -19,12 +19,14 @@
 //
 // Batches of 32-slot blocks take two more layouts, chosen when the row pointers
 // are 16-byte aligned:
-// unmask_rows_kernel: one thread per sequence, for B >= 256. The CTA stages
-//   its 128 rows of conf and pred through shared memory with 16-byte coalesced
-//   loads; each thread turns its 32 confidences into order-preserving integer
-//   keys (0 marks an unmasked slot) and ranks them with the 496 pairwise
-//   comparisons, so no lane exchange is needed; the chosen lists leave through
-//   shared memory as one coalesced write. Same selection as unmask_kernel.
+// unmask_quad_kernel: four lanes per sequence, for B >= 256. Each lane loads
+//   8 of the row's confidences with two coalesced 16-byte loads, turns them
+//   into order-preserving integer keys (0 marks an unmasked slot), and counts
+//   for each of its slots the slots that beat it: 28 comparisons among its
+//   own and 3 x 64 against the keys its three partners pass by shuffle.
+//   Same selection as unmask_kernel, with 4 times the sequences in flight of
+//   one thread per sequence and a quarter of the warp-wide shuffles of one
+//   warp per sequence.
 // verify32_kernel: one warp per 32 sequences, every global access 16 bytes
 //   wide; a warp load covers 4 rows (8 lanes a row), the mismatch bits of a row
 //   are OR-ed over its 8 lanes, and the per-sequence results are written by the
@@ -143,8 +145,8 @@ __global__ void __launch_bounds__(128) verify_kernel(const int32_t* __restrict__
   }
 }
 
-constexpr int ROWS_PER_CTA = 128;
-constexpr int UNMASK_ROWS_MIN_B = 256;
+constexpr int QUAD_ROWS_PER_CTA = 32;  // 128 threads, 4 a sequence
+constexpr int UNMASK_QUAD_MIN_B = 256;
 
 // Order-preserving key of a non-NaN float: larger float, larger key; -0 and +0
 // share a key so that they tie as float comparison has them tie. Every key is
@@ -155,97 +157,98 @@ __device__ __forceinline__ uint32_t order_key(float c) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(ROWS_PER_CTA)
-    unmask_rows_kernel(const float* __restrict__ conf, const int32_t* __restrict__ pred, int B,
+// Four lanes share a sequence; lane q (0..3) owns slots 4q..4q+3 and
+// 16+4q..16+4q+3, so each of its two 16-byte loads of a row is coalesced with
+// the other lanes' (a warp load covers the first or second half of 8 rows).
+__device__ __forceinline__ constexpr int quad_slot(int q, int e) {
+  return e < 4 ? 4 * q + e : 16 + 4 * q + (e - 4);
+}
+
+__global__ void __launch_bounds__(128)
+    unmask_quad_kernel(const float* __restrict__ conf, const int32_t* __restrict__ pred, int B,
                        int k, uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                        int32_t* chosen) {
-  // 16-byte chunk j of row r sits at r * 8 + (j ^ (r & 7)), so the 8 threads of
-  // a quarter warp reading chunk j of their own rows hit 8 different bank groups.
-  __shared__ int4 s_conf[ROWS_PER_CTA * 8];
-  __shared__ int4 s_pred[ROWS_PER_CTA * 8];
   griddep_launch();
   griddep_wait();
-  const int row0 = blockIdx.x * ROWS_PER_CTA;
-  const int nrows = min(ROWS_PER_CTA, B - row0);
-  const int tid = threadIdx.x;
-  {
-    const int4* gc = reinterpret_cast<const int4*>(conf) + (size_t)row0 * 8;
-    const int4* gp = reinterpret_cast<const int4*>(pred) + (size_t)row0 * 8;
-    int4 vc[8], vp[8];
+  const int q = threadIdx.x & 3;
+  const int b = blockIdx.x * QUAD_ROWS_PER_CTA + (threadIdx.x >> 2);
+  const bool live = b < B;
+  // every lane takes part in the shuffles: a lane past the batch reads row 0
+  // (B >= 1) and writes nothing
+  const int row = live ? b : 0;
+  const int4* gc = reinterpret_cast<const int4*>(conf) + (size_t)row * 8;
+  const int4* gp = reinterpret_cast<const int4*>(pred) + (size_t)row * 8;
+  const int4 c0 = __ldg(gc + q), c1 = __ldg(gc + 4 + q);
+  const int4 p0 = __ldg(gp + q), p1 = __ldg(gp + 4 + q);
+  const uint32_t mask = mask_bits[row];
+  uint32_t key[8] = {order_key(__int_as_float(c0.x)), order_key(__int_as_float(c0.y)),
+                     order_key(__int_as_float(c0.z)), order_key(__int_as_float(c0.w)),
+                     order_key(__int_as_float(c1.x)), order_key(__int_as_float(c1.y)),
+                     order_key(__int_as_float(c1.z)), order_key(__int_as_float(c1.w))};
+  const int32_t pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int q = it * ROWS_PER_CTA + tid;
-      if ((q >> 3) < nrows) {
-        vc[it] = __ldg(gc + q);
-        vp[it] = __ldg(gp + q);
-      }
-    }
+  for (int e = 0; e < 8; ++e) key[e] = ((mask >> quad_slot(q, e)) & 1u) ? key[e] : 0u;
+  // rank[e] = number of slots that beat own slot e: o beats m when
+  // key_o + [slot_o < slot_m] > key_m (ties go to the lower slot; the +1 never
+  // overflows since every key is <= key(+inf) = 0xff800000).
+  int rank[8];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int q = it * ROWS_PER_CTA + tid;
-      const int r = q >> 3, j = q & 7;
-      if (r < nrows) {
-        s_conf[r * 8 + (j ^ (r & 7))] = vc[it];
-        s_pred[r * 8 + (j ^ (r & 7))] = vp[it];
-      }
-    }
-  }
-  __syncthreads();
-  const bool live = tid < nrows;
-  const int b = row0 + tid;
-  const uint32_t mask = live ? mask_bits[b] : 0u;
-  uint32_t key[32];
+  for (int e = 0; e < 8; ++e) rank[e] = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int4 v = s_conf[tid * 8 + (j ^ (tid & 7))];
-    key[4 * j + 0] = order_key(__int_as_float(v.x));
-    key[4 * j + 1] = order_key(__int_as_float(v.y));
-    key[4 * j + 2] = order_key(__int_as_float(v.z));
-    key[4 * j + 3] = order_key(__int_as_float(v.w));
-  }
+  for (int e = 0; e < 8; ++e) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) key[i] = ((mask >> i) & 1u) ? key[i] : 0u;
-  // rank[i] = number of slots that beat slot i; for i < j, j beats i only on a
-  // strictly larger key (ties go to the lower slot). Unmasked slots (key 0)
-  // never beat a masked one, and their own ranks are not used.
-  int rank[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) rank[i] = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-#pragma unroll
-    for (int j = i + 1; j < 32; ++j) {
-      const int p = key[j] > key[i] ? 1 : 0;
-      rank[i] += p;
-      rank[j] += 1 - p;
+    for (int f = e + 1; f < 8; ++f) {  // own slots rise with e
+      const int p = key[f] > key[e] ? 1 : 0;
+      rank[e] += p;
+      rank[f] += 1 - p;
     }
   }
-  __syncthreads();  // every thread holds its keys: s_conf now holds the chosen lists
-  int32_t* s_chosen = reinterpret_cast<int32_t*>(s_conf);
+#pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    uint32_t o[8];
+#pragma unroll
+    for (int f = 0; f < 8; ++f) o[f] = __shfl_xor_sync(0xffffffffu, key[f], d);
+    // the partner's first-half slots lie below every own second-half slot and
+    // its second-half slots above every own first-half slot; within a half
+    // the lower lane has the lower slots
+    const uint32_t lower = ((q ^ d) < q) ? 1u : 0u;
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+      const uint32_t same = o[f] + lower, below = o[f] + 1u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rank[e] += same > key[e] ? 1 : 0;
+#pragma unroll
+      for (int e = 4; e < 8; ++e) rank[e] += below > key[e] ? 1 : 0;
+    }
+#pragma unroll
+    for (int f = 4; f < 8; ++f) {
+      const uint32_t same = o[f] + lower;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rank[e] += o[f] > key[e] ? 1 : 0;
+#pragma unroll
+      for (int e = 4; e < 8; ++e) rank[e] += same > key[e] ? 1 : 0;
+    }
+  }
+  const int kk = min(k, __popc(mask));
+  uint32_t taken = 0u;
   if (live) {
-    const int kk = min(k, __popc(mask));
-    uint32_t taken = 0u;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int4 v = s_pred[tid * 8 + (j ^ (tid & 7))];
-      const int32_t pv4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * j + e;
-        if (key[i] != 0u && rank[i] < kk) {
-          draft[(size_t)b * 32 + i] = pv4[e];
-          if (i <= 30) block_in[(size_t)b * 32 + i + 1] = pv4[e];
-          s_chosen[tid * k + rank[i]] = i;
-          taken |= 1u << i;
-        }
+    for (int e = 0; e < 8; ++e) {
+      const int i = quad_slot(q, e);
+      if (key[e] != 0u && rank[e] < kk) {
+        draft[(size_t)b * 32 + i] = pv[e];
+        if (i <= 30) block_in[(size_t)b * 32 + i + 1] = pv[e];
+        chosen[(size_t)b * k + rank[e]] = i;
+        taken |= 1u << i;
       }
     }
-    for (int r = kk; r < k; ++r) s_chosen[tid * k + r] = -1;
-    mask_bits[b] = mask & ~taken;
   }
-  __syncthreads();
-  int32_t* out = chosen + (size_t)row0 * k;
-  for (int q = tid; q < nrows * k; q += ROWS_PER_CTA) out[q] = s_chosen[q];
+  taken |= __shfl_xor_sync(0xffffffffu, taken, 1);
+  taken |= __shfl_xor_sync(0xffffffffu, taken, 2);
+  if (live) {
+    for (int r = kk + q; r < k; r += 4) chosen[(size_t)b * k + r] = -1;
+    if (q == 0) mask_bits[b] = mask & ~taken;
+  }
 }
 
 __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict__ draft,
@@ -313,10 +316,10 @@ ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T,
                            uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                            int32_t* chosen, cudaStream_t stream) {
   if (B == 0) return NDIFF_OK;
-  if (T == 32 && B >= UNMASK_ROWS_MIN_B && aligned16(conf) && aligned16(pred)) {
-    NDIFF_CUDA_TRY(launch_k(unmask_rows_kernel, dim3((B + ROWS_PER_CTA - 1) / ROWS_PER_CTA),
-                            dim3(ROWS_PER_CTA), 0, stream, conf, pred, B, k, mask_bits, block_in,
-                            draft, chosen));
+  if (T == 32 && B >= UNMASK_QUAD_MIN_B && aligned16(conf) && aligned16(pred)) {
+    NDIFF_CUDA_TRY(launch_k(unmask_quad_kernel,
+                            dim3((B + QUAD_ROWS_PER_CTA - 1) / QUAD_ROWS_PER_CTA), dim3(128), 0,
+                            stream, conf, pred, B, k, mask_bits, block_in, draft, chosen));
     return NDIFF_OK;
   }
   NDIFF_CUDA_TRY(launch_k(unmask_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, conf, pred, B, T,

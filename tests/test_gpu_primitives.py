@@ -209,9 +209,9 @@ def test_unmask(nd, T, ties, allm):
 @pytest.mark.parametrize("B", [256, 4096 + 77])
 @pytest.mark.parametrize("ties,allm", [(False, False), (True, False), (True, True)])
 def test_unmask_row_parallel_batches(nd, B, ties, allm):
-    """Batches of 32-slot blocks from 256 sequences up take the row-parallel
-    layout (one thread per sequence, ranks from pairwise key comparisons); a
-    ragged last CTA and every k in {1, 4, 8, 32}, bit for bit."""
+    """Batches of 32-slot blocks from 256 sequences up take the four-lanes-a-
+    sequence layout (ranks from pairwise key comparisons, keys passed by
+    shuffle); a ragged last CTA and every k in {1, 4, 8, 32}, bit for bit."""
     T = 32
     conf, pred, mask = synth.unmask_inputs(B, T, 151936, 301 + B, ties=ties, all_masked=allm)
     for k in (1, 4, 8, 32):
@@ -231,7 +231,7 @@ def test_unmask_row_parallel_batches(nd, B, ties, allm):
 def test_unmask_signed_zero_and_infinite_confidence(nd):
     """-0 ties +0 (the lower slot wins), -inf ranks below every finite value
     and +inf above; both layouts (one warp per sequence below 256 sequences,
-    one thread per sequence from 256) against the oracle."""
+    four lanes per sequence from 256) against the oracle."""
     T = 32
     vals = np.array([0.0, -0.0, -np.inf, np.inf, 1e-30, -1e-30, 0.5, -0.5], dtype=np.float32)
     for B in (64, 512):
