@@ -24,9 +24,12 @@
 //   into order-preserving integer keys (0 marks an unmasked slot), and counts
 //   for each of its slots the slots that beat it: 28 comparisons among its
 //   own and 3 x 64 against the keys its three partners pass by shuffle.
-//   Same selection as unmask_kernel, with 4 times the sequences in flight of
-//   one thread per sequence and a quarter of the warp-wide shuffles of one
-//   warp per sequence.
+//   The lane merges the chosen tokens into its 16-byte chunks of the draft and
+//   next-input rows (one shuffle brings the lower lane's last slot for the
+//   shift by one) and writes back whole chunks, so no store is a partial
+//   sector. Same selection as unmask_kernel, with 4 times the sequences in
+//   flight of one thread per sequence and a quarter of the warp-wide shuffles
+//   of one warp per sequence.
 // verify32_kernel: one warp per 32 sequences, every global access 16 bytes
 //   wide; a warp load covers 4 rows (8 lanes a row), the mismatch bits of a row
 //   are OR-ed over its 8 lanes, and the per-sequence results are written by the
@@ -180,6 +183,9 @@ __global__ void __launch_bounds__(128)
   const int4* gp = reinterpret_cast<const int4*>(pred) + (size_t)row * 8;
   const int4 c0 = __ldg(gc + q), c1 = __ldg(gc + 4 + q);
   const int4 p0 = __ldg(gp + q), p1 = __ldg(gp + 4 + q);
+  int4* gd = reinterpret_cast<int4*>(draft) + (size_t)row * 8;
+  int4* gb = reinterpret_cast<int4*>(block_in) + (size_t)row * 8;
+  const int4 d0 = gd[q], d1 = gd[4 + q], i0 = gb[q], i1 = gb[4 + q];
   const uint32_t mask = mask_bits[row];
   uint32_t key[8] = {order_key(__int_as_float(c0.x)), order_key(__int_as_float(c0.y)),
                      order_key(__int_as_float(c0.z)), order_key(__int_as_float(c0.w)),
@@ -230,25 +236,45 @@ __global__ void __launch_bounds__(128)
     }
   }
   const int kk = min(k, __popc(mask));
+  bool sel[8];
   uint32_t taken = 0u;
-  if (live) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int i = quad_slot(q, e);
-      if (key[e] != 0u && rank[e] < kk) {
-        draft[(size_t)b * 32 + i] = pv[e];
-        if (i <= 30) block_in[(size_t)b * 32 + i + 1] = pv[e];
-        chosen[(size_t)b * k + rank[e]] = i;
-        taken |= 1u << i;
-      }
-    }
+  for (int e = 0; e < 8; ++e) {
+    sel[e] = key[e] != 0u && rank[e] < kk;
+    if (sel[e]) taken |= 1u << quad_slot(q, e);
   }
+  // block_in[i + 1] takes pred[i]: the first slot of each of the lane's two
+  // chunks follows the last slot of the lower lane's chunk (lane 3's first
+  // chunk for lane 0's second; nothing for slot 0)
+  const int src_lane = (threadIdx.x & ~3) | ((q + 3) & 3);
+  const int nb_sel3 = __shfl_sync(0xffffffffu, sel[3] ? 1 : 0, src_lane);
+  const int32_t nb_pv3 = __shfl_sync(0xffffffffu, pv[3], src_lane);
+  const int nb_sel7 = __shfl_sync(0xffffffffu, sel[7] ? 1 : 0, src_lane);
+  const int32_t nb_pv7 = __shfl_sync(0xffffffffu, pv[7], src_lane);
   taken |= __shfl_xor_sync(0xffffffffu, taken, 1);
   taken |= __shfl_xor_sync(0xffffffffu, taken, 2);
-  if (live) {
-    for (int r = kk + q; r < k; r += 4) chosen[(size_t)b * k + r] = -1;
-    if (q == 0) mask_bits[b] = mask & ~taken;
-  }
+  if (!live) return;
+  const bool in0 = q > 0 && nb_sel3;
+  const bool in4 = q > 0 ? (nb_sel7 != 0) : (nb_sel3 != 0);
+  const int32_t v4 = q > 0 ? nb_pv7 : nb_pv3;
+  // merged chunks; a chunk is written back only where a slot changed
+  const int4 nd0 = make_int4(sel[0] ? pv[0] : d0.x, sel[1] ? pv[1] : d0.y, sel[2] ? pv[2] : d0.z,
+                             sel[3] ? pv[3] : d0.w);
+  const int4 nd1 = make_int4(sel[4] ? pv[4] : d1.x, sel[5] ? pv[5] : d1.y, sel[6] ? pv[6] : d1.z,
+                             sel[7] ? pv[7] : d1.w);
+  const int4 ni0 = make_int4(in0 ? nb_pv3 : i0.x, sel[0] ? pv[0] : i0.y, sel[1] ? pv[1] : i0.z,
+                             sel[2] ? pv[2] : i0.w);
+  const int4 ni1 = make_int4(in4 ? v4 : i1.x, sel[4] ? pv[4] : i1.y, sel[5] ? pv[5] : i1.z,
+                             sel[6] ? pv[6] : i1.w);
+  if (sel[0] || sel[1] || sel[2] || sel[3]) gd[q] = nd0;
+  if (sel[4] || sel[5] || sel[6] || sel[7]) gd[4 + q] = nd1;
+  if (in0 || sel[0] || sel[1] || sel[2]) gb[q] = ni0;
+  if (in4 || sel[4] || sel[5] || sel[6]) gb[4 + q] = ni1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (sel[e]) chosen[(size_t)b * k + rank[e]] = quad_slot(q, e);
+  for (int r = kk + q; r < k; r += 4) chosen[(size_t)b * k + r] = -1;
+  if (q == 0) mask_bits[b] = mask & ~taken;
 }
 
 __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict__ draft,
@@ -316,7 +342,8 @@ ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T,
                            uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                            int32_t* chosen, cudaStream_t stream) {
   if (B == 0) return NDIFF_OK;
-  if (T == 32 && B >= UNMASK_QUAD_MIN_B && aligned16(conf) && aligned16(pred)) {
+  if (T == 32 && B >= UNMASK_QUAD_MIN_B && aligned16(conf) && aligned16(pred) &&
+      aligned16(draft) && aligned16(block_in)) {
     NDIFF_CUDA_TRY(launch_k(unmask_quad_kernel,
                             dim3((B + QUAD_ROWS_PER_CTA - 1) / QUAD_ROWS_PER_CTA), dim3(128), 0,
                             stream, conf, pred, B, k, mask_bits, block_in, draft, chosen));
