@@ -30,10 +30,11 @@
 //   sector. Same selection as unmask_kernel, with 4 times the sequences in
 //   flight of one thread per sequence and a quarter of the warp-wide shuffles
 //   of one warp per sequence.
-// verify32_kernel: one warp per 32 sequences, every global access 16 bytes
-//   wide; a warp load covers 4 rows (8 lanes a row), the mismatch bits of a row
-//   are OR-ed over its 8 lanes, and the per-sequence results are written by the
-//   lane of that sequence.
+// verify32_kernel: one warp per 8 sequences (two passes of 4), every global
+//   access 16 bytes wide; a warp load covers 4 rows (8 lanes a row), the
+//   mismatch bits of a row are OR-ed over its 8 lanes, and the per-sequence
+//   results are written by the lane of that sequence. Few rows a warp keeps
+//   registers low, so a 65536-sequence batch is resident in one wave.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -277,6 +278,9 @@ __global__ void __launch_bounds__(128)
   if (q == 0) mask_bits[b] = mask & ~taken;
 }
 
+constexpr int VERIFY_PASSES = 2;                   // rows a warp takes: 4 per pass
+constexpr int VERIFY_ROWS_PER_WARP = 4 * VERIFY_PASSES;
+
 __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict__ draft,
                                                        const int32_t* __restrict__ target, int B,
                                                        int32_t* accept_len, int32_t* commit,
@@ -284,15 +288,15 @@ __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict
   griddep_launch();
   griddep_wait();
   const int lane = threadIdx.x & 31;
-  const int base = (blockIdx.x * 4 + (threadIdx.x >> 5)) * 32;
+  const int base = (blockIdx.x * 4 + (threadIdx.x >> 5)) * VERIFY_ROWS_PER_WARP;
   if (base >= B) return;  // uniform over the warp
   const int g = lane >> 3, c = lane & 7;
   const int4* gd = reinterpret_cast<const int4*>(draft);
   const int4* gt = reinterpret_cast<const int4*>(target);
   int4* gc = reinterpret_cast<int4*>(commit);
-  int4 d[8], t[8];
+  int4 d[VERIFY_PASSES], t[VERIFY_PASSES];
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
+  for (int it = 0; it < VERIFY_PASSES; ++it) {
     const int row = base + it * 4 + g;
     if (row < B) {
       d[it] = __ldg(gd + (size_t)row * 8 + c);
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict
   }
   int my_len = 32;
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
+  for (int it = 0; it < VERIFY_PASSES; ++it) {
     const uint32_t nib = (d[it].x != t[it].x ? 1u : 0u) | (d[it].y != t[it].y ? 2u : 0u) |
                          (d[it].z != t[it].z ? 4u : 0u) | (d[it].w != t[it].w ? 8u : 0u);
     uint32_t bits = nib << (4 * c);
@@ -320,13 +324,13 @@ __global__ void __launch_bounds__(128) verify32_kernel(const int32_t* __restrict
           make_int4(s0 + 0 < n ? t[it].x : -1, s0 + 1 < n ? t[it].y : -1,
                     s0 + 2 < n ? t[it].z : -1, s0 + 3 < n ? t[it].w : -1);
     }
-    // lane o reports sequence base + o, whose row was loaded in pass o / 4 by
-    // lanes 8 * (o % 4) ..
+    // lane o < VERIFY_ROWS_PER_WARP reports sequence base + o, whose row was
+    // loaded in pass o / 4 by lanes 8 * (o % 4) ..
     const int Lo = __shfl_sync(0xffffffffu, L, (lane & 3) * 8);
     if ((lane >> 2) == it) my_len = Lo;
   }
   const int row = base + lane;
-  if (row < B) {
+  if (lane < VERIFY_ROWS_PER_WARP && row < B) {
     const int n = min(my_len + 1, 32);
     accept_len[row] = my_len;
     n_commit[row] = n;
@@ -370,8 +374,10 @@ ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, i
                                   int32_t* kv_len, cudaStream_t stream) {
   if (B == 0) return NDIFF_OK;
   if (T == 32 && aligned16(draft) && aligned16(target) && aligned16(commit)) {
-    NDIFF_CUDA_TRY(launch_k(verify32_kernel, dim3((B + 127) / 128), dim3(128), 0, stream, draft,
-                            target, B, accept_len, commit, n_commit, kv_len));
+    const int rows_per_cta = 4 * VERIFY_ROWS_PER_WARP;
+    NDIFF_CUDA_TRY(launch_k(verify32_kernel, dim3((B + rows_per_cta - 1) / rows_per_cta),
+                            dim3(128), 0, stream, draft, target, B, accept_len, commit, n_commit,
+                            kv_len));
     return NDIFF_OK;
   }
   NDIFF_CUDA_TRY(launch_k(verify_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, draft, target, B,
