@@ -25,11 +25,14 @@ def visible_count(P: int, T: int, i: int, mode: int) -> int:
     return P + (i + 1 if mode == CAUSAL else T)
 
 
-def block_attn(q, k_cache, v_cache, kv_len, mode: int, scale: float) -> np.ndarray:
+def block_attn(q, k_cache, v_cache, kv_len, mode: int, scale: float, perturb_p=None) -> np.ndarray:
     """q [B][T][Hq][D]; k_cache, v_cache [B][Hkv][Lmax][D]; kv_len [B].
 
     out[b][i][h] = sum_j p_j v[b][g][j] with p = softmax(scale * q.k_j) over the
     visible keys j of slot i, g = h // (Hq/Hkv). Returns float64 [B][T][Hq][D].
+    perturb_p (None for the definition): a function applied to each row's
+    probabilities before the product with V, used only by the perturbation
+    analysis that derives the bf16 model's tolerance (oracle.model.Perturbation).
     """
     q = np.asarray(q, dtype=np.float64)
     k_cache = np.asarray(k_cache, dtype=np.float64)
@@ -50,6 +53,8 @@ def block_attn(q, k_cache, v_cache, kv_len, mode: int, scale: float) -> np.ndarr
                 s = scale * (keys @ q[b, i, h])    # [n]
                 p = np.exp(s - s.max())
                 p /= p.sum()
+                if perturb_p is not None:
+                    p = perturb_p(p)
                 out[b, i, h] = p @ vals
     return out
 
