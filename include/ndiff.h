@@ -32,9 +32,10 @@
  *   - Device pointers are raw CUDA device addresses owned by the caller; the
  *     library never frees them and never allocates on the kernel entry points.
  *     Work is enqueued asynchronously on the caller's stream (0 = legacy stream).
- *   - Errors found by a kernel (a bounded wait that expired) are recorded in a
- *     device status word and reported by ndiff_check() (which synchronises the
- *     stream) as NDIFF_ERR_TIMEOUT.
+ *   - Errors found by a kernel are recorded in a device status word and
+ *     reported by ndiff_check() (which synchronises the stream): a bounded wait
+ *     that expired as NDIFF_ERR_TIMEOUT, a device-side input outside its range
+ *     (a kv_len the host cannot see) as NDIFF_ERR_INVALID_ARG.
  *   - The model handle (ndiff_model_*) is the one exception to caller
  *     ownership: it owns its weights, KV cache and scratch.
  */
@@ -86,7 +87,9 @@ NDIFF_API const char* ndiff_status_string(ndiff_status s);
 
 /* Reads back and clears the device status word after synchronising `stream`.
  * Returns NDIFF_ERR_TIMEOUT if any kernel recorded an expired wait since the
- * last check, NDIFF_ERR_CUDA on a CUDA error, else NDIFF_OK. */
+ * last check, NDIFF_ERR_INVALID_ARG if a kernel read a device-side input
+ * outside its documented range (a kv_len outside [0, Lmax - T], a token id
+ * outside [0, vocab)), NDIFF_ERR_CUDA on a CUDA error, else NDIFF_OK. */
 NDIFF_API ndiff_status ndiff_check(cudaStream_t stream);
 
 /* Failure-path self-test (a library facility; the pages have no counterpart):
@@ -119,8 +122,11 @@ NDIFF_API ndiff_status ndiff_selftest_timeout(int limit_us, cudaStream_t stream)
  * ws/ws_bytes: device scratch of at least ndiff_block_attn_workspace_size()
  *   bytes (may be NULL when that size is 0). Contents need no initialisation.
  * Values stored in the cache at positions >= kv_len[b] + T are never used
- * (they may hold anything, including NaN). kv_len values outside the range
- * above are clamped on the device.
+ * (they may hold anything, including NaN). A kv_len outside the range above
+ * is an error that only the device sees: the kernels record it in the device
+ * status word (the next ndiff_check() returns NDIFF_ERR_INVALID_ARG) and clamp
+ * it only to keep every access inside the cache; the output of that call is
+ * then meaningless.
  * ------------------------------------------------------------------------ */
 NDIFF_API ndiff_status ndiff_block_attn(ndiff_dtype dt, const void* q, const void* k_cache,
                               const void* v_cache, const int32_t* kv_len, int B, int T,
@@ -149,8 +155,10 @@ NDIFF_API size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, in
  * a static array inside the library of NDIFF_NOALLOC_SCRATCH_BYTES per GPU,
  * held until the process exits; nothing is allocated. Shapes whose
  * ndiff_block_attn_workspace_size() exceeds that size are rejected with
- * NDIFF_ERR_WORKSPACE. The first call on a device looks up the array's device
- * address and should come before any stream capture. All calls share the one
+ * NDIFF_ERR_WORKSPACE; argument errors are reported first, as by
+ * ndiff_block_attn. The first call on a device looks up the array's device
+ * address (again whenever the current CUDA context has changed, e.g. after a
+ * cudaDeviceReset) and should come before any stream capture. All calls share the one
  * array: calls whose kernels overlap on the GPU race and must be serialised by
  * the caller. The array keeps what the previous call left in it; nothing in
  * it has to start at zero, because each call writes every partial result

@@ -16,6 +16,7 @@ thread_local bool g_pdl = false;
 __device__ unsigned int g_status_word;
 
 struct DeviceCache {
+  void* ctx = nullptr;            // the context the addresses below belong to
   unsigned int* status = nullptr;
   int sms = 0;
 };
@@ -41,17 +42,39 @@ ndiff_status cuda_error(cudaError_t e, const char* what) {
   return set_error(NDIFF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+void* current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// The status word's address and the SM count of the current device, looked
+// up again whenever the current context is not the one they were taken in.
 static DeviceCache* dev_cache() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceCache& c = g_dev[dev];
-  if (c.status == nullptr) {
+  void* ctx = current_context();
+  if (c.status == nullptr || ctx == nullptr || ctx != c.ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) c.status = (unsigned int*)p;
+    c.status = cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess ? (unsigned int*)p : nullptr;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     c.sms = sms > 0 ? sms : 148;
+    c.ctx = current_context();  // the lookup above makes the primary context current
   }
   return &c;
 }
@@ -135,6 +158,11 @@ ndiff_status ndiff_check(cudaStream_t stream) {
     NDIFF_CUDA_TRY(cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice));
     if (v & kStatusTimeout)
       return set_error(NDIFF_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", v);
+    if (v & kStatusBadInput)
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "a kernel read an input outside its range: kv_len outside [0, Lmax - T] or "
+                       "a token id outside [0, V) (status 0x%x)",
+                       v);
   }
   return NDIFF_OK;
 }
@@ -163,9 +191,11 @@ __global__ void selftest_timeout_kernel(unsigned long long limit_ns, unsigned in
 }
 }  // namespace
 
-static ndiff_status check_attn_args(ndiff_dtype dt, const void* q, const void* k, const void* v,
-                                    const int32_t* kv_len, int B, int T, int Hq, int Hkv, int D,
-                                    int Lmax, ndiff_mask mode, const void* out) {
+extern "C++" {
+namespace ndiff {
+ndiff_status check_block_attn_args(ndiff_dtype dt, const void* q, const void* k, const void* v,
+                                   const int32_t* kv_len, int B, int T, int Hq, int Hkv, int D,
+                                   int Lmax, ndiff_mask mode, const void* out) {
   if (dt != NDIFF_BF16 && dt != NDIFF_F32)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_block_attn: bad dtype %d", (int)dt);
   if (mode != NDIFF_BIDIR && mode != NDIFF_CAUSAL)
@@ -195,6 +225,8 @@ static ndiff_status check_attn_args(ndiff_dtype dt, const void* q, const void* k
   }
   return NDIFF_OK;
 }
+}  // namespace ndiff
+}  // extern "C++"
 
 size_t ndiff_block_attn_split_workspace_size(ndiff_dtype dt, int B, int T, int Hq, int Hkv, int D,
                                              int Lmax, int split_keys) {
@@ -213,7 +245,7 @@ ndiff_status ndiff_block_attn_split(ndiff_dtype dt, const void* q, const void* k
                                     int Hq, int Hkv, int D, int Lmax, ndiff_mask mode,
                                     float scale, int split_keys, void* out, void* ws,
                                     size_t ws_bytes, cudaStream_t stream) {
-  ndiff_status s = check_attn_args(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lmax, mode, out);
+  ndiff_status s = check_block_attn_args(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lmax, mode, out);
   if (s != NDIFF_OK) return s;
   if (split_keys < 0 || split_keys % 64 != 0)
     return set_error(NDIFF_ERR_INVALID_ARG,

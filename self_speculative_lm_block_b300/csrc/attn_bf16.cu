@@ -155,8 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     b = item / p.nsplit_max;
     s_idx = item % p.nsplit_max;
   }
-  int P = p.kv_len[b];
-  P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+  const int P = checked_prefix(p.kv_len[b], p.Lmax - p.T, p.status);
   const int nkeys = P + p.T;
   const int k_begin = s_idx * p.split;
   if (k_begin >= nkeys) return;  // this split is past the sequence (uniform per CTA)
@@ -508,8 +507,7 @@ __global__ void __launch_bounds__(128)
   griddep_launch();
   griddep_wait();
   if (r >= p.G * p.T) return;
-  int P = p.kv_len[b];
-  P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+  const int P = checked_prefix(p.kv_len[b], p.Lmax - p.T, nullptr);  // reported by the main kernel
   const int nkeys = P + p.T;
   const int ns = (nkeys + p.split - 1) / p.split;
   if (ns <= 1) return;  // written directly by the main kernel
@@ -554,8 +552,7 @@ constexpr int PLAN_BUCKETS = 4096;
 __device__ __forceinline__ int plan_key(const int32_t* kv_len, int it, int T, int Lmax, int split,
                                         int nsplit, int nb) {
   const int b = it / nsplit, s = it % nsplit;
-  int P = kv_len[b];
-  P = P < 0 ? 0 : (P > Lmax - T ? Lmax - T : P);
+  const int P = checked_prefix(kv_len[b], Lmax - T, nullptr);  // reported by the attention kernel
   int len = P + T - s * split;
   if (len <= 0) return 0;
   len = len < split ? len : split;

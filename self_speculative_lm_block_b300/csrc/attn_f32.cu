@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
                                                        const int32_t* __restrict__ kv_len, int B,
                                                        int T, int Hq, int Hkv, int D, int Lmax,
                                                        int causal, float scale,
-                                                       float* __restrict__ out) {
+                                                       float* __restrict__ out,
+                                                       unsigned int* __restrict__ status) {
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * T * Hq) return;
@@ -29,8 +30,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float* __restrict__
   const int t = (row / Hq) % T;
   const int b = row / (Hq * T);
   const int g = h / (Hq / Hkv);
-  int P = kv_len[b];
-  P = P < 0 ? 0 : (P > Lmax - T ? Lmax - T : P);
+  const int P = checked_prefix(kv_len[b], Lmax - T, status);
   const int nvis = P + (causal ? t + 1 : T);
   const float* qr = q + (size_t)row * D;
   const float* kb = kc + ((size_t)b * Hkv + g) * Lmax * D;
@@ -84,7 +84,8 @@ ndiff_status launch_attn_f32(const float* q, const float* k, const float* v,
   const long long rows = (long long)B * T * Hq;
   if (rows == 0) return NDIFF_OK;
   attn_f32_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(q, k, v, kv_len, B, T, Hq, Hkv,
-                                                                   D, Lmax, causal, scale, out);
+                                                                   D, Lmax, causal, scale, out,
+                                                                   device_status_word());
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
 }

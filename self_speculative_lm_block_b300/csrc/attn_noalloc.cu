@@ -11,13 +11,15 @@
 // the library is loaded on that GPU until the process exits). It performs no
 // allocation of any kind.
 //
-// Set-up: the device address of the array is looked up once per device, by the
-// first call made while that device is current; that first call should come
-// before any stream capture. Every call shares the one array, so calls whose
-// kernels overlap on the GPU (for instance on two streams) race on it and must
-// be serialised by the caller. The array keeps whatever the last call left in
-// it; nothing needs to start at zero, because every partial result the merge
-// step reads was written earlier by the same call.
+// Set-up: the device address of the array is looked up by the first call made
+// while a device is current, and again whenever the current CUDA context is no
+// longer the one it was taken in (after a cudaDeviceReset, or under a context
+// the caller made current); that first call should come before any stream
+// capture. Every call shares the one array, so calls whose kernels overlap on
+// the GPU (for instance on two streams) race on it and must be serialised by
+// the caller. The array keeps whatever the last call left in it; nothing needs
+// to start at zero, because every partial result the merge step reads was
+// written earlier by the same call.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,10 +31,14 @@ constexpr size_t kNoallocScratchBytes = NDIFF_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-void* g_scratch_ptr[64] = {nullptr};
+struct ScratchAddr {
+  void* ctx = nullptr;   // context the address was looked up in
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch[64];
 std::mutex g_scratch_mu;
 
-// Device address of g_noalloc_scratch on the current device (host code must
+// Device address of g_noalloc_scratch in the current context (host code must
 // not pass the symbol itself to a kernel: on the host it names a stand-in).
 ndiff_status scratch_address(void** out) {
   int dev = 0;
@@ -41,13 +47,19 @@ ndiff_status scratch_address(void** out) {
   if (dev < 0 || dev >= 64)
     return ndiff::set_error(NDIFF_ERR_UNSUPPORTED, "ndiff_block_attn_noalloc: device %d", dev);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchAddr& a = g_scratch[dev];
+  void* ctx = ndiff::current_context();
+  if (a.ptr == nullptr || ctx == nullptr || ctx != a.ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return ndiff::cuda_error(e, "cudaGetSymbolAddress(scratch)");
-    g_scratch_ptr[dev] = p;
+    if (e != cudaSuccess) {
+      a.ptr = nullptr;
+      return ndiff::cuda_error(e, "cudaGetSymbolAddress(scratch)");
+    }
+    a.ptr = p;
+    a.ctx = ndiff::current_context();
   }
-  *out = g_scratch_ptr[dev];
+  *out = a.ptr;
   return NDIFF_OK;
 }
 
@@ -58,6 +70,10 @@ extern "C" ndiff_status ndiff_block_attn_noalloc(ndiff_dtype dt, const void* q,
                                                  const int32_t* kv_len, int B, int T, int Hq,
                                                  int Hkv, int D, int Lmax, ndiff_mask mode,
                                                  float scale, void* out, cudaStream_t stream) {
+  // the same argument errors as ndiff_block_attn, reported before the size check
+  ndiff_status s = ndiff::check_block_attn_args(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D,
+                                                Lmax, mode, out);
+  if (s != NDIFF_OK) return s;
   const size_t need = ndiff_block_attn_workspace_size(dt, B, T, Hq, Hkv, D, Lmax);
   if (need > kNoallocScratchBytes)
     return ndiff::set_error(NDIFF_ERR_WORKSPACE,
@@ -66,7 +82,7 @@ extern "C" ndiff_status ndiff_block_attn_noalloc(ndiff_dtype dt, const void* q,
                             need, kNoallocScratchBytes);
   void* ws = nullptr;
   if (need > 0) {
-    ndiff_status s = scratch_address(&ws);
+    s = scratch_address(&ws);
     if (s != NDIFF_OK) return s;
   }
   return ndiff_block_attn(dt, q, k_cache, v_cache, kv_len, B, T, Hq, Hkv, D, Lmax, mode, scale,

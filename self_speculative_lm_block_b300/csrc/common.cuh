@@ -24,6 +24,10 @@ int num_sms();
 unsigned int* device_status_word();
 
 constexpr unsigned int kStatusTimeout = 1u;
+// A device-side input outside its documented range (a kv_len outside
+// [0, Lmax - T], a token id outside [0, V)): ndiff_check() returns
+// NDIFF_ERR_INVALID_ARG.
+constexpr unsigned int kStatusBadInput = 2u;
 
 // Expiry of bounded device waits, in nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -142,6 +146,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
       }
     }
   }
+}
+
+// A committed prefix length read on the device. A value outside [0, hi] is
+// recorded in the status word (the next ndiff_check() returns
+// NDIFF_ERR_INVALID_ARG) and clamped only so that every cache access stays in
+// bounds; the results of that launch are then meaningless.
+__device__ __forceinline__ int checked_prefix(int P, int hi, unsigned int* status) {
+  if (P < 0 || P > hi) {
+    if (status != nullptr) atomicOr(status, kStatusBadInput);
+    P = P < 0 ? 0 : hi;
+  }
+  return P;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -144,8 +144,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, f
     case GEMM_EPI_QKV: {
       // tile = one head: q heads, then k heads, then v heads. In q and k heads
       // even rows hold dim i = r/2 and odd rows dim i + 64 (the RoPE pair).
-      int P = p.kv_len[0];
-      P = P < 0 ? 0 : (P > p.Lmax - p.T ? p.Lmax - p.T : P);
+      const int P = checked_prefix(p.kv_len[0], p.Lmax - p.T, p.status);
       const int h = tile;
       const bool rot = h < p.Hq + p.Hkv;
       const int i = r >> 1;

@@ -152,8 +152,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, i
         const int m = m0 + j;
         if (m >= p.T) continue;
         const int b = m / p.Tb, slot = m - b * p.Tb;
-        int P = __ldg(p.kv_len + b);
-        P = P < 0 ? 0 : (P > p.Lmax - p.Tb ? p.Lmax - p.Tb : P);
+        const int P = checked_prefix(__ldg(p.kv_len + b), p.Lmax - p.Tb, p.status);
         const int pos = P + slot;
         float y = v[j];
         if (rot) {

@@ -12,6 +12,15 @@
 
 namespace ndiff {
 
+// api.cu: the argument checks of ndiff_block_attn (every entry point of block
+// attention runs them before anything else), and the CUDA context current on
+// the calling thread (nullptr if none), which keys the caches of device
+// addresses: a cudaDeviceReset or another context makes a cached address stale.
+ndiff_status check_block_attn_args(ndiff_dtype dt, const void* q, const void* k, const void* v,
+                                   const int32_t* kv_len, int B, int T, int Hq, int Hkv, int D,
+                                   int Lmax, ndiff_mask mode, const void* out);
+void* current_context();
+
 // attn_bf16.cu
 int attn_bf16_auto_split(int B, int Hkv, int Lmax);
 size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split);

@@ -455,7 +455,10 @@ ndiff_status finish(cudaStream_t s) {
     if (v) {
       unsigned int z = 0;
       NDIFF_CUDA_TRY(cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice));
-      return set_error(NDIFF_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", v);
+      if (v & kStatusTimeout)
+        return set_error(NDIFF_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", v);
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "a kernel read an input outside its range (status 0x%x)", v);
     }
   }
   return NDIFF_OK;

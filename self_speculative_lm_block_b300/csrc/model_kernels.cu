@@ -128,12 +128,16 @@ __global__ void rope_table_kernel(float2* tab, int Lmax, int D, double base) {
 
 // ---------------------------------------------------------------- activations
 template <bool BF16>
-__global__ void embed_kernel(const void* E, const int32_t* ids, int V, int d, float* x) {
+__global__ void embed_kernel(const void* E, const int32_t* ids, int V, int d, float* x,
+                             unsigned int* status) {
   griddep_launch();
   griddep_wait();
   const int m = blockIdx.x;
   int id = ids[m];
-  id = id < 0 ? 0 : (id >= V ? V - 1 : id);
+  if (id < 0 || id >= V) {  // reported, and clamped only to keep the read in bounds
+    if (threadIdx.x == 0 && status != nullptr) atomicOr(status, kStatusBadInput);
+    id = id < 0 ? 0 : V - 1;
+  }
   for (int k = threadIdx.x; k < d; k += blockDim.x) {
     const size_t at = (size_t)id * d + k;
     x[(size_t)m * d + k] = BF16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(E)[at])
@@ -196,15 +200,14 @@ __global__ void __launch_bounds__(256) linear_f32_kernel(const float* x, int ldx
 // k and v to the caches [Hkv][Lmax][D] at positions P + m.
 __global__ void qkv_rope_f32_kernel(const float* y, int T, int Hq, int Hkv, int D, int Lmax,
                                     const int32_t* kv_len, const float2* rope, float* qb,
-                                    float* kc, float* vc) {
+                                    float* kc, float* vc, unsigned int* status) {
   griddep_launch();
   griddep_wait();
   const int Ntot = (Hq + 2 * Hkv) * D;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= T * Ntot) return;
   const int m = e / Ntot, c = e % Ntot, h = c / D, d = c % D, half = D / 2;
-  int P = kv_len[0];
-  P = P < 0 ? 0 : (P > Lmax - T ? Lmax - T : P);
+  const int P = checked_prefix(kv_len[0], Lmax - T, status);
   const float* yr = y + (size_t)m * Ntot + (size_t)h * D;
   float v = yr[d];
   if (h < Hq + Hkv) {
@@ -348,9 +351,11 @@ ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaSt
 ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
                           float* x, cudaStream_t s) {
   if (bf16)
-    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<true>, dim3(T), dim3(256), 0, s, E, ids, V, d, x));
+    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<true>, dim3(T), dim3(256), 0, s, E, ids, V, d, x,
+                            device_status_word()));
   else
-    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<false>, dim3(T), dim3(256), 0, s, E, ids, V, d, x));
+    NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<false>, dim3(T), dim3(256), 0, s, E, ids, V, d, x,
+                            device_status_word()));
   return NDIFF_OK;
 }
 
@@ -376,7 +381,7 @@ ndiff_status launch_qkv_rope_f32(const float* y, int T, int Hq, int Hkv, int D, 
                                  float* vc, cudaStream_t s) {
   const int n = T * (Hq + 2 * Hkv) * D;
   mk::qkv_rope_f32_kernel<<<(n + 255) / 256, 256, 0, s>>>(y, T, Hq, Hkv, D, Lmax, kv_len, rope,
-                                                          qb, kc, vc);
+                                                          qb, kc, vc, device_status_word());
   NDIFF_CUDA_TRY(cudaGetLastError());
   return NDIFF_OK;
 }

@@ -103,3 +103,26 @@ def test_workspace_sizes(nd):
     w = nd.ndiff_block_attn_split_workspace_size(nd.NDIFF_BF16, 2, 32, 32, 8, 128, 512, 128)
     assert w == 2 * 8 * 4 * 128 * (128 * 4 + 8) + 256
     assert nd.ndiff_block_attn_workspace_size(nd.NDIFF_F32, 2, 32, 4, 4, 32, 512) == 0
+
+
+def test_noalloc_reports_argument_errors_before_the_scratch_limit(nd):
+    """A shape too large for the built-in scratch with a bad argument reports
+    the argument error (as ndiff_block_attn would), not NDIFF_ERR_WORKSPACE;
+    with valid arguments it reports NDIFF_ERR_WORKSPACE. All on the host."""
+    B, T, Hq, Hkv, D, Lmax = 64, 32, 32, 8, 128, 32800
+    assert nd.ndiff_block_attn_workspace_size(nd.NDIFF_BF16, B, T, Hq, Hkv, D, Lmax) > \
+        nd.NDIFF_NOALLOC_SCRATCH_BYTES
+    bad = [
+        (dict(Hq=30), nd.NDIFF_ERR_INVALID_ARG),          # Hq % Hkv != 0
+        (dict(mode=7), nd.NDIFF_ERR_INVALID_ARG),         # bad mask mode
+        (dict(dt=5), nd.NDIFF_ERR_INVALID_ARG),           # bad dtype
+        (dict(q=17), nd.NDIFF_ERR_INVALID_ARG),           # misaligned bf16 pointer
+        (dict(T=64), nd.NDIFF_ERR_UNSUPPORTED),           # G * T = 256 > 128
+    ]
+    for change, want in bad + [({}, nd.NDIFF_ERR_WORKSPACE)]:
+        a = dict(dt=nd.NDIFF_BF16, q=16, B=B, T=T, Hq=Hq, mode=0)
+        a.update(change)
+        with pytest.raises(nd.NdiffError) as e:
+            nd.ndiff_block_attn_noalloc(a["dt"], a["q"], 16, 16, 16, a["B"], a["T"], a["Hq"], Hkv, D, Lmax,
+                                        a["mode"], 0.1, 16, stream=0)
+        assert e.value.status == want, (change, e.value.status)
