@@ -303,13 +303,34 @@ class AttnWorkload:
         return nbytes / dt / 1e9, desc, dt
 
 
-def _oracle_threads():
+def host_cpu():
+    """The host the oracle is timed on: its CPU model (from /proc/cpuinfo) and
+    the number of cores this process may run on (nproc)."""
+    model = "unknown"
     try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        return max([i.get("num_threads", 1) for i in info] or [1])
-    except Exception:
-        return os.cpu_count()
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        nproc = os.cpu_count()
+    return {"model": model, "nproc": nproc}
+
+
+def oracle_sample_1thread(wl):
+    """The oracle's sample timed on one core: NumPy's BLAS and OpenMP pools
+    limited to one thread for the duration (the plain single-threaded CPU
+    baseline). Returns (GB/s, description, seconds, threads used)."""
+    import threadpoolctl
+    with threadpoolctl.threadpool_limits(limits=1):
+        used = max([i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()] or [1])
+        v, desc, dt = wl.oracle_sample()
+    return v, desc, dt, used
 
 
 def weight_bytes_8b(c):
@@ -586,7 +607,7 @@ def run_reference(args, rank, world):
     wl = AttnWorkload(args.workload, 0, host_only=True)
     vals, secs, desc = [], [], ""
     for i in range(args.warmup + args.steps):
-        v, desc, dt = wl.oracle_sample()
+        v, desc, dt, threads = oracle_sample_1thread(wl)
         if i >= args.warmup:
             vals.append(v)
             secs.append(dt)
@@ -595,8 +616,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(secs)) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": wl.config(),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": _oracle_threads(),
-                             "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": desc, "host": host_cpu()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -757,9 +778,10 @@ def main():
         if batched is not None:
             out["model_8b_batched"] = batched
         if not args.no_cpu_baseline:
-            cv, desc, dt = wl.oracle_sample()
-            out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": _oracle_threads(),
-                                   "kind": "oracle", "sample": desc, "seconds": dt}
+            cv, desc, dt, threads = oracle_sample_1thread(wl)
+            out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": threads,
+                                   "kind": "oracle", "sample": desc, "seconds": dt,
+                                   "host": host_cpu()}
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

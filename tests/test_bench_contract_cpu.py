@@ -22,7 +22,8 @@ def _check_line(out: str, n: int):
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "attn-batched"
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"] and cb["value"] == d["value"]
+    assert cb["host"]["nproc"] >= 1 and cb["host"]["model"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
