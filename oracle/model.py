@@ -33,6 +33,16 @@ Readings where the pages are silent (each is listed in the design notes):
   committed; when all 32 drafts were accepted, the second half's argmaxes are
   the next block's draft, otherwise the next cycle drafts afresh (one BIDIR
   forward). Each fused forward counts as one forward.
+- Quadratic self-speculation (same page and table: 6.4x against linear 6x)
+  is read as drafting the next block, in the verifying forward, for more than
+  the one acceptance length the linear variant assumes: for L = 32 as above,
+  and for each candidate length L < 32 in a given set, a block of 32 [MASK]
+  inputs at positions P+L+1 .. P+L+32 over the prefix plus the verified
+  block's first L+1 inputs (the state after committing L drafts and the
+  correction; the correction itself is not known inside the forward, so its
+  slot stays masked). If the verified L is 32 or a candidate, that block's
+  argmaxes are the next draft, else the next cycle drafts afresh. The whole
+  forward counts as one.
 - Threshold sampler (either mode): BIDIR drafting rounds until no slot is
   masked, each fixing the masked slots whose confidence reaches tau (else the
   most confident one) after revising earlier slots (oracle.decode.
@@ -316,10 +326,60 @@ class Session:
         self.pending_draft = nxt if int(L[0]) == BLOCK else None
         return out
 
-    def generate(self, mode: str, n_new: int, steps: int = 1, tau=None) -> list[int]:
+    def step_selfspec_quadratic(self, cands) -> list[int]:
+        """One cycle of quadratic self-speculation with candidate acceptance
+        lengths `cands` (each in [0, 32), besides 32 itself)."""
+        P = self.kv_len
+        d = self.pending_draft
+        if d is None:
+            d = self.draft(1)
+        blk = [self.last] + [int(t) for t in d[:BLOCK - 1]]
+        a = self._argmax(self.forward(blk, attention.CAUSAL))[0]       # writes KV of [P, P+32)
+        # the candidate blocks overwrite cache rows past their own prefix;
+        # every one of them starts from the verified block's K/V
+        saved = [(k[:, P:].copy(), v[:, P:].copy()) for k, v in zip(self.k, self.v)]
+
+        def restore():
+            for (k0, v0), k, v in zip(saved, self.k, self.v):
+                k[:, P:] = k0
+                v[:, P:] = v0
+
+        mask = self.cfg.mask_id
+        nxt = {}
+        self.kv_len = P + BLOCK
+        nxt[BLOCK] = self._argmax(self.forward([int(d[BLOCK - 1])] + [mask] * (BLOCK - 1),
+                                               attention.BIDIR))[0]
+        for Lc in sorted(set(int(c) for c in cands)):
+            assert 0 <= Lc < BLOCK
+            restore()
+            self.kv_len = P + Lc + 1
+            nxt[Lc] = self._argmax(self.forward([mask] * BLOCK, attention.BIDIR))[0]
+        restore()
+        self.kv_len = P
+        self.forwards -= len(nxt)               # verification and all drafts are one forward
+        L, commit, n, _ = decode.verify_accept(np.asarray(d)[None], a[None])
+        n0, L0 = int(n[0]), int(L[0])
+        self.accept_lens.append(L0)
+        self.kv_len += n0
+        out = [int(t) for t in commit[0, :n0]]
+        self.last = out[-1]
+        self.tokens.extend(out)
+        self.pending_draft = nxt.get(L0)
+        return out
+
+    def draft_masked(self) -> np.ndarray:
+        """The draft a quadratic candidate block gives from the current state:
+        the argmaxes of one BIDIR forward of 32 [MASK] inputs, the pending
+        token's slot included."""
+        logits = self.forward([self.cfg.mask_id] * BLOCK, attention.BIDIR)
+        self.forwards -= 1
+        return self._argmax(logits)[0]
+
+    def generate(self, mode: str, n_new: int, steps: int = 1, tau=None, cands=(0, 1)) -> list[int]:
         """Decode until n_new tokens (extra committed tokens are cut). `tau`:
         None for the top-k draft of `steps` rounds, or (tau, tau_revise) for
-        the threshold sampler."""
+        the threshold sampler. `cands`: the candidate acceptance lengths of
+        quadratic self-speculation."""
         while len(self.tokens) < n_new:
             if mode == "ar":
                 self.step_ar()
@@ -329,6 +389,8 @@ class Session:
                 self.step_selfspec(steps, tau)
             elif mode == "selfspec-fused":
                 self.step_selfspec_fused()
+            elif mode == "selfspec-quad":
+                self.step_selfspec_quadratic(cands)
             else:
                 raise ValueError(mode)
         return self.tokens[:n_new]

@@ -211,3 +211,60 @@ def test_fused_next_draft_is_the_draft_of_the_new_state():
     assert f.tokens[:160] == ar
     assert 32 in f.accept_lens and min(f.accept_lens) < 32
     assert checked >= 1
+
+
+# ---------------------------------------------------------------- quadratic self-speculation
+@pytest.mark.parametrize("cands", [(0, 1), (0, 5, 31), ()])
+def test_quadratic_selfspec_equals_ar(cands):
+    cfg = tiny_cfg()
+    w = model.Weights(cfg)
+    pr = synth.prompt(32, cfg.vocab, cfg.seed)
+    s = model.Session(cfg, w, max_seq=400); s.prefill(pr)
+    ar = s.generate("ar", 64)
+    q = model.Session(cfg, w, max_seq=400); q.prefill(pr)
+    assert q.generate("selfspec-quad", 64, cands=cands) == ar
+
+
+def test_quadratic_with_every_candidate_drafts_once():
+    """Candidates 0..31 plus full acceptance cover every outcome, so only the
+    first cycle runs a drafting forward: forwards = cycles + 1."""
+    cfg = _cfg_vocab(8, seed=11)
+    w = model.Weights(cfg)
+    pr = [int(x) for x in synth.prompt(24, cfg.vocab, 5)]
+    s = model.Session(cfg, w, max_seq=900); s.prefill(pr)
+    ar = s.generate("ar", 96)
+    q = model.Session(cfg, w, max_seq=900); q.prefill(pr)
+    assert q.generate("selfspec-quad", 96, cands=tuple(range(32))) == ar
+    assert q.forwards == len(q.accept_lens) + 1
+    assert min(q.accept_lens) < 32
+
+
+def test_quadratic_full_acceptance_is_linear():
+    """Two ids: every draft is accepted; the quadratic mode then behaves as the
+    linear one (one drafting forward, one forward per block)."""
+    cfg = _cfg_vocab(2)
+    w = model.Weights(cfg)
+    s = model.Session(cfg, w, max_seq=400); s.prefill([0] * 20)
+    assert s.generate("selfspec-quad", 96, cands=(0, 3)) == [0] * 96
+    assert s.forwards == 1 + 3 and s.accept_lens == [32, 32, 32]
+
+
+def test_quadratic_candidate_draft_is_the_masked_draft_of_the_new_state():
+    """After a cycle whose acceptance length L < 32 was a candidate, the draft
+    it leaves is the masked draft computed afresh from the committed tokens
+    (prefix length P + L + 1, the correction pending): the positions and the
+    prefix of every candidate block are those of the state it stands for."""
+    cfg = _cfg_vocab(8, seed=11)
+    w = model.Weights(cfg)
+    pr = [int(x) for x in synth.prompt(24, cfg.vocab, 5)]
+    q = model.Session(cfg, w, max_seq=900); q.prefill(pr)
+    checked = 0
+    while len(q.tokens) < 200 and checked < 4:
+        q.step_selfspec_quadratic(tuple(range(32)))
+        if q.pending_draft is not None and q.accept_lens[-1] < 32:
+            fresh = model.Session(cfg, w, max_seq=900)
+            fresh.prefill(pr + q.tokens)
+            assert fresh.kv_len == q.kv_len and fresh.last == q.last
+            assert np.array_equal(fresh.draft_masked(), q.pending_draft)
+            checked += 1
+    assert checked >= 2
