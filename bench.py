@@ -322,15 +322,33 @@ def host_cpu():
     return {"model": model, "nproc": nproc}
 
 
-def oracle_sample_1thread(wl):
-    """The oracle's sample timed on one core: NumPy's BLAS and OpenMP pools
-    limited to one thread for the duration (the plain single-threaded CPU
-    baseline). Returns (GB/s, description, seconds, threads used)."""
-    import threadpoolctl
-    with threadpoolctl.threadpool_limits(limits=1):
-        used = max([i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()] or [1])
-        v, desc, dt = wl.oracle_sample()
-    return v, desc, dt, used
+_ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                   "BLIS_NUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def oracle_sample_1thread(name):
+    """The oracle's sample of workload `name` timed on one core (the plain
+    single-threaded CPU baseline): NumPy's BLAS and OpenMP pools limited to
+    one thread, by threadpoolctl where it is installed, else in a child
+    process started with the thread-count variables set to 1 (the pools are
+    sized when NumPy loads). Returns (GB/s, description, seconds, threads)."""
+    try:
+        import threadpoolctl
+    except ImportError:
+        threadpoolctl = None
+    if threadpoolctl is not None:
+        wl = AttnWorkload(name, 0, host_only=True)
+        with threadpoolctl.threadpool_limits(limits=1):
+            used = max([i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()] or [1])
+            v, desc, dt = wl.oracle_sample()
+        return v, desc, dt, used
+    env = dict(os.environ, **_ONE_THREAD_ENV)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample-only",
+                        "--workload", name], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    return d["value"], d["sample"], d["seconds"], 1
 
 
 def weight_bytes_8b(c):
@@ -607,7 +625,7 @@ def run_reference(args, rank, world):
     wl = AttnWorkload(args.workload, 0, host_only=True)
     vals, secs, desc = [], [], ""
     for i in range(args.warmup + args.steps):
-        v, desc, dt, threads = oracle_sample_1thread(wl)
+        v, desc, dt, threads = oracle_sample_1thread(args.workload)
         if i >= args.warmup:
             vals.append(v)
             secs.append(dt)
@@ -668,8 +686,14 @@ def main():
                     help="sequences of the batched 8B-shaped decode (0: skip)")
     ap.add_argument("--batch-tokens", type=int, default=32,
                     help="tokens generated per sequence and mode by the batched decode")
+    ap.add_argument("--oracle-sample-only", action="store_true",
+                    help="(internal) print one oracle sample of --workload as JSON and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.oracle_sample_only:
+        v, desc, dt = AttnWorkload(args.workload, 0, host_only=True).oracle_sample()
+        print(json.dumps({"value": v, "sample": desc, "seconds": dt}), flush=True)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -778,7 +802,7 @@ def main():
         if batched is not None:
             out["model_8b_batched"] = batched
         if not args.no_cpu_baseline:
-            cv, desc, dt, threads = oracle_sample_1thread(wl)
+            cv, desc, dt, threads = oracle_sample_1thread(args.workload)
             out["cpu_baseline"] = {"value": cv, "unit": "GB/s", "cores": threads,
                                    "kind": "oracle", "sample": desc, "seconds": dt,
                                    "host": host_cpu()}
