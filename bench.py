@@ -365,7 +365,7 @@ def run_model(rank, n_tokens, steps=1):
     c = synth.MODEL_8B
     seed = c["seed"] + 1000 * rank
     m = nd.Model(c["layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
-                 c["vocab"], dtype="bf16", max_seq=c["prompt"] + n_tokens + 64, seed=seed)
+                 c["vocab"], dtype="bf16", max_seq=c["prompt"] + n_tokens + 512, seed=seed)
     prompt = synth.prompt(c["prompt"], c["vocab"], seed)
     out = {"model": "8B-shaped random init (36L, d4096, 32/8x128, ffn 12288, V151936, bf16)",
            "prompt": c["prompt"], "tokens": n_tokens}
@@ -389,6 +389,47 @@ def run_model(rank, n_tokens, steps=1):
             hist = [int(x) for x in st.accept_hist]
             out[name]["accept_len_hist"] = {str(i): v for i, v in enumerate(hist) if v}
             out[name]["draft_forwards_per_block"] = steps
+    # quadratic self-speculation: the verifying forward also drafts the next
+    # block for the two acceptance lengths below 32 that the linear run saw
+    # most often (ties: the shorter)
+    hist = out["selfspec"].get("accept_len_hist", {})
+    ranked = sorted(((-v, int(k)) for k, v in hist.items() if int(k) < 32))
+    cands = [k for _, k in ranked[:2]] or [0]
+    if len(cands) == 1:
+        cands.append(1 if cands[0] != 1 else 0)
+    m.prefill(prompt)
+    m.step(nd.NDIFF_MODE_SELFSPEC_QUAD, cands=cands)   # warm-up (graph capture)
+    m.prefill(prompt)
+    m.stats = nd.Stats()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    toks = m.generate(nd.NDIFF_MODE_SELFSPEC_QUAD, n_tokens, cands=cands)
+    dt = time.perf_counter() - t0
+    st = m.stats
+    qh = [int(x) for x in st.accept_hist]
+    out["selfspec_quadratic"] = {
+        "candidates": cands, "tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+        "tokens_per_forward": st.tokens / st.forwards, "ms_per_forward": dt * 1e3 / st.forwards,
+        "seconds": dt, "accept_len_hist": {str(i): v for i, v in enumerate(qh) if v},
+        "rows_per_forward": 128, "equals_ar": toks == res["ar"]}
+    # drafting forwards per block (steps S; each unmasks 32/S slots)
+    sweep = {}
+    for S in (2, 4):
+        ns = min(n_tokens, 64)
+        m.prefill(prompt)
+        m.step(nd.NDIFF_MODE_SELFSPEC, S)
+        m.prefill(prompt)
+        m.stats = nd.Stats()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        toks = m.generate(nd.NDIFF_MODE_SELFSPEC, ns, S)
+        dt = time.perf_counter() - t0
+        st = m.stats
+        sweep[str(S)] = {"tokens": ns, "tokens_per_s": st.tokens / dt, "forwards": int(st.forwards),
+                         "tokens_per_forward": st.tokens / st.forwards,
+                         "ms_per_forward": dt * 1e3 / st.forwards,
+                         "equals_ar": toks == res["ar"][:len(toks)]}
+    out["selfspec_steps_sweep"] = sweep
     # the threshold sampler's host-driven round loop (a 4-byte read between
     # rounds), at tau = 0: one drafting round per block, the same forwards as
     # the one-round top-k draft above, so the difference is the loop's cost
@@ -659,6 +700,39 @@ def job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
     return step_bytes * world / (ms_per_step * 1e-3) / 1e9
 
 
+def run_attn_alone(name, rank, steps, warmup):
+    """Block attention of workload `name` (attn-single: batch 1 x 4096 keys;
+    attn-long: batch 4 x 32768 keys) timed alone: CUDA-graph replays of its
+    launches on device-resident inputs, rotating over KV copies when one copy
+    would stay in L2. Returns its roofline block (achieved = algorithmic bytes
+    per launch / device time per launch)."""
+    import torch
+    wl = AttnWorkload(name, rank)
+    for _ in range(warmup):
+        wl.step(attn_only=True)
+    torch.cuda.synchronize()
+    g = capture(torch, lambda: wl.step(attn_only=True), wl.ncopy)
+    reps = max(2, (steps + wl.ncopy - 1) // wl.ncopy)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * wl.ncopy)
+    gbs = wl.attn_bytes / (ms * 1e-3) / 1e9
+    hbm, _, _, src = _peaks()
+    out = {"config": wl.config(), "kernel": "attn_bf16_kernel (+attn_combine_kernel)", "bound": "hbm",
+           "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "peak_source": src,
+           "frac_of_spec_8tbs": gbs / SPEC_HBM_GBS, "bytes_per_launch": wl.attn_bytes,
+           "ms_per_launch": ms, "traffic": ATTN_TRAFFIC.get(name), "launches": reps * wl.ncopy}
+    del wl, g
+    torch.cuda.empty_cache()
+    return out
+
+
 def capture(torch, fn, n):
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -764,6 +838,12 @@ def main():
     e2e_ms = reduce_over_ranks(f0.elapsed_time(f1), "max", world, "cuda") / n_e2e
     e2e_val = job_gbs(wl.step_bytes, world, e2e_ms)
 
+    # the other attention configurations (batch 1 x 4096, batch 4 x 32768)
+    extra_attn = {}
+    if args.workload == "attn-batched":
+        for nm in ("attn-single", "attn-long"):
+            extra_attn[nm.replace("-", "_")] = run_attn_alone(nm, rank, args.steps, args.warmup)
+
     model = run_model(rank, args.model_tokens) if args.model_tokens > 0 else None
     lm_head = run_lm_head() if args.model_tokens > 0 else None
     forced = run_forced_accept(rank) if args.model_tokens > 0 else None
@@ -792,6 +872,7 @@ def main():
                "gpu_launches": wl.launches * steps_done,
                "timing": "CUDA-graph replay of whole steps; attention timed by a graph of its launches",
                "clocks": clk.summary()}
+        out.update(extra_attn)
         if model is not None:
             out["model_8b"] = model
         if lm_head is not None:

@@ -79,7 +79,9 @@ typedef enum {
     NDIFF_MODE_AR = 0,
     NDIFF_MODE_DIFF = 1,
     NDIFF_MODE_SELFSPEC = 2,
-    NDIFF_MODE_SELFSPEC_FUSED = 3  /* verification of a block and the draft of the next in one forward */
+    NDIFF_MODE_SELFSPEC_FUSED = 3, /* verification of a block and the draft of the next in one forward */
+    NDIFF_MODE_SELFSPEC_QUAD = 4   /* verification of a block and drafts of the next for several
+                                      acceptance lengths in one forward */
 } ndiff_mode;
 
 NDIFF_API const char* ndiff_last_error(void);
@@ -366,6 +368,8 @@ typedef struct {
     int steps;          /* TOPK: 1 <= steps <= 32, 32 % steps == 0 */
     float tau;          /* THRESHOLD: fix threshold, 0 <= tau */
     float tau_revise;   /* THRESHOLD: revision threshold, 0 <= tau_revise (> 1: off) */
+    int n_cand;         /* SELFSPEC_QUAD: candidate acceptance lengths besides 32 (1 or 2) */
+    int cand[2];        /* SELFSPEC_QUAD: the candidates, each in [0, 32) */
 } ndiff_decode_opts;
 
 NDIFF_API ndiff_status ndiff_model_create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model** out);
@@ -395,6 +399,18 @@ NDIFF_API ndiff_status ndiff_prefill(ndiff_model* m, const int32_t* prompt_host,
  *             correction; when all 32 drafts were accepted, the second half's
  *             argmaxes are the next cycle's draft ([FFI] 吞吐量数据: linear
  *             self-speculation). Needs max_seq >= committed + 64.
+ *   SELFSPEC_QUAD (bf16, one sequence; ndiff_decode_step_ex with n_cand and
+ *             cand, ndiff_decode_step uses the candidates 0 and 1): as
+ *             SELFSPEC_FUSED, and the same forward also drafts the next block
+ *             for each candidate acceptance length L < 32: 32 [MASK] inputs
+ *             at positions P+L+1 .. P+L+32 (BIDIR) over the prefix plus the
+ *             verified block's first L+1 inputs (the state after committing L
+ *             drafts and the correction, whose slot stays masked because the
+ *             forward cannot know it). When the verified L is 32 or a
+ *             candidate, that block's argmaxes are the next cycle's draft
+ *             ([FFI] 吞吐量数据: quadratic self-speculation). 128 rows per
+ *             forward; needs max_seq >= committed + 448 (the candidate blocks'
+ *             K/V sit in cache rows past the verified block).
  * steps: drafting forwards per block (1 <= steps <= 32, 32 % steps == 0);
  *   ignored for AR and SELFSPEC_FUSED (one drafting forward).
  * out_tokens_host: host buffer of >= 32 int32; *n_out receives the count.
@@ -403,7 +419,8 @@ NDIFF_API ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int st
                                int32_t* out_tokens_host, int* n_out, ndiff_stats* stats,
                                cudaStream_t stream);
 
-/* ndiff_decode_step with a choice of draft sampler (see ndiff_decode_opts).
+/* ndiff_decode_step with a choice of draft sampler (see ndiff_decode_opts) and,
+ * for NDIFF_MODE_SELFSPEC_QUAD, of the candidate acceptance lengths.
  * With NDIFF_SAMPLER_THRESHOLD the rounds run one after another with a 4-byte
  * read of the block's mask word between them (the round count depends on the
  * model's confidence); every round and the final forward are CUDA graphs.

@@ -11,7 +11,8 @@ benchmark is bench.py and the parity tests are under tests/.
         12288, bf16), after a prefill. --layers 1 --vocab 4096 keeps one
         layer's projections at full width with a device footprint near 0.5 GB;
         --batch B decodes B sequences together (ragged prompts in
-        [prompt/2, prompt]) through the batch calls.
+        [prompt/2, prompt]) through the batch calls; --quad runs a quadratic
+        self-speculation cycle (candidates 0 and 1) instead of the linear one.
 
     python profile_workloads.py gemm [--rows 2048] [--n 6144] [--k 4096]
                                      [--lm-rows 32] [--vocab 151936]
@@ -41,7 +42,7 @@ from self_speculative_lm_block_b300 import synth  # noqa: E402
 def decode(args):
     c = synth.MODEL_8B
     m = nd.Model(args.layers, c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
-                 args.vocab, dtype="bf16", max_seq=args.prompt + 256, seed=c["seed"],
+                 args.vocab, dtype="bf16", max_seq=args.prompt + 512, seed=c["seed"],
                  batch=args.batch)
     if args.batch == 1:
         m.prefill(synth.prompt(args.prompt, args.vocab, c["seed"]))
@@ -52,7 +53,10 @@ def decode(args):
     torch.cuda.nvtx.range_push("decode")
     if args.batch == 1:
         m.step(nd.NDIFF_MODE_AR)
-        m.step(nd.NDIFF_MODE_SELFSPEC, args.steps)
+        if args.quad:
+            m.step(nd.NDIFF_MODE_SELFSPEC_QUAD, cands=(0, 1))
+        else:
+            m.step(nd.NDIFF_MODE_SELFSPEC, args.steps)
     else:
         m.step_batch(nd.NDIFF_MODE_AR)
         m.step_batch(nd.NDIFF_MODE_SELFSPEC, args.steps)
@@ -112,6 +116,7 @@ def main():
     d.add_argument("--prompt", type=int, default=c["prompt"])
     d.add_argument("--steps", type=int, default=1, help="drafting forwards per block")
     d.add_argument("--batch", type=int, default=1)
+    d.add_argument("--quad", action="store_true", help="a quadratic self-speculation cycle")
     g = sub.add_parser("gemm")
     g.add_argument("--rows", type=int, default=2048)
     g.add_argument("--n", type=int, default=6144)

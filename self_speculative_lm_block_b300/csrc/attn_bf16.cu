@@ -24,6 +24,13 @@
 //     and masked keys contribute exact zeros, so a row's result does not
 //     depend on T: a CAUSAL block of T rows reproduces T single-row calls.
 //   * Splits of one (b, g) are merged by attn_combine (log-sum-exp weights).
+//   * Remapped keys (the draft blocks of quadratic self-speculation): a
+//     sequence may read the cache of another (all candidate blocks share the
+//     verified sequence's cache) and may move its virtual keys from a
+//     64-aligned position x on to a 64-aligned scratch row S of that cache, so
+//     that a block can follow a prefix of any length without overwriting the
+//     cache rows past it. The rows [x, P) of the prefix that share x's tile are
+//     copied to S by the one CTA that reads that tile, before its loads.
 //   * Every mbarrier wait is bounded; on expiry the CTA records a timeout in
 //     the device status word, drains its TMA loads, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -68,10 +75,15 @@ struct Params {
   int split;          // keys per split (multiple of BN)
   int nsplit_max;     // splits per (b, g) in the grid
   __nv_bfloat16* out;
+  const __nv_bfloat16* kc;  // the caches (for the remapped-key copy)
+  const __nv_bfloat16* vc;
   float* ws_o;        // [B][Hkv][nsplit_max][128][128]
   float2* ws_ml;      // [B][Hkv][nsplit_max][128]
   const int32_t* order;  // [B * nsplit_max] items (b * nsplit_max + split), longest first;
                          // nullptr: the grid is (nsplit_max, Hkv, B) in natural order
+  const int4* remap;     // per sequence {x, S, cache index, 0}: virtual keys >= x sit at
+                         // cache rows S + (key - x) of that cache; nullptr: none
+  int ncache;            // caches behind k/v when remap is set
   unsigned int* status;
 };
 
@@ -156,6 +168,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     s_idx = item % p.nsplit_max;
   }
   const int P = checked_prefix(p.kv_len[b], p.Lmax - p.T, p.status);
+  int cb = b, rx = 0x7fffffff, rs = 0;
+  if (p.remap != nullptr) {
+    const int4 rm = p.remap[b];
+    // an entry outside its contract (64-aligned x <= P and S, room for the
+    // moved keys, an existing cache) is reported and ignored
+    const bool ok = rm.z >= 0 && rm.z < p.ncache && rm.y >= 0 && (rm.y & 63) == 0 &&
+                    (rm.x & 63) == 0 && rm.x >= 0 && (rm.x == 0x7fffffc0 ||
+                    (rm.x <= P && rm.y + (P - rm.x) + p.T + 63 < p.Lmax));
+    if (ok) {
+      rx = rm.x;
+      rs = rm.y;
+      cb = rm.z;
+    } else if (threadIdx.x == 0) {
+      atomicOr(p.status, kStatusBadInput);
+    }
+    if (!ok) cb = b < p.ncache ? b : 0;
+  }
   const int nkeys = P + p.T;
   const int k_begin = s_idx * p.split;
   if (k_begin >= nkeys) return;  // this split is past the sequence (uniform per CTA)
@@ -217,13 +246,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    const int row0 = (cb * p.Hkv + g) * p.Lmax;
+    if (rx >= k_begin && rx < k_end && rx < P) {
+      // this CTA reads the tile at x: copy its prefix rows [x, P) to S first
+      // (generic-proxy stores, then a proxy fence before the TMA loads)
+      const int nrow = P - rx;
+      for (int e = lane; e < 2 * nrow * 16; e += 32) {
+        const int which = e / (nrow * 16), rem = e % (nrow * 16);
+        const int row = rem / 16, c16 = rem % 16;
+        const __nv_bfloat16* base = which ? p.vc : p.kc;
+        const uint4 val = reinterpret_cast<const uint4*>(base + ((size_t)row0 + rx + row) * DH)[c16];
+        reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(base) + ((size_t)row0 + rs + row) * DH)[c16] =
+            val;
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    }
     if (lane == 0) {
-      const int row0 = (b * p.Hkv + g) * p.Lmax;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % NST, use = j / NST;
         if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, p.status, abort_flag)) break;
-        const int key = row0 + k_begin + j * BN;
+        const int vkey = k_begin + j * BN;
+        const int key = row0 + (vkey >= rx ? rs + (vkey - rx) : vkey);
         uint8_t* dk = sK + st * KT_BYTES;
         uint8_t* dv = sV + st * KT_BYTES;
         mbar_arrive_expect_tx(&k_full[st], KT_BYTES);
@@ -499,6 +544,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Merges the KV splits of each (b, g) row: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// One warp per row. The splits' (m, l) are read one split per lane (32 at a
+// time) and M is a warp maximum; the partial O rows (512 B, 16 B a lane) are
+// loaded eight splits at a time and added in split order, the weight and l of
+// split s coming from lane s % 32 by shuffle. The additions are those of a
+// plain loop over s = 0, 1, ...; the batching only keeps many loads in flight.
 __global__ void __launch_bounds__(128)
     attn_combine_kernel(const Params p) {
   const int g = blockIdx.y, b = blockIdx.z;
@@ -513,19 +563,36 @@ __global__ void __launch_bounds__(128)
   if (ns <= 1) return;  // written directly by the main kernel
   const size_t base = (size_t)(b * p.Hkv + g) * p.nsplit_max;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.ws_ml[(base + s) * ROWS + r].x);
+  for (int s0 = 0; s0 < ns; s0 += 32)
+    if (s0 + lane < ns) M = fmaxf(M, p.ws_ml[(base + s0 + lane) * ROWS + r].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = p.ws_ml[(base + s) * ROWS + r];
-    const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
-    L += w * ml.y;
-    const float4 o =
-        *reinterpret_cast<const float4*>(p.ws_o + ((base + s) * ROWS + r) * DH + lane * 4);
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const int cnt = min(32, ns - s0);
+    const float2 ml = lane < cnt ? p.ws_ml[(base + s0 + lane) * ROWS + r] : make_float2(-INFINITY, 0.f);
+    const float wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float4 o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        o[j] = (j0 + j < cnt) ? *reinterpret_cast<const float4*>(
+                                    p.ws_o + ((base + s0 + j0 + j) * ROWS + r) * DH + lane * 4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+        const float l = __shfl_sync(0xffffffffu, ml.y, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+          L += w * l;
+          acc.x += w * o[j].x;
+          acc.y += w * o[j].y;
+          acc.z += w * o[j].z;
+          acc.w += w * o[j].w;
+        }
+      }
+    }
   }
   const float inv = 1.f / L;
   const int t = r / p.G, hh = r % p.G;
@@ -669,7 +736,7 @@ size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
 ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const int4* remap, int ncache) {
   const int G = Hq / Hkv;
   const int nsplit = (Lmax + split - 1) / split;
   const size_t need = attn_bf16_workspace(B, T, Hq, Hkv, Lmax, split);
@@ -678,7 +745,9 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
                      need, ws_bytes);
   CUtensorMap tk, tv;
   {
-    const uint64_t dims[2] = {128, (uint64_t)B * Hkv * Lmax};
+    // the caches the launch reads: B of them, or ncache when sequences share
+    // caches through the remap table
+    const uint64_t dims[2] = {128, (uint64_t)(remap != nullptr ? ncache : B) * Hkv * Lmax};
     const uint64_t strides[1] = {128 * 2};
     const uint32_t box[2] = {64, (uint32_t)attn::BN};
     ndiff_status s = make_tmap_bf16(&tk, k, 2, dims, strides, box);
@@ -700,6 +769,10 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   prm.split = split;
   prm.nsplit_max = nsplit;
   prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.kc = static_cast<const __nv_bfloat16*>(k);
+  prm.vc = static_cast<const __nv_bfloat16*>(v);
+  prm.remap = remap;
+  prm.ncache = remap != nullptr ? ncache : B;
   prm.ws_o = static_cast<float*>(ws);
   const size_t partials = attn_partials_bytes(B, Hkv, nsplit);
   prm.ws_ml = partials ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +

@@ -52,11 +52,12 @@ constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int THREADS = 192;
 
 // Shared-memory and TMEM geometry for MT token rows (the MMA's N): 32 for a
-// block or one token, 64 for the fused verify + draft forward of two blocks.
+// block or one token, 64 for the fused verify + draft forward of two blocks,
+// 128 for the quadratic forward (verification and three draft blocks).
 template <int MT_>
 struct Geo {
   static constexpr int MT = MT_;
-  static constexpr int NST = MT_ == 32 ? 5 : 7;          // pipeline stages
+  static constexpr int NST = MT_ == 32 ? 5 : (MT_ == 64 ? 7 : 6);  // pipeline stages
   static constexpr int B_BYTES = MT_ * BK * 2;           // 4 KB / 8 KB
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NST * A_BYTES;
@@ -73,6 +74,8 @@ static_assert(Geo<32>::OFF_B % 1024 == 0 && Geo<64>::OFF_B % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(2 * Geo<32>::SMEM_BYTES <= 227 * 1024, "two CTAs per SM at 32 token rows");
 static_assert(Geo<64>::SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+static_assert(Geo<128>::OFF_B % 1024 == 0 && Geo<128>::SMEM_BYTES <= 227 * 1024,
+              "shared memory per CTA at 128 token rows");
 
 __device__ __forceinline__ bool bar_and(bool pred) {
   uint32_t r;
@@ -97,45 +100,45 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void split_range(int s, int S, int nks, int& lo, int& hi) {
-  lo = (int)(((long long)s * nks) / S);
-  hi = (int)(((long long)(s + 1) * nks) / S);
-}
 
-// Epilogue of one finished 128-row tile. Thread r holds y[m] for storage row
-// tile*128 + r and token rows m < T. Loads are issued before stores so that
-// the 32 token rows do not serialise on memory latency.
-template <int MT>
-__device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[MT]) {
+// Epilogue of one finished 128-row tile. Thread r holds y[m0 + j] for storage
+// row tile*128 + r and token rows m0 + j < T (j < W). Loads are issued before
+// stores so that the token rows do not serialise on memory latency.
+// QKV rows: token row m has RoPE position pos(m) and cache row slot(m): both
+// kv_len[0] + m, or, with blk_pos, blk_pos[2b] + m % 32 and blk_pos[2b + 1] +
+// m % 32 for its 32-row block b (the draft blocks of the quadratic forward
+// sit at other positions and cache rows than the block under verification).
+template <int W>
+__device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, float (&v)[W], int m0) {
   const int n = tile * BM + r;
   switch (p.mode) {
     case GEMM_EPI_F32: {
       if (n < p.N) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (m < p.T) p.out[(size_t)m * p.ldo + n] = v[m];
+        for (int j = 0; j < W; ++j)
+          if (m0 + j < p.T) p.out[(size_t)(m0 + j) * p.ldo + n] = v[j];
       }
       break;
     }
     case GEMM_EPI_RESID: {
       if (n < p.N) {
-        float old[MT];
+        float old[W];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) old[m] = (m < p.T) ? p.out[(size_t)m * p.ldo + n] : 0.f;
+        for (int j = 0; j < W; ++j) old[j] = (m0 + j < p.T) ? p.out[(size_t)(m0 + j) * p.ldo + n] : 0.f;
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (m < p.T) p.out[(size_t)m * p.ldo + n] = old[m] + v[m];
+        for (int j = 0; j < W; ++j)
+          if (m0 + j < p.T) p.out[(size_t)(m0 + j) * p.ldo + n] = old[j] + v[j];
       }
       break;
     }
     case GEMM_EPI_SWIGLU: {
       // even rows: gate j = tile*64 + r/2; odd rows: up of the same j
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const float u = __shfl_xor_sync(0xffffffffu, v[m], 1);
-        if (!(r & 1) && m < p.T) {
-          const float g = v[m];
-          p.act[(size_t)m * p.lda + tile * 64 + (r >> 1)] =
+      for (int j = 0; j < W; ++j) {
+        const float u = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        if (!(r & 1) && m0 + j < p.T) {
+          const float g = v[j];
+          p.act[(size_t)(m0 + j) * p.lda + tile * 64 + (r >> 1)] =
               __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
         }
       }
@@ -149,35 +152,45 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int tile, int r, f
       const bool rot = h < p.Hq + p.Hkv;
       const int i = r >> 1;
       const int dim = rot ? ((r & 1) ? i + 64 : i) : r;
-      float pv[MT];
+      float pv[W];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) pv[m] = __shfl_xor_sync(0xffffffffu, v[m], 1);
-      __nv_bfloat16* dst;
-      size_t mstride;
-      if (h < p.Hq) {
-        dst = p.q + (size_t)h * BM + dim;
-        mstride = (size_t)p.Hq * BM;
-      } else if (h < p.Hq + p.Hkv) {
-        dst = p.kc + ((size_t)(h - p.Hq) * p.Lmax + P) * BM + dim;
-        mstride = BM;
-      } else {
-        dst = p.vc + ((size_t)(h - p.Hq - p.Hkv) * p.Lmax + P) * BM + dim;
-        mstride = BM;
-      }
+      for (int j = 0; j < W; ++j) pv[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
+      const bool isq = h < p.Hq;
+      __nv_bfloat16* base;
+      if (isq)
+        base = p.q + (size_t)h * BM + dim;
+      else if (h < p.Hq + p.Hkv)
+        base = p.kc + (size_t)(h - p.Hq) * p.Lmax * BM + dim;
+      else
+        base = p.vc + (size_t)(h - p.Hq - p.Hkv) * p.Lmax * BM + dim;
 #pragma unroll
-      for (int m0 = 0; m0 < MT; m0 += 8) {
+      for (int j0 = 0; j0 < W; j0 += 8) {
+        int pos[8], slot[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = m0 + j0 + j;
+          if (p.blk_pos != nullptr) {
+            pos[j] = p.blk_pos[2 * (m >> 5)] + (m & 31);
+            slot[j] = p.blk_pos[2 * (m >> 5) + 1] + (m & 31);
+          } else {
+            pos[j] = P + m;
+            slot[j] = P + m;
+          }
+        }
         float2 cs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          cs[j] = (rot && m0 + j < p.T) ? __ldg(p.rope + (size_t)(P + m0 + j) * 64 + i)
-                                        : make_float2(1.f, 0.f);
+          cs[j] = (rot && m0 + j0 + j < p.T) ? __ldg(p.rope + (size_t)pos[j] * 64 + i)
+                                             : make_float2(1.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int m = m0 + j;
+          const int m = m0 + j0 + j;
           if (m < p.T) {
-            float y = v[m];
-            if (rot) y = (r & 1) ? y * cs[j].x + pv[m] * cs[j].y : y * cs[j].x - pv[m] * cs[j].y;
-            dst[(size_t)m * mstride] = __float2bfloat16_rn(y);
+            float y = v[j0 + j];
+            if (rot)
+              y = (r & 1) ? y * cs[j].x + pv[j0 + j] * cs[j].y : y * cs[j].x - pv[j0 + j] * cs[j].y;
+            const size_t at = isq ? (size_t)m * p.Hq * BM : (size_t)slot[j] * BM;
+            base[at] = __float2bfloat16_rn(y);
           }
         }
       }
@@ -354,52 +367,61 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
   tc_fence_after();
   griddep_launch();
   const uint32_t tmem = *tmem_slot;
-  const int grid = gridDim.x;
+  // stream-K partition: CTA c owns k-steps [c U / G, (c + 1) U / G) of the
+  // U = ntiles * nks k-steps; it depends on (N, K, grid) only, never on the
+  // token rows, so a row's arithmetic is the same in every launch
+  // (32-bit arithmetic: the launcher keeps U * (grid + 1) below 2^31)
+  const int U = p.ntiles * p.nks;
+  const int kb0 = (int)((long long)blockIdx.x * U / gridDim.x);
+  const int kb1 = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      // Weight tiles of the first NST steps go out before the wait for the
-      // previous kernel (no kernel writes weights); activation tiles after it.
-      int npre = 0;
-      for (int it = blockIdx.x; npre < NST && it < p.items; it += grid) {
-        const int tile = it / p.S;
-        int lo, hi;
-        split_range(it % p.S, p.S, p.nks, lo, hi);
-        for (int ks = lo; ks < hi && npre < NST; ++ks, ++npre) {
-          mbar_arrive_expect_tx(&full[npre], A_BYTES + B_BYTES);
+      // This CTA's k-steps are the contiguous run [kb0, kb1) of all tiles' k-steps
+      // (k-step g is k-step g % nks of tile g / nks; in tiled storage it is the
+      // 16 KB run of rows g * 128). Weights of the first NST steps go out before
+      // the wait for the previous kernel (no kernel writes weights); activation
+      // tiles after it.
+      const int nk = kb1 - kb0;
+      const int npre = nk < NST ? nk : NST;
+      {
+        int tile = kb0 / p.nks, ks = kb0 % p.nks;
+        for (int j = 0; j < npre; ++j) {
+          mbar_arrive_expect_tx(&full[j], A_BYTES + B_BYTES);
           if (p.w_tiled)
-            tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], 0, (tile * p.nks + ks) * BM);
+            tma_load_2d(sA + j * A_BYTES, &tmW, &full[j], 0, (kb0 + j) * BM);
           else
-            tma_load_2d(sA + npre * A_BYTES, &tmW, &full[npre], ks * BK, tile * BM);
+            tma_load_2d(sA + j * A_BYTES, &tmW, &full[j], ks * BK, tile * BM);
+          if (++ks == p.nks) {
+            ks = 0;
+            ++tile;
+          }
         }
       }
       griddep_wait();
       int kc = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; ok && it < p.items; it += grid) {
-        const int tile = it / p.S, s = it % p.S;
-        int lo, hi;
-        split_range(s, p.S, p.nks, lo, hi);
-        for (int ks = lo; ks < hi; ++ks) {
-          const int st = kc % NST;
-          if (kc >= npre) {
-            if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
-            if (p.w_tiled)
-              tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], 0, (tile * p.nks + ks) * BM);
-            else
-              tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
-          }
-          tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
-          ++kc;
+      int tile = kb0 / p.nks, ks = kb0 % p.nks;
+      for (; kc < nk; ++kc) {
+        const int st = kc % NST;
+        if (kc >= npre) {
+          if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) break;
+          mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
+          if (p.w_tiled)
+            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], 0, (kb0 + kc) * BM);
+          else
+            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
+        }
+        tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
+        if (++ks == p.nks) {
+          ks = 0;
+          ++tile;
         }
       }
       if (*abort_flag) {
         for (int j = (kc > NST ? kc - NST : 0); j < kc; ++j) mbar_drain(&full[j % NST], (j / NST) & 1);
+        // weights prefetched past the point where the loop stopped
+        for (int j = kc; j < npre; ++j) mbar_drain(&full[j], 0);
       }
     }
   } else if (warp == 1) {
@@ -409,10 +431,11 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
       int kc = 0, ic = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < p.items; it += grid) {
-        const int s = it % p.S;
-        int lo, hi;
-        split_range(s, p.S, p.nks, lo, hi);
+      // one accumulator per segment (this CTA's part of one tile)
+      for (int g0 = kb0; ok && g0 < kb1; ++ic) {
+        const int lo = g0 % p.nks;
+        const int hi = (kb1 - g0) < (p.nks - lo) ? lo + (kb1 - g0) : p.nks;
+        g0 += hi - lo;
         const int buf = ic & 1;
         if (ic >= 2 && !mbar_wait(&acc_empty[buf], ((ic >> 1) - 1) & 1, p.status, abort_flag)) {
           ok = false;
@@ -438,7 +461,6 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
         }
         if (!ok) break;
         umma_commit(&acc_full[buf]);
-        ++ic;
       }
       // every MMA issued above has finished before TMEM is released
       umma_commit(mma_done);
@@ -451,74 +473,188 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
     const int tid = threadIdx.x - 64;
     const uint32_t tl = tmem + ((quarter * 32u) << 16);
     griddep_wait();
+    const int G = gridDim.x;
+    const int c = blockIdx.x;
     int ic = 0;
-    for (int it = blockIdx.x; it < p.items; it += grid, ++ic) {
+    for (int g0 = kb0; g0 < kb1; ++ic) {
+      const int tile = g0 / p.nks;
+      const int lo = g0 % p.nks;
+      const int hi = (kb1 - g0) < (p.nks - lo) ? lo + (kb1 - g0) : p.nks;
+      g0 += hi - lo;
+      const bool whole = lo == 0 && hi == p.nks;
+      // A split tile's contributors are CTAs cf..cl, in k order. Contributor x
+      // keeps its partial in slot 0 when its range starts inside the tile (the
+      // tile is its first segment), else in slot 1: so cf uses slot 1 (its
+      // range holds the tile's first k-step) and every later one slot 0.
+      const int t0 = tile * p.nks;
+      const int cf = ((t0 + 1) * G - 1) / U;
+      const int cl = ((t0 + p.nks) * G - 1) / U;
+      const int my_slot = lo > 0 ? 0 : 1;
       const int buf = ic & 1;
       bool ok = mbar_wait(&acc_full[buf], (ic >> 1) & 1, p.status, abort_flag);
       if (!bar_and(ok)) break;
       tc_fence_after();
-      float v[MT];
+      if constexpr (MT > 64) {
+        // 32-column slices (registers): the accumulator stays in TMEM until the
+        // segment is done; per column the arithmetic is that of the narrow
+        // instances (the same partials, summed in the same order).
+        constexpr int NSL = MT / 32;
+        bool last = true;
+        if (!whole) {
+          float4* part = reinterpret_cast<float4*>(p.ws + ((size_t)(c * 2 + my_slot) * BM + r) * MT);
+#pragma unroll 1
+          for (int sl = 0; sl < NSL && sl * 32 < p.T; ++sl) {
+            float v[32];
+            tmem_ld32(tl + buf * MT + sl * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < MT; c += 32) tmem_ld32(tl + buf * MT + c, v + c);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
-
-      const int tile = it / p.S, s = it % p.S;
-      if (p.S > 1) {
-        // partial tile layout [item][row r][32 token rows]: 16-byte stores per thread
-        float4* part = reinterpret_cast<float4*>(p.ws + ((size_t)it * BM + r) * MT);
-#pragma unroll
-        for (int c = 0; c < MT / 4; ++c)
-          if (c * 4 < p.T)
-            __stcg(part + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
-        // The barrier orders the group's partial stores before thread 0's
-        // release-acquire increment (cumulative at GPU scope); the last split
-        // to arrive then sees every other split's partial.
-        bar_sync128();
-        if (tid == 0) {
-          int old;
-          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                       : "=r"(old)
-                       : "l"(p.counters + tile)
-                       : "memory");
-          *last_flag = (old == p.S - 1) ? 1 : 0;
-        }
-        bar_sync128();
-        if (!*last_flag) continue;
-        // sum the splits in order 0..S-1; every split's loads are issued together
-        float acc[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        for (int s2 = 0; s2 < p.S; ++s2) {
-          if (s2 == s) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] += v[m];
-            continue;
+            for (int q = 0; q < 8; ++q)
+              if (sl * 32 + q * 4 < p.T)
+                __stcg(part + sl * 8 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
           }
-          const float4* src =
-              reinterpret_cast<const float4*>(p.ws + ((size_t)(tile * p.S + s2) * BM + r) * MT);
-          float4 t[MT / 4];
-#pragma unroll
-          for (int c = 0; c < MT / 4; ++c)
-            t[c] = (c * 4 < p.T) ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < MT / 4; ++c) {
-            acc[4 * c] += t[c].x;
-            acc[4 * c + 1] += t[c].y;
-            acc[4 * c + 2] += t[c].z;
-            acc[4 * c + 3] += t[c].w;
+          bar_sync128();
+          if (tid == 0) {
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(p.counters + tile)
+                         : "memory");
+            *last_flag = (old == cl - cf) ? 1 : 0;
           }
+          bar_sync128();
+          last = *last_flag != 0;
         }
+        if (last) {
+#pragma unroll 1
+          for (int sl = 0; sl < NSL && sl * 32 < p.T; ++sl) {
+            float v[32];
+            tmem_ld32(tl + buf * MT + sl * 32, v);
+            tmem_wait_ld();
+            if (!whole) {
+              float acc[32];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = acc[m];
-        if (tid == 0) p.counters[tile] = 0;
-      }
-      if constexpr (ARGMAX) {
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              for (int x = cf; x <= cl; ++x) {
+                if (x == c) {
 #pragma unroll
-        for (int c = 0; c < MT; c += 32) epilogue_argmax(p, tile, r, lane, quarter, v + c, sred, MT, c);
+                  for (int j = 0; j < 32; ++j) acc[j] += v[j];
+                  continue;
+                }
+                const int xs = x == cf ? 1 : 0;
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.ws + ((size_t)(x * 2 + xs) * BM + r) * MT) + sl * 8;
+                float4 t[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  t[q] = (sl * 32 + q * 4 < p.T) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  acc[4 * q] += t[q].x;
+                  acc[4 * q + 1] += t[q].y;
+                  acc[4 * q + 2] += t[q].z;
+                  acc[4 * q + 3] += t[q].w;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = acc[j];
+            }
+            if constexpr (ARGMAX) {
+              epilogue_argmax(p, tile, r, lane, quarter, v, sred, MT, sl * 32);
+            } else {
+              epilogue<32>(p, tile, r, v, sl * 32);
+            }
+          }
+          if (!whole && tid == 0) p.counters[tile] = 0;
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
       } else {
-        epilogue<MT>(p, tile, r, v);
+        float v[MT];
+#pragma unroll
+        for (int q = 0; q < MT; q += 32) tmem_ld32(tl + buf * MT + q, v + q);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        if (!whole) {
+          // partial layout [CTA][slot][row r][MT token rows]: 16-byte stores
+          float4* part = reinterpret_cast<float4*>(p.ws + ((size_t)(c * 2 + my_slot) * BM + r) * MT);
+#pragma unroll
+          for (int q = 0; q < MT / 4; ++q)
+            if (q * 4 < p.T)
+              __stcg(part + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+          // The barrier orders the group's partial stores before thread 0's
+          // release-acquire increment (cumulative at GPU scope); the last
+          // contributor to arrive then sees every other contributor's partial.
+          bar_sync128();
+          if (tid == 0) {
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(p.counters + tile)
+                         : "memory");
+            *last_flag = (old == cl - cf) ? 1 : 0;
+          }
+          bar_sync128();
+          if (!*last_flag) continue;
+          // sum the contributors in k order (the same additions for every T)
+          float acc[MT];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+          if (p.T <= 4) {
+            // one 16-byte partial per contributor: load eight at a time, then add
+            for (int x0 = cf; x0 <= cl; x0 += 8) {
+              float4 t[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int x = x0 + j;
+                t[j] = (x <= cl && x != c)
+                           ? __ldcg(reinterpret_cast<const float4*>(
+                                 p.ws + ((size_t)(x * 2 + (x == cf ? 1 : 0)) * BM + r) * MT))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int x = x0 + j;
+                if (x > cl) break;
+                const float4 y = x == c ? make_float4(v[0], v[1], v[2], v[3]) : t[j];
+                acc[0] += y.x;
+                acc[1] += y.y;
+                acc[2] += y.z;
+                acc[3] += y.w;
+              }
+            }
+          } else {
+            for (int x = cf; x <= cl; ++x) {
+              if (x == c) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m] += v[m];
+                continue;
+              }
+              const float4* src = reinterpret_cast<const float4*>(
+                  p.ws + ((size_t)(x * 2 + (x == cf ? 1 : 0)) * BM + r) * MT);
+              float4 t[MT / 4];
+#pragma unroll
+              for (int q = 0; q < MT / 4; ++q)
+                t[q] = (q * 4 < p.T) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int q = 0; q < MT / 4; ++q) {
+                acc[4 * q] += t[q].x;
+                acc[4 * q + 1] += t[q].y;
+                acc[4 * q + 2] += t[q].z;
+                acc[4 * q + 3] += t[q].w;
+              }
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m) v[m] = acc[m];
+          if (tid == 0) p.counters[tile] = 0;
+        }
+        if constexpr (ARGMAX) {
+#pragma unroll
+          for (int q = 0; q < MT; q += 32) epilogue_argmax(p, tile, r, lane, quarter, v + q, sred, MT, q);
+        } else {
+          epilogue<MT>(p, tile, r, v, 0);
+        }
       }
     }
   }
@@ -580,34 +716,20 @@ GemmPlan gemm_plan(int N, int K) {
   GemmPlan pl;
   pl.ntiles = (N + gemm::BM - 1) / gemm::BM;
   pl.nks = K / gemm::BK;
+  // stream-K: one CTA per SM, each an equal contiguous run of the tiles'
+  // k-steps (so every SM streams the same number of 16 KB weight tiles)
+  const long long U = (long long)pl.ntiles * pl.nks;
   const int sms = num_sms();
-  // Cost of a split count S: the busiest CTA's k-steps (16 KB of weights
-  // each) plus, when split, about eight k-steps' worth for the partial tile
-  // and the last split's merge. Splits stay at three or fewer: on B300 every
-  // projection of the model measured slower with more (the merge epilogue
-  // then outlasts an item's main loop). Ties keep the larger S.
-  long long best = -1;
-  int bestS = 1;
-  const int smax = pl.nks < 3 ? pl.nks : 3;
-  for (int S = 1; S <= smax; ++S) {
-    const long long items = (long long)pl.ntiles * S;
-    const long long waves = (items + sms - 1) / sms;
-    const long long steps = (pl.nks + S - 1) / S;
-    const long long cost = waves * (steps + (S > 1 ? 8 : 0));
-    if (best < 0 || cost <= best) {
-      best = cost;
-      bestS = S;
-    }
-  }
-  pl.S = bestS;
+  pl.grid = U < sms ? (int)U : sms;
+  pl.S = 0;
   pl.nchunks = 1;
-  pl.items = pl.ntiles * pl.S;
-  pl.grid = pl.items < sms ? pl.items : sms;
+  pl.items = pl.ntiles;
   return pl;
 }
 
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt) {
-  return pl.S > 1 ? (size_t)pl.items * mt * gemm::BM * sizeof(float) : 0;
+  // two partial tiles per CTA: its first segment and its last
+  return (size_t)pl.grid * 2 * gemm::BM * mt * sizeof(float);
 }
 
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
@@ -657,19 +779,26 @@ static ndiff_status launch_variant(const CUtensorMap& tmW, const CUtensorMap& tm
 
 ndiff_status launch_gemm_bf16(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmPlan& pl,
                               GemmParams p, cudaStream_t stream, int mt) {
-  if (mt != 32 && mt != 64)
-    return set_error(NDIFF_ERR_UNSUPPORTED, "projection kernel: 32 or 64 token rows (got %d)", mt);
+  if (mt != 32 && mt != 64 && mt != 128)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "projection kernel: 32, 64 or 128 token rows (got %d)", mt);
   if (p.T > mt) return set_error(NDIFF_ERR_INVALID_ARG, "projection kernel: %d rows > %d", p.T, mt);
-  p.S = pl.S;
+  if ((long long)pl.ntiles * pl.nks * (pl.grid + 1) >= (1LL << 31))
+    return set_error(NDIFF_ERR_UNSUPPORTED, "projection kernel: %d x %d k-steps is too large",
+                     pl.ntiles, pl.nks);
+  p.S = 0;
   p.nks = pl.nks;
-  p.items = pl.items;
+  p.items = pl.ntiles;
+  p.ntiles = pl.ntiles;
   p.status = device_status_word();
   const bool am = p.mode == GEMM_EPI_ARGMAX;
   if (mt == 32)
     return am ? launch_variant<32, true>(tmW, tmX, pl, p, stream)
               : launch_variant<32, false>(tmW, tmX, pl, p, stream);
-  return am ? launch_variant<64, true>(tmW, tmX, pl, p, stream)
-            : launch_variant<64, false>(tmW, tmX, pl, p, stream);
+  if (mt == 64)
+    return am ? launch_variant<64, true>(tmW, tmX, pl, p, stream)
+              : launch_variant<64, false>(tmW, tmX, pl, p, stream);
+  return am ? launch_variant<128, true>(tmW, tmX, pl, p, stream)
+            : launch_variant<128, false>(tmW, tmX, pl, p, stream);
 }
 
 }  // namespace ndiff

@@ -24,10 +24,19 @@ void* current_context();
 // attn_bf16.cu
 int attn_bf16_auto_split(int B, int Hkv, int Lmax);
 size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split);
+// remap (device, [B] {x, S, cache index, 0}, nullptr = none): sequence b reads
+// cache `cache index` (of ncache caches) and finds its virtual keys >= x (a
+// multiple of 64, at most kv_len) at cache rows S (a multiple of 64) + key - x;
+// the prefix rows [x, kv_len) are copied there by the kernel. Needs
+// S + (kv_len - x) + T + 63 < Lmax. x = kNoRemap: no moved keys, only the
+// cache index applies. Entries outside this contract are reported as bad
+// input and ignored.
+constexpr int kNoRemap = 0x7fffffc0;
+
 ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const int4* remap = nullptr, int ncache = 0);
 
 // attn_f32.cu
 ndiff_status launch_attn_f32(const float* q, const float* k, const float* v,
@@ -57,8 +66,9 @@ enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV =
 struct GemmParams {
   int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
   int w_tiled;             // W stored as contiguous 128 x 64 tiles (else row-major)
-  int S, nks, items;       // K splits, 64-wide K steps, work items (set by the launcher)
-  float* ws;               // split partials [items][128][32] fp32 (S > 1)
+  int S, nks, items;       // wide kernel: K splits, 64-wide K steps, work items (set by the launcher)
+  int ntiles;              // weight-streaming kernel: 128-row tiles (set by the launcher)
+  float* ws;               // weight-streaming kernel: partial tiles [grid][2][128][MT] fp32
   int* counters;           // [tiles] arrival counters, zero between launches
   unsigned int* status;    // device status word
   float* out;              // F32: out[m*ldo + n] = y; RESID: out[m*ldo + n] += y
@@ -76,17 +86,23 @@ struct GemmParams {
   int excl;                // ARGMAX: id left out of the argmax (-1: none)
   int Tb;                  // wide kernel, QKV: tokens per sequence (token m is slot m % Tb
                            // of sequence m / Tb; caches [B][Hkv][Lmax][128], kv_len [B])
+  const int32_t* blk_pos;  // QKV, weight-streaming kernel (nullptr: token row m has position
+                           // and cache row kv_len[0] + m): {position, cache row} of the first
+                           // row of each 32-row block [MT/32][2]
 };
 
+// Weight-streaming kernel: a stream-K partition of the ntiles * nks k-steps
+// over `grid` CTAs (S unused, items = ntiles). Wide kernel: items of (tile,
+// token chunk), S = 1.
 struct GemmPlan {
   int ntiles, nks, S, items, grid;
   int nchunks;             // wide kernel: 256-row token chunks (1 for the skinny kernel)
 };
 
 // The weight-streaming projection for mt = 32 token rows (a block, or one
-// token) or mt = 64 (two blocks: the fused verify + draft forward). The K
-// split depends on (N, K) only, so a row's arithmetic is the same for every
-// row count and both mt.
+// token), mt = 64 (two blocks: the fused verify + draft forward) or mt = 128
+// (four blocks: the quadratic forward). The K split depends on (N, K) only,
+// so a row's arithmetic is the same for every row count and every mt.
 GemmPlan gemm_plan(int N, int K);
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt = 32);
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,

@@ -119,8 +119,14 @@ struct ndiff_model {
   CUtensorMap tm_h_w, tm_oact_w, tm_a_w;  // 256-row boxes for the wide kernel (B > 1)
   CUtensorMap tm_h_w64, tm_oact_w64, tm_a_w64;  // 64-row boxes: its AR forwards (B <= 64 rows)
   CUtensorMap tm_h64, tm_oact64, tm_a64;  // 64-row boxes: the fused verify + draft forward
-  int32_t* fin = nullptr;       // [64] fused forward input
+  CUtensorMap tm_h128, tm_oact128, tm_a128;  // 128-row boxes: the quadratic forward
+  int32_t* fin = nullptr;       // [128] fused / quadratic forward input
   int32_t* kv_len2 = nullptr;   // [1] prefix of the fused forward's draft half
+  int32_t* kvc = nullptr;       // [4] quadratic forward: prefixes of its three draft blocks
+  int4* remap = nullptr;        // [4] quadratic forward: their key remaps
+  int32_t* blk_pos = nullptr;   // [8] quadratic forward: position and cache row of each block
+  int32_t* cand_dev = nullptr;  // [2] candidate acceptance lengths of the quadratic mode
+  int cand_host[2] = {-1, -1};
   bool have_draft = false;      // the last fused forward left a draft of the next block
   int last_L0 = -1;             // accept length of sequence 0 in the last verification
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
@@ -229,9 +235,10 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
   const int B = m->B, M = B * T;
   const bool wide = B > 1;
   const bool fused = T == 2 * kBlock;
-  if (fused && (wide || !m->bf16))
+  const bool quad = T == 4 * kBlock;
+  if ((fused || quad) && (wide || !m->bf16))
     return set_error(NDIFF_ERR_UNSUPPORTED, "fused verify + draft forward: one bf16 sequence only");
-  const int mt = fused ? 2 * kBlock : kBlock;
+  const int mt = quad ? 4 * kBlock : (fused ? 2 * kBlock : kBlock);
   TRY(launch_embed(m->embed, m->bf16, ids, M, m->V, m->d, m->x, s));
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
@@ -244,17 +251,18 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
   // the activation maps of one projection input: 32-row boxes (one block),
   // 64-row boxes (fused forward), and the wide kernel's 256- and 64-row boxes
   struct XMaps {
-    const CUtensorMap &x32, &x64, &w256, &w64;
+    const CUtensorMap &x32, &x64, &x128, &w256, &w64;
   };
-  const XMaps xh{m->tm_h, m->tm_h64, m->tm_h_w, m->tm_h_w64};
-  const XMaps xo{m->tm_oact, m->tm_oact64, m->tm_oact_w, m->tm_oact_w64};
-  const XMaps xa{m->tm_a, m->tm_a64, m->tm_a_w, m->tm_a_w64};
+  const XMaps xh{m->tm_h, m->tm_h64, m->tm_h128, m->tm_h_w, m->tm_h_w64};
+  const XMaps xo{m->tm_oact, m->tm_oact64, m->tm_oact128, m->tm_oact_w, m->tm_oact_w64};
+  const XMaps xa{m->tm_a, m->tm_a64, m->tm_a128, m->tm_a_w, m->tm_a_w64};
   auto proj = [&](const CUtensorMap& tw, const XMaps& xm, const GemmPlan& pl, int N, int K,
                   const GemmParams& p) -> ndiff_status {
     if (wide)
       return launch_gemm_wide(tw, gemm_wide_box_rows(M) == 64 ? xm.w64 : xm.w256,
                               gemm_wide_plan(N, K, M), p, s);
     if (fused) return launch_gemm_bf16(tw, xm.x64, pl, p, s, mt);
+    if (quad) return launch_gemm_bf16(tw, xm.x128, pl, p, s, mt);
     return launch_gemm_bf16(tw, xm.x32, pl, p, s);
   };
   for (int l = 0; l < m->L; ++l) {
@@ -272,8 +280,20 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.Lmax = m->Lmax;
       p.kv_len = m->kv_len;
       p.rope = m->rope;
+      p.blk_pos = quad ? m->blk_pos : nullptr;
       TRY(proj(ly.tm_qkv, xh, m->pl_qkv, m->NQKV, m->d, p));
-      if (fused) {
+      if (quad) {
+        // the block under verification (causal at prefix P), then its three
+        // draft blocks as one batch over the same cache (bidirectional, each at
+        // its own prefix, the candidate blocks' keys remapped to their rows)
+        const size_t blk = (size_t)kBlock * m->HD;
+        __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(m->ob);
+        TRY(launch_attn_bf16(qb, ly.kc, ly.vc, m->kv_len, 1, kBlock, m->Hq, m->Hkv, m->Lmax, 1,
+                             scale, m->attn_split, ob, m->aws, m->aws_bytes, s));
+        TRY(launch_attn_bf16(qb + blk, ly.kc, ly.vc, m->kvc, 3, kBlock, m->Hq, m->Hkv, m->Lmax, 0,
+                             scale, m->attn_split, ob + blk, m->aws, m->aws_bytes, s, m->remap, 1));
+      } else if (fused) {
         const size_t half = (size_t)kBlock * m->HD;  // elements of one block's q / output rows
         __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
         __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(m->ob);
@@ -337,7 +357,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     TRY(proj(m->tm_lm, xh, m->pl_lm, m->V, m->d, p));
     return launch_argmax_merge(m->red, m->pl_lm.ntiles, M, wide ? M : mt, m->pred, m->conf, s);
   }
-  if (wide || fused)
+  if (wide || fused || quad)
     return set_error(NDIFF_ERR_UNSUPPORTED, "model logits: one block of one sequence only");
   if (m->bf16) {
     GemmParams p = gp;
@@ -408,7 +428,22 @@ ndiff_status enqueue_fused(ndiff_model* m, bool need_draft, cudaStream_t s) {
   return launch_fused_stash(m->pred + kBlock, m->acclen, m->last_dev, m->draft, m->block_in, s);
 }
 
-enum { PART_CYCLE = 0, PART_INIT = 1, PART_ROUND = 2, PART_TAIL = 3, PART_FUSED = 4 };
+// One cycle of quadratic self-speculation (one sequence): as enqueue_fused,
+// with one forward of 128 rows that verifies the block and drafts the next
+// for full acceptance and for the two candidate acceptance lengths in
+// m->cand_dev; the draft of the verified length, if drafted, is stashed.
+ndiff_status enqueue_quad(ndiff_model* m, bool need_draft, cudaStream_t s) {
+  if (need_draft) TRY(draft_block(m, 1, s));
+  TRY(launch_quad_input(m->fin, m->block_in, m->draft, m->mask_id, m->kv_len, m->cand_dev, m->kvc,
+                        m->remap, m->blk_pos, s));
+  TRY(forward(m, m->fin, 4 * kBlock, 1, FWD_TOKENS, s));
+  TRY(launch_verify_accept(m->draft, m->pred, 1, kBlock, m->acclen, m->commit, m->ncommit,
+                           m->kv_len, s));
+  TRY(launch_commit(m->commit, kBlock, m->ncommit, 0, 0, m->last_dev, m->kv_len, 1, s));
+  return launch_quad_stash(m->pred, m->acclen, m->cand_dev, m->last_dev, m->draft, m->block_in, s);
+}
+
+enum { PART_CYCLE = 0, PART_INIT = 1, PART_ROUND = 2, PART_TAIL = 3, PART_FUSED = 4, PART_QUAD = 5 };
 
 // The launches `fn` enqueues, as an instantiated CUDA graph captured on the
 // model's stream on first use and kept under `key`.
@@ -496,8 +531,8 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   m->last.assign(m->B, -1);
   const size_t esz = m->esz;
   const size_t d = m->d;
-  // activation rows: B blocks, or the two blocks of a fused forward
-  const size_t R = (size_t)(m->B > 1 ? m->B * kBlock : 2 * kBlock);
+  // activation rows: B blocks, or the four blocks of a quadratic forward
+  const size_t R = (size_t)(m->B > 1 ? m->B * kBlock : 4 * kBlock);
   cudaStream_t s = 0;
 
   TRY(dalloc(m, &m->embed, (size_t)m->V * d * esz));
@@ -547,7 +582,13 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
   TRY(dalloc_t(m, &m->chosen, R * 4));
   TRY(dalloc_t(m, &m->prompt, (size_t)m->Lmax * 4));
   TRY(dalloc_t(m, &m->last_dev, Bn * 4));
-  TRY(dalloc_t(m, &m->fin, 2 * kBlock * 4));
+  TRY(dalloc_t(m, &m->fin, 4 * kBlock * 4));
+  TRY(dalloc_t(m, &m->kvc, 16));
+  TRY(dalloc_t(m, &m->remap, 4 * sizeof(int4)));
+  TRY(dalloc_t(m, &m->blk_pos, 8 * 4));
+  TRY(dalloc_t(m, &m->cand_dev, 16));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->remap, 0, 4 * sizeof(int4), s));
+  NDIFF_CUDA_TRY(cudaMemsetAsync(m->cand_dev, 0, 16, s));
   TRY(dalloc_t(m, &m->kv_len2, 16));
   TRY(dalloc_t(m, &m->rope, (size_t)m->Lmax * (m->D / 2) * sizeof(float2)));
   NDIFF_CUDA_TRY(cudaMemsetAsync(m->ids, 0, R * 4, s));
@@ -565,7 +606,7 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     size_t ws = 16;
     int tiles = 1;
     for (const GemmPlan* pl : pls) {
-      const size_t b = gemm_partials_bytes(*pl, 2 * kBlock);
+      const size_t b = gemm_partials_bytes(*pl, m->B > 1 ? 2 * kBlock : 4 * kBlock);
       if (b > ws) ws = b;
       if (pl->ntiles > tiles) tiles = pl->ntiles;
     }
@@ -575,6 +616,10 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     NDIFF_CUDA_TRY(cudaMemsetAsync(m->gcnt, 0, (size_t)tiles * 4, s));
     m->attn_split = attn_bf16_auto_split(m->B, m->Hkv, m->Lmax);
     m->aws_bytes = attn_bf16_workspace(m->B, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
+    if (m->B == 1) {  // the quadratic forward's three draft blocks run as one batch
+      const size_t q3 = attn_bf16_workspace(3, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
+      if (q3 > m->aws_bytes) m->aws_bytes = q3;
+    }
     if (m->aws_bytes) TRY(dalloc(m, &m->aws, m->aws_bytes));
     TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, kBlock, nullptr, &m->tm_h));
     TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, kBlock, nullptr, &m->tm_oact));
@@ -584,6 +629,13 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
                        2 * kBlock));
     TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, 2 * kBlock, nullptr, &m->tm_a64,
                        2 * kBlock));
+    if (m->B == 1) {
+      TRY(gemm_make_maps(nullptr, 0, m->d, false, m->h, 4 * kBlock, nullptr, &m->tm_h128, 4 * kBlock));
+      TRY(gemm_make_maps(nullptr, 0, m->HD, false, m->ob, 4 * kBlock, nullptr, &m->tm_oact128,
+                         4 * kBlock));
+      TRY(gemm_make_maps(nullptr, 0, m->ffn, false, m->ab, 4 * kBlock, nullptr, &m->tm_a128,
+                         4 * kBlock));
+    }
     TRY(gemm_wide_make_xmap(m->h, (int)R, m->d, &m->tm_h_w));
     TRY(gemm_wide_make_xmap(m->ob, (int)R, m->HD, &m->tm_oact_w));
     TRY(gemm_wide_make_xmap(m->ab, (int)R, m->ffn, &m->tm_a_w));
@@ -860,8 +912,41 @@ static ndiff_status decode_cycle(ndiff_model* m, const ndiff_decode_opts* opts,
   const ndiff_mode mode = opts->mode;
   if (!m->ready) return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: no prefill yet");
   if (mode != NDIFF_MODE_AR && mode != NDIFF_MODE_DIFF && mode != NDIFF_MODE_SELFSPEC &&
-      mode != NDIFF_MODE_SELFSPEC_FUSED)
+      mode != NDIFF_MODE_SELFSPEC_FUSED && mode != NDIFF_MODE_SELFSPEC_QUAD)
     return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: bad mode %d", (int)mode);
+  if (mode == NDIFF_MODE_SELFSPEC_QUAD) {
+    if (m->B != 1 || !m->bf16)
+      return set_error(NDIFF_ERR_UNSUPPORTED,
+                       "ndiff_decode_step: quadratic self-speculation needs one bf16 sequence");
+    if (opts->n_cand < 1 || opts->n_cand > 2)
+      return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: n_cand must be 1 or 2 (got %d)",
+                       opts->n_cand);
+    const int c0 = opts->cand[0], c1 = opts->n_cand > 1 ? opts->cand[1] : opts->cand[0];
+    if (c0 < 0 || c0 >= kBlock || c1 < 0 || c1 >= kBlock)
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "ndiff_decode_step: candidate acceptance lengths must be in [0, 32) (got %d, %d)",
+                       c0, c1);
+    if (m->P[0] + 448 > m->Lmax)
+      return set_error(NDIFF_ERR_INVALID_ARG,
+                       "ndiff_decode_step: quadratic mode needs max_seq >= committed + 448 (%d of %d)",
+                       m->P[0], m->Lmax);
+    TRY(set_device(m));
+    NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
+    if (c0 != m->cand_host[0] || c1 != m->cand_host[1]) {
+      const int32_t hc[2] = {c0, c1};
+      NDIFF_CUDA_TRY(cudaMemcpy(m->cand_dev, hc, sizeof(hc), cudaMemcpyHostToDevice));
+      m->cand_host[0] = c0;
+      m->cand_host[1] = c1;
+    }
+    const bool need = !m->have_draft;
+    cudaGraphExec_t ge = nullptr;
+    TRY(cached_graph(m, std::make_tuple((int)PART_QUAD, (int)mode, need ? 1 : 0, 0u, 0u),
+                     [&](cudaStream_t s2) { return enqueue_quad(m, need, s2); }, &ge));
+    NDIFF_CUDA_TRY(cudaGraphLaunch(ge, m->ms));
+    TRY(collect(m, mode, need ? 2 : 1, need ? 1 : 0, 0, out_tokens_host, n_out, stats));
+    m->have_draft = m->last_L0 == kBlock || m->last_L0 == c0 || m->last_L0 == c1;
+    return NDIFF_OK;
+  }
   if (mode == NDIFF_MODE_SELFSPEC_FUSED) {
     if (m->B != 1 || !m->bf16)
       return set_error(NDIFF_ERR_UNSUPPORTED,
@@ -899,6 +984,10 @@ static ndiff_status decode_cycle(ndiff_model* m, const ndiff_decode_opts* opts,
       return set_error(NDIFF_ERR_INVALID_ARG, "ndiff_decode_step: KV cache of sequence %d full (%d of %d)",
                        b, m->P[b], m->Lmax);
   TRY(set_device(m));
+  // a draft left by a fused or quadratic cycle belongs to the state those
+  // modes carry from cycle to cycle; a cycle of any other mode moves the
+  // session on without it
+  m->have_draft = false;
   // the cycle runs on the model's stream, after the caller's earlier work
   NDIFF_CUDA_TRY(cudaStreamSynchronize(stream));
   if (!thr) {
@@ -988,6 +1077,9 @@ ndiff_status ndiff_decode_step(ndiff_model* m, ndiff_mode mode, int steps, int32
   o.steps = steps;
   o.tau = 0.f;
   o.tau_revise = 2.f;
+  o.n_cand = 2;  // the quadratic mode's default candidates
+  o.cand[0] = 0;
+  o.cand[1] = 1;
   return ndiff_decode_step_ex(m, &o, out_tokens_host, n_out, stats, stream);
 }
 

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "kernels.h"
 #include "model_kernels.h"
 
 namespace ndiff {
@@ -310,6 +311,58 @@ __global__ void fused_stash_kernel(const int32_t* pred2, const int32_t* acclen, 
   if (i <= 30) block_in[i + 1] = pred2[i];
 }
 
+// Quadratic forward of one sequence (128 rows): the block under verification
+// [last, d0..d30] at prefix P, the next block [d31, MASK x 31] for full
+// acceptance at prefix P + 32, and for each candidate acceptance length c
+// (cand[0], cand[1]) a block of 32 [MASK] at prefix P_c = P + c + 1. The
+// candidate blocks' K/V go to cache rows past both blocks: S_c = align64(P +
+// 64) + 128 (c index), and the attention finds their keys there (remap
+// {x_c = P_c rounded down to 64, S_c}); blk_pos gives the QKV epilogue each
+// block's first position and cache row.
+__global__ void quad_input_kernel(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                                  int32_t mask_id, const int32_t* kv_len, const int32_t* cand,
+                                  int32_t* kvc, int4* remap, int32_t* blk_pos) {
+  griddep_launch();
+  griddep_wait();
+  const int i = threadIdx.x;
+  if (i < 32) fin[i] = block_in[i];
+  else if (i < 128) fin[i] = i == 32 ? draft[31] : mask_id;
+  if (i == 0) {
+    const int P = kv_len[0];
+    const int S0 = (P + 64 + 63) & ~63;
+    kvc[0] = P + 32;
+    remap[0] = make_int4(kNoRemap, 0, 0, 0);
+    blk_pos[0] = P;
+    blk_pos[1] = P;
+    blk_pos[2] = P + 32;
+    blk_pos[3] = P + 32;
+    for (int c = 0; c < 2; ++c) {
+      const int Pc = P + cand[c] + 1;
+      const int x = Pc & ~63, S = S0 + 128 * c;
+      kvc[1 + c] = Pc;
+      remap[1 + c] = make_int4(x, S, 0, 0);
+      blk_pos[4 + 2 * c] = Pc;
+      blk_pos[5 + 2 * c] = S + (Pc - x);
+    }
+  }
+}
+
+// After verification: the draft block of the verified acceptance length (32,
+// cand[0], cand[1], in that order), if any, becomes the next draft and its
+// verification input [last, d'0..d'30].
+__global__ void quad_stash_kernel(const int32_t* pred, const int32_t* acclen, const int32_t* cand,
+                                  const int32_t* last, int32_t* draft, int32_t* block_in) {
+  griddep_launch();
+  griddep_wait();
+  const int i = threadIdx.x;
+  const int L = acclen[0];
+  const int src = L == 32 ? 32 : (L == cand[0] ? 64 : (L == cand[1] ? 96 : -1));
+  if (src < 0 || i >= 32) return;
+  draft[i] = pred[src + i];
+  if (i == 0) block_in[0] = last[0];
+  if (i <= 30) block_in[i + 1] = pred[src + i];
+}
+
 }  // namespace mk
 
 // ---------------------------------------------------------------- launchers
@@ -428,6 +481,22 @@ ndiff_status launch_fused_input(int32_t* fin, const int32_t* block_in, const int
                                 cudaStream_t s) {
   NDIFF_CUDA_TRY(launch_k(mk::fused_input_kernel, dim3(1), dim3(64), 0, s, fin, block_in, draft,
                           mask_id, kv_len, kv_len2));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_quad_input(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                               int32_t mask_id, const int32_t* kv_len, const int32_t* cand,
+                               int32_t* kvc, int4* remap, int32_t* blk_pos, cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::quad_input_kernel, dim3(1), dim3(128), 0, s, fin, block_in, draft,
+                          mask_id, kv_len, cand, kvc, remap, blk_pos));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_quad_stash(const int32_t* pred, const int32_t* acclen, const int32_t* cand,
+                               const int32_t* last, int32_t* draft, int32_t* block_in,
+                               cudaStream_t s) {
+  NDIFF_CUDA_TRY(launch_k(mk::quad_stash_kernel, dim3(1), dim3(32), 0, s, pred, acclen, cand, last,
+                          draft, block_in));
   return NDIFF_OK;
 }
 

@@ -48,6 +48,15 @@ ndiff_status launch_kv_add(int32_t* kv_len, int add, cudaStream_t s);
 ndiff_status launch_fused_input(int32_t* fin, const int32_t* block_in, const int32_t* draft,
                                 int32_t mask_id, const int32_t* kv_len, int32_t* kv_len2,
                                 cudaStream_t s);
+// Quadratic forward (one sequence, 128 rows): its input, the candidate
+// blocks' prefixes / key remaps / positions, and the stash of the draft of the
+// verified acceptance length.
+ndiff_status launch_quad_input(int32_t* fin, const int32_t* block_in, const int32_t* draft,
+                               int32_t mask_id, const int32_t* kv_len, const int32_t* cand,
+                               int32_t* kvc, int4* remap, int32_t* blk_pos, cudaStream_t s);
+ndiff_status launch_quad_stash(const int32_t* pred, const int32_t* acclen, const int32_t* cand,
+                               const int32_t* last, int32_t* draft, int32_t* block_in,
+                               cudaStream_t s);
 ndiff_status launch_fused_stash(const int32_t* pred2, const int32_t* acclen, const int32_t* last,
                                 int32_t* draft, int32_t* block_in, cudaStream_t s);
 

@@ -20,6 +20,7 @@ NDIFF_ERR_CUDA, NDIFF_ERR_OOM, NDIFF_ERR_WORKSPACE, NDIFF_ERR_TIMEOUT = 3, 4, 5,
 NDIFF_BF16, NDIFF_F32 = 0, 1
 NDIFF_BIDIR, NDIFF_CAUSAL = 0, 1
 NDIFF_MODE_AR, NDIFF_MODE_DIFF, NDIFF_MODE_SELFSPEC, NDIFF_MODE_SELFSPEC_FUSED = 0, 1, 2, 3
+NDIFF_MODE_SELFSPEC_QUAD = 4
 NDIFF_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -49,7 +50,8 @@ NDIFF_SAMPLER_THRESHOLD = 1
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("sampler", ctypes.c_int), ("steps", ctypes.c_int),
-                ("tau", ctypes.c_float), ("tau_revise", ctypes.c_float)]
+                ("tau", ctypes.c_float), ("tau_revise", ctypes.c_float), ("n_cand", ctypes.c_int),
+                ("cand", ctypes.c_int * 2)]
 
 
 _P = ctypes.c_void_p
@@ -342,21 +344,27 @@ class Model:
         arr = np.ascontiguousarray(np.asarray(prompt, dtype=np.int32))
         ndiff_prefill(self.handle, arr.ctypes.data, int(arr.shape[0]))
 
-    def step(self, mode: int, steps: int = 1, tau: float | None = None, tau_revise: float = 2.0):
-        """One decode cycle; with `tau` the draft uses the threshold sampler."""
+    def step(self, mode: int, steps: int = 1, tau: float | None = None, tau_revise: float = 2.0,
+             cands=None):
+        """One decode cycle; with `tau` the draft uses the threshold sampler;
+        `cands` (one or two lengths in [0, 32)) are the candidate acceptance
+        lengths of NDIFF_MODE_SELFSPEC_QUAD."""
         buf = (ctypes.c_int32 * 32)()
-        if tau is None:
+        if tau is None and cands is None:
             n = ndiff_decode_step(self.handle, mode, steps, ctypes.addressof(buf), self.stats)
         else:
-            o = DecodeOpts(mode, NDIFF_SAMPLER_THRESHOLD, steps, tau, tau_revise)
+            c = list(cands) if cands is not None else [0]
+            o = DecodeOpts(mode, NDIFF_SAMPLER_THRESHOLD if tau is not None else NDIFF_SAMPLER_TOPK,
+                           steps, 0.0 if tau is None else tau, tau_revise, len(c),
+                           (ctypes.c_int * 2)(*(c + c)[:2]))
             n = ndiff_decode_step_ex(self.handle, o, ctypes.addressof(buf), self.stats)
         return list(buf[:n])
 
     def generate(self, mode: int, n_new: int, steps: int = 1, tau: float | None = None,
-                 tau_revise: float = 2.0):
+                 tau_revise: float = 2.0, cands=None):
         out = []
         while len(out) < n_new:
-            out.extend(self.step(mode, steps, tau, tau_revise))
+            out.extend(self.step(mode, steps, tau, tau_revise, cands))
         return out[:n_new]
 
     # ---- batched sessions (batch > 1)

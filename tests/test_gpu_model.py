@@ -116,9 +116,22 @@ def _gemm_check(nd, M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 300, 128), (32, 4096, 4096), (32, 1000, 12288),
-                                   (17, 6144, 4096), (2, 24576, 4096)])
+                                   (17, 6144, 4096), (2, 24576, 4096), (1, 128, 12288),
+                                   (3, 128, 12288), (32, 256, 12288), (1, 4096, 12288)])
 def test_gemm_bf16_within_fp32_bound(nd, M, N, K):
+    """The stream-K partition gives every CTA an equal run of k-steps; a tile
+    whose k-steps span several CTAs is summed by the last one to finish (one
+    128-row tile with K = 12288 is shared by 148 CTAs)."""
     _gemm_check(nd, M, N, K, seed=M * 7 + N + K)
+
+
+def test_gemm_rows_do_not_depend_on_block_with_many_contributors(nd):
+    x, w, y = _gemm_check(nd, 32, 128, 12288, seed=6)
+    for m in (0, 3, 31):
+        one = nd.gemm_bf16(x[m:m + 1].cuda(), w.cuda()).cpu().numpy()
+        assert np.array_equal(one[0], y[m].astype(np.float32)), m
+    few = nd.gemm_bf16(x[:3].cuda(), w.cuda()).cpu().numpy()
+    assert np.array_equal(few, y[:3].astype(np.float32))
 
 
 def test_gemm_rows_do_not_depend_on_block(nd):
@@ -744,4 +757,111 @@ def test_fused_selfspec_equals_ar_8b_like_width(nd):
     ar = m.generate(0, 48)
     m.prefill(pr)
     assert m.generate(3, 48) == ar
+    m.close()
+
+
+# ---------------------------------------------------------------- quadratic self-speculation
+@pytest.mark.parametrize("cands", [(0, 1), (0, 5), (3,)])
+def test_quad_selfspec_equals_ar(nd, cands):
+    """Quadratic self-speculation emits the AR tokens exactly: the verification
+    rows of the 128-row forward are computed as in a one-token forward."""
+    c = MID_BF16
+    pr = synth.prompt(40, c["vocab"], 17)
+    m = _gpu_model(nd, c, "bf16", max_seq=800)
+    m.prefill(pr)
+    ar = m.generate(0, 96)
+    m.prefill(pr)
+    m.stats = type(m.stats)()
+    assert m.generate(nd.NDIFF_MODE_SELFSPEC_QUAD, 96, cands=cands) == ar
+    m.close()
+
+
+def _quad_run_gpu(nd, m, pr, n, cands):
+    m.prefill(pr)
+    m.stats = type(m.stats)()
+    toks, Ls, fwd = [], [], []
+    while len(toks) < n:
+        f0 = m.stats.forwards
+        toks += m.step(nd.NDIFF_MODE_SELFSPEC_QUAD, cands=cands)
+        fwd.append(int(m.stats.forwards - f0))
+        Ls.append(int(m.stats.last_accept_len))
+    return toks[:n], Ls, fwd
+
+
+def _quad_run_oracle(cfg, w, pr, n, cands, pz=None):
+    s = PZ.PerturbedSession(cfg, w, len(pr) + n + 500, pz) if pz else \
+        OM.Session(cfg, w, max_seq=len(pr) + n + 500)
+    s.prefill(pr)
+    s.generate("selfspec-quad", n, cands=cands)
+    return tuple(s.accept_lens)
+
+
+def test_quad_reuses_candidate_drafts_and_tracks_oracle(nd):
+    """16-id bf16 model with candidates 0 and 2: the tokens are the AR tokens;
+    a cycle runs its own drafting forward exactly when the previous verified
+    length (32, 0 or 2) had no draft; the sequence of acceptance lengths is the
+    oracle's (Session.step_selfspec_quadratic), under the near-tie rule of the
+    perturbation analysis."""
+    cands = (0, 2)
+    c, m = _small_model(nd, 16, max_seq=1400)
+    cfg = _ocfg(c, "bf16")
+    w = OM.Weights(cfg)
+    pr = [int(x) for x in synth.prompt(24, c["vocab"], 5)]
+    m.prefill(pr)
+    ar = m.generate(0, 200)
+    toks, Ls, fwd = _quad_run_gpu(nd, m, pr, 200, cands)
+    m.close()
+    assert toks == ar
+    drafted = False
+    for L, f in zip(Ls, fwd):
+        assert f == (1 if drafted else 2), (Ls, fwd)
+        drafted = L == 32 or L in cands
+    assert any(L in cands for L in Ls[:-1]), Ls          # candidate drafts were used
+    ref = _quad_run_oracle(cfg, w, pr, 200, cands)
+    adm = {ref} | {_quad_run_oracle(cfg, w, pr, 200, cands, PZ.Perturbation(r + 1)) for r in range(6)}
+    print(f"GPU acceptance lengths {Ls}; oracle {list(ref)}; admissible outcomes {len(adm)}")
+    if len(adm) <= 2:
+        assert tuple(Ls) in adm
+    else:
+        common = 0
+        while all(len(a) > common and a[common] == ref[common] for a in adm):
+            common += 1
+        assert tuple(Ls[:common]) == ref[:common] and common >= 3
+
+
+def test_quad_rejects_bad_candidates_and_short_caches(nd):
+    c = MID_BF16
+    m = _gpu_model(nd, c, "bf16", max_seq=300)
+    m.prefill(synth.prompt(40, c["vocab"], 17))
+    with pytest.raises(nd.NdiffError) as e:        # needs committed + 448 cache rows
+        m.step(nd.NDIFF_MODE_SELFSPEC_QUAD, cands=(0, 1))
+    assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    m.close()
+    m = _gpu_model(nd, c, "bf16", max_seq=600)
+    m.prefill(synth.prompt(40, c["vocab"], 17))
+    for bad in ((32,), (-1, 0), (0, 40)):
+        with pytest.raises(nd.NdiffError) as e:
+            m.step(nd.NDIFF_MODE_SELFSPEC_QUAD, cands=bad)
+        assert e.value.status == nd.NDIFF_ERR_INVALID_ARG
+    m.close()
+
+
+def test_mode_switches_drop_a_pending_fused_draft(nd):
+    """16-id model: after a fused cycle that accepted its whole block (a draft
+    of the next block is pending), an AR step moves the session on; the next
+    fused cycle must draft afresh, not verify the stale block (the tokens stay
+    the AR tokens)."""
+    c, m = _small_model(nd, 16)
+    pr = [int(x) for x in synth.prompt(24, c["vocab"], 5)]
+    m.prefill(pr)
+    ar = m.generate(0, 240)
+    m.prefill(pr)
+    toks, switches = [], 0
+    while len(toks) < 200:
+        toks += m.step(3)
+        if m.stats.last_accept_len == 32 and len(toks) < 200:
+            toks += m.step(0)
+            switches += 1
+    assert switches >= 1
+    assert toks[:200] == ar[:200]
     m.close()
