@@ -115,6 +115,7 @@ struct ndiff_model {
   void* aws = nullptr;          // attention split-KV scratch
   size_t aws_bytes = 0;
   int attn_split = 0;
+  int attn_split_quad = 0;      // the quadratic forward's three draft blocks (one launch)
   CUtensorMap tm_h, tm_oact, tm_a, tm_lm;
   CUtensorMap tm_h_w, tm_oact_w, tm_a_w;  // 256-row boxes for the wide kernel (B > 1)
   CUtensorMap tm_h_w64, tm_oact_w64, tm_a_w64;  // 64-row boxes: its AR forwards (B <= 64 rows)
@@ -292,7 +293,8 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
         TRY(launch_attn_bf16(qb, ly.kc, ly.vc, m->kv_len, 1, kBlock, m->Hq, m->Hkv, m->Lmax, 1,
                              scale, m->attn_split, ob, m->aws, m->aws_bytes, s));
         TRY(launch_attn_bf16(qb + blk, ly.kc, ly.vc, m->kvc, 3, kBlock, m->Hq, m->Hkv, m->Lmax, 0,
-                             scale, m->attn_split, ob + blk, m->aws, m->aws_bytes, s, m->remap, 1));
+                             scale, m->attn_split_quad, ob + blk, m->aws, m->aws_bytes, s, m->remap,
+                             1));
       } else if (fused) {
         const size_t half = (size_t)kBlock * m->HD;  // elements of one block's q / output rows
         __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
@@ -616,8 +618,12 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     NDIFF_CUDA_TRY(cudaMemsetAsync(m->gcnt, 0, (size_t)tiles * 4, s));
     m->attn_split = attn_bf16_auto_split(m->B, m->Hkv, m->Lmax);
     m->aws_bytes = attn_bf16_workspace(m->B, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
-    if (m->B == 1) {  // the quadratic forward's three draft blocks run as one batch
-      const size_t q3 = attn_bf16_workspace(3, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split);
+    if (m->B == 1) {
+      // The quadratic forward's three draft blocks run as one batch with a split
+      // length of their own (the block under verification keeps the AR split:
+      // its rows must match single-token forwards bit for bit; draft rows need not).
+      m->attn_split_quad = attn_bf16_auto_split(3, m->Hkv, m->Lmax);
+      const size_t q3 = attn_bf16_workspace(3, kBlock, m->Hq, m->Hkv, m->Lmax, m->attn_split_quad);
       if (q3 > m->aws_bytes) m->aws_bytes = q3;
     }
     if (m->aws_bytes) TRY(dalloc(m, &m->aws, m->aws_bytes));
