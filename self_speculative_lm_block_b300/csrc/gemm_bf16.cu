@@ -494,6 +494,23 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
       bool ok = mbar_wait(&acc_full[buf], (ic >> 1) & 1, p.status, abort_flag);
       if (!bar_and(ok)) break;
       tc_fence_after();
+      if (!ARGMAX && p.mode == GEMM_EPI_PARTIAL) {
+        // the partial alone, token-major so that the consumer's reads of a
+        // token row are coalesced; no counter, no merge
+        float* part = p.ws + (size_t)(c * 2 + my_slot) * MT * BM + r;
+#pragma unroll 1
+        for (int sl = 0; sl < MT / 32 && sl * 32 < p.T; ++sl) {
+          float v[32];
+          tmem_ld32(tl + buf * MT + sl * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (sl * 32 + j < p.T) __stcg(part + (size_t)(sl * 32 + j) * BM, v[j]);
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
       if constexpr (MT > 64) {
         // 32-column slices (registers): the accumulator stays in TMEM until the
         // segment is done; per column the arithmetic is that of the narrow
@@ -725,6 +742,11 @@ GemmPlan gemm_plan(int N, int K) {
   pl.nchunks = 1;
   pl.items = pl.ntiles;
   return pl;
+}
+
+bool gemm_plan_all_split(const GemmPlan& pl) {
+  const long long U = (long long)pl.ntiles * pl.nks;
+  return (U + pl.grid - 1) / pl.grid < pl.nks;
 }
 
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt) {

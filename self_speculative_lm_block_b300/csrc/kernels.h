@@ -61,7 +61,13 @@ ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, i
                                   int32_t* kv_len, cudaStream_t stream);
 
 // gemm_bf16.cu — y = x W^T for at most 32 token rows, with fused epilogues
-enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3, GEMM_EPI_ARGMAX = 4 };
+// GEMM_EPI_PARTIAL (weight-streaming kernel, plans without whole tiles): every
+// segment stores its partial tile at ws[((c * 2 + slot) * MT + m) * 128 + r]
+// (CTA c, slot 0 for its first segment when it starts inside the tile, else 1;
+// token row m, tile row r) and nothing else; the consumer adds the partials
+// of a tile in contributor order (launch_residual_rmsnorm).
+enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3, GEMM_EPI_ARGMAX = 4,
+       GEMM_EPI_PARTIAL = 5 };
 
 struct GemmParams {
   int N, T, mode;          // weight rows, valid token rows (<= 32), epilogue
@@ -104,6 +110,9 @@ struct GemmPlan {
 // (four blocks: the quadratic forward). The K split depends on (N, K) only,
 // so a row's arithmetic is the same for every row count and every mt.
 GemmPlan gemm_plan(int N, int K);
+// Whether every CTA's run of k-steps is shorter than a tile, so every tile is
+// split and GEMM_EPI_PARTIAL applies.
+bool gemm_plan_all_split(const GemmPlan& pl);
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt = 32);
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
                             CUtensorMap* tmW, CUtensorMap* tmX, int mt = 32);

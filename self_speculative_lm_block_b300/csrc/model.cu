@@ -131,6 +131,10 @@ struct ndiff_model {
   bool have_draft = false;      // the last fused forward left a draft of the next block
   int last_L0 = -1;             // accept length of sequence 0 in the last verification
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
+  // The output and down projections of a single-sequence bf16 model leave their
+  // partial tiles unsummed when every tile is split; the RMSNorm that follows
+  // adds them to the residual stream (no merge at the projection's end).
+  bool part_o = false, part_d = false;
   int32_t* pin = nullptr;       // pinned host staging [pin_n]
   size_t pin_n = 0;
   int32_t* last_dev = nullptr;  // [B] pending last token per sequence
@@ -266,9 +270,18 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     if (quad) return launch_gemm_bf16(tw, xm.x128, pl, p, s, mt);
     return launch_gemm_bf16(tw, xm.x32, pl, p, s);
   };
+  // the residual add of an output / down projection whose partial tiles were
+  // left unsummed, fused with the RMSNorm that follows it
+  auto norm_after = [&](bool partial, const GemmPlan& pl) -> ndiff_status {
+    if (!partial) return launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s);
+    return launch_residual_rmsnorm(m->x, M, m->d, m->eps, static_cast<__nv_bfloat16*>(m->h), m->gws,
+                                   mt, pl.nks, pl.ntiles * pl.nks, pl.grid, s);
+  };
+  const bool part_o = m->bf16 && !wide && m->part_o;
+  const bool part_d = m->bf16 && !wide && m->part_d;
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
-    TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s));
+    TRY(norm_after(l > 0 && part_d, m->pl_d));
     if (m->bf16) {
       GemmParams p = gp;
       p.N = m->NQKV;
@@ -309,11 +322,11 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       }
       p = gp;
       p.N = m->d;
-      p.mode = GEMM_EPI_RESID;
+      p.mode = part_o ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
       TRY(proj(ly.tm_o, xo, m->pl_o, m->d, m->HD, p));
-      TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, true, s));
+      TRY(norm_after(part_o, m->pl_o));
       p = gp;
       p.N = 2 * m->ffn;
       p.mode = GEMM_EPI_SWIGLU;
@@ -322,7 +335,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       TRY(proj(ly.tm_gu, xh, m->pl_gu, 2 * m->ffn, m->d, p));
       p = gp;
       p.N = m->d;
-      p.mode = GEMM_EPI_RESID;
+      p.mode = part_d ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
       p.out = m->x;
       p.ldo = m->d;
       TRY(proj(ly.tm_d, xa, m->pl_d, m->d, m->ffn, p));
@@ -348,8 +361,9 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       TRY(launch_resid_add_f32(m->x, m->y, T * m->d, s));
     }
   }
+  // (a forward that leaves nothing but the KV cache needs no final residual)
   if (out == FWD_NONE) return NDIFF_OK;
-  TRY(launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s));
+  TRY(norm_after(part_d, m->pl_d));
   if (m->bf16 && out == FWD_TOKENS) {
     GemmParams p = gp;
     p.N = m->V;
@@ -604,6 +618,8 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     m->pl_gu = gemm_plan(2 * m->ffn, m->d);
     m->pl_d = gemm_plan(m->d, m->ffn);
     m->pl_lm = gemm_plan(m->V, m->d);
+    m->part_o = m->B == 1 && gemm_plan_all_split(m->pl_o);
+    m->part_d = m->B == 1 && gemm_plan_all_split(m->pl_d);
     const GemmPlan* pls[5] = {&m->pl_qkv, &m->pl_o, &m->pl_gu, &m->pl_d, &m->pl_lm};
     size_t ws = 16;
     int tiles = 1;

@@ -178,6 +178,92 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int d, flo
   }
 }
 
+// The residual add of a projection whose partial tiles were left unsummed
+// (GEMM_EPI_PARTIAL) fused with the RMSNorm that follows it: for token row m,
+//   x[m][n] += sum over the contributors of n's tile, in k order, of their
+//              partials (the stream-K partition of U k-steps over G CTAs),
+//   h[m] = bf16(x[m] / sqrt(mean(x[m]^2) + eps)).
+// One CTA per row with one warp per 128-column tile (up to 32 warps; more
+// tiles: warp w also takes w + 32, ...), lane l on columns 4l .. 4l+3
+// (16-byte loads). A tile's x and the partials of its first six contributors
+// are loaded together, then added in contributor order. Every sum has a fixed
+// order (lane, warp-shuffle tree, warps in order), so a row's result does not
+// depend on the other rows. Requires d % 128 == 0.
+constexpr int RR_BATCH = 6;   // contributors whose partials are loaded together
+
+template <int MT>
+__global__ void __launch_bounds__(1024)
+    residual_rmsnorm_kernel(float* __restrict__ x, int d, float eps, __nv_bfloat16* __restrict__ h,
+                            const float* __restrict__ part, int nks, int U, int G) {
+  griddep_launch();
+  griddep_wait();
+  const int m = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int ntile = d >> 7;
+  float* xr = x + (size_t)m * d;
+  float ss = 0.f;
+  for (int t = warp; t < ntile; t += nw) {  // uniform over the warp
+    const int t0 = t * nks;
+    const int cf = ((t0 + 1) * G - 1) / U, cl = ((t0 + nks) * G - 1) / U;
+    float4* xp = reinterpret_cast<float4*>(xr + t * 128 + lane * 4);
+    const float4 xo = *xp;
+    float4 pv[RR_BATCH];
+#pragma unroll
+    for (int j = 0; j < RR_BATCH; ++j) {
+      const int c = cf + j;
+      pv[j] = c <= cl ? __ldcg(reinterpret_cast<const float4*>(
+                            part + ((size_t)(c * 2 + (j == 0 ? 1 : 0)) * MT + m) * 128 + lane * 4))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < RR_BATCH; ++j) {
+      if (cf + j <= cl) {
+        acc.x += pv[j].x;
+        acc.y += pv[j].y;
+        acc.z += pv[j].z;
+        acc.w += pv[j].w;
+      }
+    }
+    for (int c = cf + RR_BATCH; c <= cl; ++c) {  // tiles with more contributors
+      const float4 q =
+          __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(c * 2) * MT + m) * 128 + lane * 4));
+      acc.x += q.x;
+      acc.y += q.y;
+      acc.z += q.z;
+      acc.w += q.w;
+    }
+    const float4 v = make_float4(xo.x + acc.x, xo.y + acc.y, xo.z + acc.z, xo.w + acc.w);
+    *xp = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float wsum[32];
+  __shared__ float inv_s;
+  if (lane == 0) wsum[warp] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += wsum[w];
+    inv_s = 1.f / sqrtf(t / (float)d + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  for (int t = warp; t < ntile; t += nw) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + t * 128 + lane * 4);
+    uint2 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x * inv)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y * inv)) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z * inv)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w * inv)) << 16);
+    *reinterpret_cast<uint2*>(h + (size_t)m * d + t * 128 + lane * 4) = o;
+  }
+}
+
 // y[m][n] = sum_k x[m][k] W[n][k] in fp32: one warp per (n, m), lane-strided
 // partial sums merged by a fixed shuffle tree.
 __global__ void __launch_bounds__(256) linear_f32_kernel(const float* x, int ldx, const float* W,
@@ -409,6 +495,26 @@ ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, i
   else
     NDIFF_CUDA_TRY(launch_k(mk::embed_kernel<false>, dim3(T), dim3(256), 0, s, E, ids, V, d, x,
                             device_status_word()));
+  return NDIFF_OK;
+}
+
+ndiff_status launch_residual_rmsnorm(float* x, int T, int d, float eps, __nv_bfloat16* h,
+                                     const float* part, int mt, int nks, int U, int G, cudaStream_t s) {
+  if (T <= 0) return NDIFF_OK;
+  if (d % 128 != 0)
+    return set_error(NDIFF_ERR_UNSUPPORTED, "residual_rmsnorm: d_model %d is not a multiple of 128", d);
+  const int threads = (d / 128) * 32 < 1024 ? (d / 128) * 32 : 1024;
+  if (mt == 32)
+    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<32>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
+                            part, nks, U, G));
+  else if (mt == 64)
+    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<64>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
+                            part, nks, U, G));
+  else if (mt == 128)
+    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<128>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
+                            part, nks, U, G));
+  else
+    return set_error(NDIFF_ERR_UNSUPPORTED, "residual_rmsnorm: %d token columns", mt);
   return NDIFF_OK;
 }
 

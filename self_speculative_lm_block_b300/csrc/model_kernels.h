@@ -25,6 +25,11 @@ ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int6
 ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaStream_t s);
 ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
                           float* x, cudaStream_t s);
+// x += the unsummed partial tiles of a GEMM_EPI_PARTIAL projection (mt token
+// columns, stream-K partition of U k-steps over G CTAs, nks k-steps a tile),
+// then h = bf16(RMSNorm(x)), for token rows 0..T-1.
+ndiff_status launch_residual_rmsnorm(float* x, int T, int d, float eps, __nv_bfloat16* h,
+                                     const float* part, int mt, int nks, int U, int G, cudaStream_t s);
 ndiff_status launch_rmsnorm(const float* x, int T, int d, float eps, void* out, bool bf16,
                             cudaStream_t s);
 ndiff_status launch_linear_f32(const float* x, int ldx, const float* W, int N, int K, float* y,
