@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
       if (!ARGMAX && p.mode == GEMM_EPI_PARTIAL) {
         // the partial alone, token-major so that the consumer's reads of a
         // token row are coalesced; no counter, no merge
-        float* part = p.ws + (size_t)(c * 2 + my_slot) * MT * BM + r;
+        float* part = p.ws + (size_t)(c * p.maxseg + ic) * MT * BM + r;
 #pragma unroll 1
         for (int sl = 0; sl < MT / 32 && sl * 32 < p.T; ++sl) {
           float v[32];
@@ -744,9 +744,14 @@ GemmPlan gemm_plan(int N, int K) {
   return pl;
 }
 
-bool gemm_plan_all_split(const GemmPlan& pl) {
+int gemm_plan_maxseg(const GemmPlan& pl) {
   const long long U = (long long)pl.ntiles * pl.nks;
-  return (U + pl.grid - 1) / pl.grid < pl.nks;
+  const long long run = (U + pl.grid - 1) / pl.grid;  // longest run of k-steps
+  return (int)((run + pl.nks - 1) / pl.nks) + 1;
+}
+
+size_t gemm_partial_only_bytes(const GemmPlan& pl, int mt) {
+  return (size_t)pl.grid * gemm_plan_maxseg(pl) * mt * gemm::BM * sizeof(float);
 }
 
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt) {

@@ -61,11 +61,11 @@ ndiff_status launch_verify_accept(const int32_t* draft, const int32_t* target, i
                                   int32_t* kv_len, cudaStream_t stream);
 
 // gemm_bf16.cu — y = x W^T for at most 32 token rows, with fused epilogues
-// GEMM_EPI_PARTIAL (weight-streaming kernel, plans without whole tiles): every
-// segment stores its partial tile at ws[((c * 2 + slot) * MT + m) * 128 + r]
-// (CTA c, slot 0 for its first segment when it starts inside the tile, else 1;
-// token row m, tile row r) and nothing else; the consumer adds the partials
-// of a tile in contributor order (launch_residual_rmsnorm).
+// GEMM_EPI_PARTIAL (weight-streaming kernel): segment s of CTA c (its part of
+// one tile; s counts from 0 in k order) stores its partial tile at
+// ws[((c * maxseg + s) * MT + m) * 128 + r] (token row m, tile row r) and does
+// nothing else; a consumer kernel adds a tile's partials in contributor order
+// (partial_slot gives contributor c's segment index for tile t).
 enum { GEMM_EPI_F32 = 0, GEMM_EPI_RESID = 1, GEMM_EPI_SWIGLU = 2, GEMM_EPI_QKV = 3, GEMM_EPI_ARGMAX = 4,
        GEMM_EPI_PARTIAL = 5 };
 
@@ -74,6 +74,7 @@ struct GemmParams {
   int w_tiled;             // W stored as contiguous 128 x 64 tiles (else row-major)
   int S, nks, items;       // wide kernel: K splits, 64-wide K steps, work items (set by the launcher)
   int ntiles;              // weight-streaming kernel: 128-row tiles (set by the launcher)
+  int maxseg;              // GEMM_EPI_PARTIAL: segment slots per CTA (gemm_plan_maxseg)
   float* ws;               // weight-streaming kernel: partial tiles [grid][2][128][MT] fp32
   int* counters;           // [tiles] arrival counters, zero between launches
   unsigned int* status;    // device status word
@@ -110,9 +111,10 @@ struct GemmPlan {
 // (four blocks: the quadratic forward). The K split depends on (N, K) only,
 // so a row's arithmetic is the same for every row count and every mt.
 GemmPlan gemm_plan(int N, int K);
-// Whether every CTA's run of k-steps is shorter than a tile, so every tile is
-// split and GEMM_EPI_PARTIAL applies.
-bool gemm_plan_all_split(const GemmPlan& pl);
+// Most segments (tiles touched) of one CTA's run of k-steps under the plan.
+int gemm_plan_maxseg(const GemmPlan& pl);
+// GEMM_EPI_PARTIAL workspace: [grid][maxseg][mt][128] fp32.
+size_t gemm_partial_only_bytes(const GemmPlan& pl, int mt);
 size_t gemm_partials_bytes(const GemmPlan& pl, int mt = 32);
 ndiff_status gemm_make_maps(const void* w, int N, int K, bool w_tiled, const void* x, int M,
                             CUtensorMap* tmW, CUtensorMap* tmX, int mt = 32);

@@ -131,10 +131,6 @@ struct ndiff_model {
   bool have_draft = false;      // the last fused forward left a draft of the next block
   int last_L0 = -1;             // accept length of sequence 0 in the last verification
   GemmPlan pl_qkv, pl_o, pl_gu, pl_d, pl_lm;
-  // The output and down projections of a single-sequence bf16 model leave their
-  // partial tiles unsummed when every tile is split; the RMSNorm that follows
-  // adds them to the residual stream (no merge at the projection's end).
-  bool part_o = false, part_d = false;
   int32_t* pin = nullptr;       // pinned host staging [pin_n]
   size_t pin_n = 0;
   int32_t* last_dev = nullptr;  // [B] pending last token per sequence
@@ -270,22 +266,34 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
     if (quad) return launch_gemm_bf16(tw, xm.x128, pl, p, s, mt);
     return launch_gemm_bf16(tw, xm.x32, pl, p, s);
   };
-  // the residual add of an output / down projection whose partial tiles were
-  // left unsummed, fused with the RMSNorm that follows it
+  // One bf16 sequence: every layer projection leaves its partial tiles unsummed
+  // (GEMM_EPI_PARTIAL, no merge at the projection's end) and the kernel after
+  // it sums them: the QKV merge (RoPE, q and the block's K/V), the residual
+  // add fused with the next RMSNorm (output and down projections), the SwiGLU
+  // merge. A batch runs the wide kernel with its fused epilogues.
+  const bool defer = m->bf16 && !wide;
+  auto pp_of = [&](const GemmPlan& pl) {
+    PartialPlan pp;
+    pp.part = m->gws;
+    pp.nks = pl.nks;
+    pp.U = pl.ntiles * pl.nks;
+    pp.G = pl.grid;
+    pp.maxseg = gemm_plan_maxseg(pl);
+    return pp;
+  };
   auto norm_after = [&](bool partial, const GemmPlan& pl) -> ndiff_status {
     if (!partial) return launch_rmsnorm(m->x, M, m->d, m->eps, m->h, m->bf16, s);
-    return launch_residual_rmsnorm(m->x, M, m->d, m->eps, static_cast<__nv_bfloat16*>(m->h), m->gws,
-                                   mt, pl.nks, pl.ntiles * pl.nks, pl.grid, s);
+    return launch_residual_rmsnorm(m->x, M, m->d, m->eps, static_cast<__nv_bfloat16*>(m->h), pp_of(pl),
+                                   mt, s);
   };
-  const bool part_o = m->bf16 && !wide && m->part_o;
-  const bool part_d = m->bf16 && !wide && m->part_d;
   for (int l = 0; l < m->L; ++l) {
     Layer& ly = m->layers[l];
-    TRY(norm_after(l > 0 && part_d, m->pl_d));
+    TRY(norm_after(l > 0 && defer, m->pl_d));
     if (m->bf16) {
       GemmParams p = gp;
       p.N = m->NQKV;
-      p.mode = GEMM_EPI_QKV;
+      p.mode = defer ? GEMM_EPI_PARTIAL : GEMM_EPI_QKV;
+      p.maxseg = gemm_plan_maxseg(m->pl_qkv);
       p.q = static_cast<__nv_bfloat16*>(m->qb);
       p.kc = static_cast<__nv_bfloat16*>(ly.kc);
       p.vc = static_cast<__nv_bfloat16*>(ly.vc);
@@ -296,6 +304,9 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       p.rope = m->rope;
       p.blk_pos = quad ? m->blk_pos : nullptr;
       TRY(proj(ly.tm_qkv, xh, m->pl_qkv, m->NQKV, m->d, p));
+      if (defer)
+        TRY(launch_qkv_merge(pp_of(m->pl_qkv), M, m->Hq, m->Hkv, m->Lmax, m->kv_len, p.blk_pos, m->rope,
+                             p.q, p.kc, p.vc, mt, s));
       if (quad) {
         // the block under verification (causal at prefix P), then its three
         // draft blocks as one batch over the same cache (bidirectional, each at
@@ -322,20 +333,25 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       }
       p = gp;
       p.N = m->d;
-      p.mode = part_o ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
+      p.mode = defer ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
+      p.maxseg = gemm_plan_maxseg(m->pl_o);
       p.out = m->x;
       p.ldo = m->d;
       TRY(proj(ly.tm_o, xo, m->pl_o, m->d, m->HD, p));
-      TRY(norm_after(part_o, m->pl_o));
+      TRY(norm_after(defer, m->pl_o));
       p = gp;
       p.N = 2 * m->ffn;
-      p.mode = GEMM_EPI_SWIGLU;
+      p.mode = defer ? GEMM_EPI_PARTIAL : GEMM_EPI_SWIGLU;
+      p.maxseg = gemm_plan_maxseg(m->pl_gu);
       p.act = static_cast<__nv_bfloat16*>(m->ab);
       p.lda = m->ffn;
       TRY(proj(ly.tm_gu, xh, m->pl_gu, 2 * m->ffn, m->d, p));
+      if (defer)
+        TRY(launch_swiglu_merge(pp_of(m->pl_gu), m->pl_gu.ntiles, M, p.act, p.lda, mt, s));
       p = gp;
       p.N = m->d;
-      p.mode = part_d ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
+      p.mode = defer ? GEMM_EPI_PARTIAL : GEMM_EPI_RESID;
+      p.maxseg = gemm_plan_maxseg(m->pl_d);
       p.out = m->x;
       p.ldo = m->d;
       TRY(proj(ly.tm_d, xa, m->pl_d, m->d, m->ffn, p));
@@ -363,7 +379,7 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
   }
   // (a forward that leaves nothing but the KV cache needs no final residual)
   if (out == FWD_NONE) return NDIFF_OK;
-  TRY(norm_after(part_d, m->pl_d));
+  TRY(norm_after(defer, m->pl_d));
   if (m->bf16 && out == FWD_TOKENS) {
     GemmParams p = gp;
     p.N = m->V;
@@ -618,13 +634,17 @@ ndiff_status create(const ndiff_model_config* cfg, uint64_t seed, ndiff_model* m
     m->pl_gu = gemm_plan(2 * m->ffn, m->d);
     m->pl_d = gemm_plan(m->d, m->ffn);
     m->pl_lm = gemm_plan(m->V, m->d);
-    m->part_o = m->B == 1 && gemm_plan_all_split(m->pl_o);
-    m->part_d = m->B == 1 && gemm_plan_all_split(m->pl_d);
+
     const GemmPlan* pls[5] = {&m->pl_qkv, &m->pl_o, &m->pl_gu, &m->pl_d, &m->pl_lm};
     size_t ws = 16;
     int tiles = 1;
+    const int mtmax = m->B > 1 ? 2 * kBlock : 4 * kBlock;
     for (const GemmPlan* pl : pls) {
-      const size_t b = gemm_partials_bytes(*pl, m->B > 1 ? 2 * kBlock : 4 * kBlock);
+      size_t b = gemm_partials_bytes(*pl, mtmax);
+      if (pl != &m->pl_lm && m->B == 1) {  // the layer projections leave unsummed partials
+        const size_t b2 = gemm_partial_only_bytes(*pl, mtmax);
+        b = b2 > b ? b2 : b;
+      }
       if (b > ws) ws = b;
       if (pl->ntiles > tiles) tiles = pl->ntiles;
     }

@@ -178,23 +178,57 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int d, flo
   }
 }
 
-// The residual add of a projection whose partial tiles were left unsummed
-// (GEMM_EPI_PARTIAL) fused with the RMSNorm that follows it: for token row m,
-//   x[m][n] += sum over the contributors of n's tile, in k order, of their
-//              partials (the stream-K partition of U k-steps over G CTAs),
-//   h[m] = bf16(x[m] / sqrt(mean(x[m]^2) + eps)).
-// One CTA per row with one warp per 128-column tile (up to 32 warps; more
-// tiles: warp w also takes w + 32, ...), lane l on columns 4l .. 4l+3
-// (16-byte loads). A tile's x and the partials of its first six contributors
-// are loaded together, then added in contributor order. Every sum has a fixed
-// order (lane, warp-shuffle tree, warps in order), so a row's result does not
-// depend on the other rows. Requires d % 128 == 0.
-constexpr int RR_BATCH = 6;   // contributors whose partials are loaded together
+// ---------------------------------------------------------------- partial tiles
+// Consumers of a projection that left its partial tiles unsummed
+// (GEMM_EPI_PARTIAL). Tile t of a stream-K partition (U k-steps over G CTAs,
+// nks k-steps a tile) is covered by CTAs cf..cl in k order; CTA c keeps its
+// segment of tile t in slot c * maxseg + (t - start(c) / nks), start(c) =
+// c * U / G. A tile's partials are summed in contributor order, the first
+// RR_BATCH of them loaded together (16 bytes a lane: 4 tile rows of one token
+// row). These sums are the same for every token row and every row count.
+constexpr int RR_BATCH = 6;
 
+template <int MT>
+__device__ __forceinline__ float4 tile_sum4(const PartialPlan& pp, int t, int m, int row4) {
+  const int t0 = t * pp.nks;
+  const int cf = ((t0 + 1) * pp.G - 1) / pp.U, cl = ((t0 + pp.nks) * pp.G - 1) / pp.U;
+  auto at = [&](int c) {
+    const int s = t - (c * pp.U / pp.G) / pp.nks;
+    return reinterpret_cast<const float4*>(pp.part + ((size_t)(c * pp.maxseg + s) * MT + m) * 128 + row4);
+  };
+  float4 pv[RR_BATCH];
+#pragma unroll
+  for (int j = 0; j < RR_BATCH; ++j) pv[j] = cf + j <= cl ? __ldcg(at(cf + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < RR_BATCH; ++j) {
+    if (cf + j <= cl) {
+      acc.x += pv[j].x;
+      acc.y += pv[j].y;
+      acc.z += pv[j].z;
+      acc.w += pv[j].w;
+    }
+  }
+  for (int c = cf + RR_BATCH; c <= cl; ++c) {  // tiles with more contributors
+    const float4 q = __ldcg(at(c));
+    acc.x += q.x;
+    acc.y += q.y;
+    acc.z += q.z;
+    acc.w += q.w;
+  }
+  return acc;
+}
+
+// Residual add of the output / down projection fused with the RMSNorm that
+// follows: for token row m,
+//   x[m][n] += the summed partial of column n,  h[m] = bf16(x[m] / rms(x[m])).
+// One CTA per row, one warp per 128-column tile (up to 32 warps; warp w also
+// takes tiles w + 32, ...), lane l on columns 4l .. 4l+3. The sum of squares
+// runs lane, warp-shuffle tree, warps in order. Requires d % 128 == 0.
 template <int MT>
 __global__ void __launch_bounds__(1024)
     residual_rmsnorm_kernel(float* __restrict__ x, int d, float eps, __nv_bfloat16* __restrict__ h,
-                            const float* __restrict__ part, int nks, int U, int G) {
+                            const PartialPlan pp) {
   griddep_launch();
   griddep_wait();
   const int m = blockIdx.x;
@@ -203,36 +237,9 @@ __global__ void __launch_bounds__(1024)
   float* xr = x + (size_t)m * d;
   float ss = 0.f;
   for (int t = warp; t < ntile; t += nw) {  // uniform over the warp
-    const int t0 = t * nks;
-    const int cf = ((t0 + 1) * G - 1) / U, cl = ((t0 + nks) * G - 1) / U;
     float4* xp = reinterpret_cast<float4*>(xr + t * 128 + lane * 4);
     const float4 xo = *xp;
-    float4 pv[RR_BATCH];
-#pragma unroll
-    for (int j = 0; j < RR_BATCH; ++j) {
-      const int c = cf + j;
-      pv[j] = c <= cl ? __ldcg(reinterpret_cast<const float4*>(
-                            part + ((size_t)(c * 2 + (j == 0 ? 1 : 0)) * MT + m) * 128 + lane * 4))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < RR_BATCH; ++j) {
-      if (cf + j <= cl) {
-        acc.x += pv[j].x;
-        acc.y += pv[j].y;
-        acc.z += pv[j].z;
-        acc.w += pv[j].w;
-      }
-    }
-    for (int c = cf + RR_BATCH; c <= cl; ++c) {  // tiles with more contributors
-      const float4 q =
-          __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(c * 2) * MT + m) * 128 + lane * 4));
-      acc.x += q.x;
-      acc.y += q.y;
-      acc.z += q.z;
-      acc.w += q.w;
-    }
+    const float4 acc = tile_sum4<MT>(pp, t, m, lane * 4);
     const float4 v = make_float4(xo.x + acc.x, xo.y + acc.y, xo.z + acc.z, xo.w + acc.w);
     *xp = v;
     ss = fmaf(v.x, v.x, ss);
@@ -261,6 +268,69 @@ __global__ void __launch_bounds__(1024)
     o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z * inv)) |
           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w * inv)) << 16);
     *reinterpret_cast<uint2*>(h + (size_t)m * d + t * 128 + lane * 4) = o;
+  }
+}
+
+// SwiGLU of the gate/up projection: tile rows 2i and 2i+1 hold gate j and up j
+// (j = tile * 64 + i); act[m][j] = bf16(silu(g) * u), the expression of the
+// projection kernel's SwiGLU epilogue. Grid (tiles / 8, token rows), one warp
+// a tile, lane l on rows 4l .. 4l+3 (two gate/up pairs).
+template <int MT>
+__global__ void __launch_bounds__(256)
+    swiglu_merge_kernel(const PartialPlan pp, int ntile, __nv_bfloat16* __restrict__ act, int64_t lda) {
+  griddep_launch();
+  griddep_wait();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), m = blockIdx.y, lane = threadIdx.x & 31;
+  if (t >= ntile) return;
+  const float4 y = tile_sum4<MT>(pp, t, m, lane * 4);
+  const float a0 = y.x / (1.f + expf(-y.x)) * y.y;
+  const float a1 = y.z / (1.f + expf(-y.z)) * y.w;
+  const uint32_t o = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a0)) |
+                     ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a1)) << 16);
+  *reinterpret_cast<uint32_t*>(act + (size_t)m * lda + t * 64 + lane * 2) = o;
+}
+
+// QKV of one sequence: tile h is one head (q heads, then k, then v). In q and
+// k heads rows 2i / 2i+1 hold dims i / i+64 (the RoPE pair) and are rotated
+// by the position's (cos, sin) with the expressions of the projection
+// kernel's QKV epilogue; v rows are dims in order. q goes to q[m][h][128], k
+// and v to the caches at the token's cache row. Positions and cache rows:
+// kv_len[0] + m, or with blk_pos those of the token's 32-row block. Grid
+// (heads, token rows), one warp; lane l on rows 4l .. 4l+3.
+template <int MT>
+__global__ void __launch_bounds__(32)
+    qkv_merge_kernel(const PartialPlan pp, int T, int Hq, int Hkv, int Lmax, const int32_t* kv_len,
+                     const int32_t* blk_pos, const float2* __restrict__ rope,
+                     __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ kc,
+                     __nv_bfloat16* __restrict__ vc, unsigned int* status) {
+  griddep_launch();
+  griddep_wait();
+  const int h = blockIdx.x, m = blockIdx.y, lane = threadIdx.x;
+  const int P = checked_prefix(kv_len[0], Lmax - T, status);
+  const int pos = blk_pos != nullptr ? blk_pos[2 * (m >> 5)] + (m & 31) : P + m;
+  const int slot = blk_pos != nullptr ? blk_pos[2 * (m >> 5) + 1] + (m & 31) : P + m;
+  const float4 y = tile_sum4<MT>(pp, h, m, lane * 4);
+  if (h < Hq + Hkv) {
+    // rows 4l, 4l+1: dims 2l, 2l+64; rows 4l+2, 4l+3: dims 2l+1, 2l+65
+    const float4 cs = __ldg(reinterpret_cast<const float4*>(rope + (size_t)pos * 64 + 2 * lane));
+    const float e0 = y.x * cs.x - y.y * cs.y, o0 = y.y * cs.x + y.x * cs.y;
+    const float e1 = y.z * cs.z - y.w * cs.w, o1 = y.w * cs.z + y.z * cs.w;
+    __nv_bfloat16* dst = h < Hq ? q + ((size_t)m * Hq + h) * 128
+                                : kc + ((size_t)(h - Hq) * Lmax + slot) * 128;
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(e0)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(e1)) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o0)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o1)) << 16);
+    *reinterpret_cast<uint32_t*>(dst + 2 * lane) = lo;
+    *reinterpret_cast<uint32_t*>(dst + 64 + 2 * lane) = hi;
+  } else {
+    __nv_bfloat16* dst = vc + ((size_t)(h - Hq - Hkv) * Lmax + slot) * 128 + 4 * lane;
+    uint2 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+    *reinterpret_cast<uint2*>(dst) = o;
   }
 }
 
@@ -498,23 +568,42 @@ ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, i
   return NDIFF_OK;
 }
 
+#define NDIFF_MT_DISPATCH(KERNEL, MT, GRID, BLOCK, ...)                                     \
+  do {                                                                                     \
+    if ((MT) == 32)                                                                        \
+      NDIFF_CUDA_TRY(launch_k(KERNEL<32>, GRID, BLOCK, 0, s, __VA_ARGS__));               \
+    else if ((MT) == 64)                                                                   \
+      NDIFF_CUDA_TRY(launch_k(KERNEL<64>, GRID, BLOCK, 0, s, __VA_ARGS__));               \
+    else if ((MT) == 128)                                                                  \
+      NDIFF_CUDA_TRY(launch_k(KERNEL<128>, GRID, BLOCK, 0, s, __VA_ARGS__));              \
+    else                                                                                   \
+      return set_error(NDIFF_ERR_UNSUPPORTED, "partial tiles of %d token columns", (MT)); \
+  } while (0)
+
 ndiff_status launch_residual_rmsnorm(float* x, int T, int d, float eps, __nv_bfloat16* h,
-                                     const float* part, int mt, int nks, int U, int G, cudaStream_t s) {
+                                     const PartialPlan& pp, int mt, cudaStream_t s) {
   if (T <= 0) return NDIFF_OK;
   if (d % 128 != 0)
     return set_error(NDIFF_ERR_UNSUPPORTED, "residual_rmsnorm: d_model %d is not a multiple of 128", d);
   const int threads = (d / 128) * 32 < 1024 ? (d / 128) * 32 : 1024;
-  if (mt == 32)
-    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<32>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
-                            part, nks, U, G));
-  else if (mt == 64)
-    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<64>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
-                            part, nks, U, G));
-  else if (mt == 128)
-    NDIFF_CUDA_TRY(launch_k(mk::residual_rmsnorm_kernel<128>, dim3(T), dim3(threads), 0, s, x, d, eps, h,
-                            part, nks, U, G));
-  else
-    return set_error(NDIFF_ERR_UNSUPPORTED, "residual_rmsnorm: %d token columns", mt);
+  NDIFF_MT_DISPATCH(mk::residual_rmsnorm_kernel, mt, dim3(T), dim3(threads), x, d, eps, h, pp);
+  return NDIFF_OK;
+}
+
+ndiff_status launch_swiglu_merge(const PartialPlan& pp, int ntile, int T, __nv_bfloat16* act, int64_t lda,
+                                 int mt, cudaStream_t s) {
+  if (T <= 0) return NDIFF_OK;
+  NDIFF_MT_DISPATCH(mk::swiglu_merge_kernel, mt, dim3((ntile + 7) / 8, T), dim3(256), pp, ntile, act, lda);
+  return NDIFF_OK;
+}
+
+ndiff_status launch_qkv_merge(const PartialPlan& pp, int T, int Hq, int Hkv, int Lmax,
+                              const int32_t* kv_len, const int32_t* blk_pos, const float2* rope,
+                              __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int mt,
+                              cudaStream_t s) {
+  if (T <= 0) return NDIFF_OK;
+  NDIFF_MT_DISPATCH(mk::qkv_merge_kernel, mt, dim3(Hq + 2 * Hkv, T), dim3(32), pp, T, Hq, Hkv, Lmax,
+                    kv_len, blk_pos, rope, q, kc, vc, device_status_word());
   return NDIFF_OK;
 }
 

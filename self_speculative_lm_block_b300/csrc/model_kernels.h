@@ -25,11 +25,27 @@ ndiff_status launch_gather_weight(const void* src, bool bf16, int64_t cols, int6
 ndiff_status launch_rope_table(float2* tab, int Lmax, int D, double base, cudaStream_t s);
 ndiff_status launch_embed(const void* E, bool bf16, const int32_t* ids, int T, int V, int d,
                           float* x, cudaStream_t s);
-// x += the unsummed partial tiles of a GEMM_EPI_PARTIAL projection (mt token
-// columns, stream-K partition of U k-steps over G CTAs, nks k-steps a tile),
-// then h = bf16(RMSNorm(x)), for token rows 0..T-1.
+// The unsummed partial tiles of a GEMM_EPI_PARTIAL projection of mt token
+// columns: the workspace and the stream-K partition (U k-steps over G CTAs,
+// nks k-steps a tile, maxseg slots a CTA).
+struct PartialPlan {
+  const float* part;
+  int nks, U, G, maxseg;
+};
+
+// x += the projection's summed partials, then h = bf16(RMSNorm(x)), for token
+// rows 0..T-1 (the output / down projection and the norm after it).
 ndiff_status launch_residual_rmsnorm(float* x, int T, int d, float eps, __nv_bfloat16* h,
-                                     const float* part, int mt, int nks, int U, int G, cudaStream_t s);
+                                     const PartialPlan& pp, int mt, cudaStream_t s);
+// act = SwiGLU of the summed gate/up partials (ntile 128-row tiles).
+ndiff_status launch_swiglu_merge(const PartialPlan& pp, int ntile, int T, __nv_bfloat16* act, int64_t lda,
+                                 int mt, cudaStream_t s);
+// q and the block's K/V cache rows from the summed QKV partials (RoPE on q and
+// k; positions / cache rows kv_len[0] + m, or per 32-row block from blk_pos).
+ndiff_status launch_qkv_merge(const PartialPlan& pp, int T, int Hq, int Hkv, int Lmax,
+                              const int32_t* kv_len, const int32_t* blk_pos, const float2* rope,
+                              __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int mt,
+                              cudaStream_t s);
 ndiff_status launch_rmsnorm(const float* x, int T, int d, float eps, void* out, bool bf16,
                             cudaStream_t s);
 ndiff_status launch_linear_f32(const float* x, int ldx, const float* W, int N, int K, float* y,
