@@ -24,6 +24,12 @@ benchmark is bench.py and the parity tests are under tests/.
     python profile_workloads.py select [--batch 65536] [--k 8]
         range "select": one unmask (top-k) and one verify/accept launch over
         65536 sequences of 32 slots, after a warm-up pair.
+
+    python profile_workloads.py attn [--workload single|batched|long] [--reps 2]
+        range "attn": block attention (CAUSAL, 32/8 heads x 128, 32-token
+        block) on the seeded inputs of a configuration (single: batch 1 x 4096
+        keys; batched: 64 sequences, prefixes in [512, 8192]; long: batch 4 x
+        32768), --reps launches after three warm-up launches.
 """
 from __future__ import annotations
 
@@ -106,6 +112,23 @@ def select(args):
     nd.ndiff_check()
 
 
+def attn(args):
+    c = {"single": synth.ATTN_SINGLE, "batched": synth.ATTN_BATCHED, "long": synth.ATTN_LONG}[args.workload]
+    lengths = synth.attn_lengths(c["B"], c["seed"], c["P_lo"], c["P_hi"])
+    Lmax = int(c["P_hi"]) + c["T"]
+    inp = synth.attn_inputs(c["B"], c["T"], c["Hq"], c["Hkv"], c["D"], lengths, Lmax, c["seed"])
+    q, k, v, kv = inp.q.cuda(), inp.k_cache.cuda(), inp.v_cache.cuda(), inp.kv_len.cuda()
+    for _ in range(3):
+        nd.block_attn(q, k, v, kv, nd.NDIFF_CAUSAL, inp.scale)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("attn")
+    for _ in range(args.reps):
+        nd.block_attn(q, k, v, kv, nd.NDIFF_CAUSAL, inp.scale)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    nd.ndiff_check()
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="what", required=True)
@@ -126,8 +149,11 @@ def main():
     s = sub.add_parser("select")
     s.add_argument("--batch", type=int, default=65536)
     s.add_argument("--k", type=int, default=8)
+    a = sub.add_parser("attn")
+    a.add_argument("--workload", default="single", choices=["single", "batched", "long"])
+    a.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
-    {"decode": decode, "gemm": gemm, "select": select}[args.what](args)
+    {"decode": decode, "gemm": gemm, "select": select, "attn": attn}[args.what](args)
     print("ok")
 
 
