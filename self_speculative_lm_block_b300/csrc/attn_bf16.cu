@@ -84,6 +84,10 @@ struct Params {
   const int4* remap;     // per sequence {x, S, cache index, 0}: virtual keys >= x sit at
                          // cache rows S + (key - x) of that cache; nullptr: none
   int ncache;            // caches behind k/v when remap is set
+  int early_kv;          // 1: kv_len is final when the kernel starts (the previous kernel
+                         // triggers its dependents only after its own wait), so the prefix
+                         // K/V tiles stream before griddepcontrol.wait; q and the block's own
+                         // K/V rows are read after it
   unsigned int* status;
 };
 
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  griddep_wait();
+  if (!p.early_kv) griddep_wait();
   int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   if (p.order != nullptr) {  // 1-D grid: item rank * Hkv + kv head
     const int item = p.order[blockIdx.x / p.Hkv];
@@ -187,7 +191,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   const int nkeys = P + p.T;
   const int k_begin = s_idx * p.split;
-  if (k_begin >= nkeys) return;  // this split is past the sequence (uniform per CTA)
+  if (k_begin >= nkeys) {  // this split is past the sequence (uniform per CTA)
+    if (p.early_kv) griddep_wait();
+    return;
+  }
   const int k_end = min(k_begin + p.split, nkeys);
   const int ntiles = (k_end - k_begin + BN - 1) / BN;
   const int nsplit_b = (nkeys + p.split - 1) / p.split;
@@ -264,7 +271,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (lane == 0) {
       int issued = 0;
+      // early_kv: the tiles of prefix keys (written by earlier steps) that fit
+      // the ring go out before the wait for the previous kernel
+      const int npre = !p.early_kv ? 0 : min(min(ntiles, NST), max(0, (P - k_begin) / BN));
       for (int j = 0; j < ntiles; ++j) {
+        if (j == npre && p.early_kv) griddep_wait();
         const int st = j % NST, use = j / NST;
         if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, p.status, abort_flag)) break;
         const int vkey = k_begin + j * BN;
@@ -332,6 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool issuer = tid128 == 0;
     if (grp == 0) {
       // Q row r (slot t, head g*G + r % G) into TMEM columns [TQ, TQ + 64).
+      if (p.early_kv) griddep_wait();
       uint32_t w[64];
       if (valid) {
         const uint4* src = reinterpret_cast<const uint4*>(
@@ -546,9 +558,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Merges the KV splits of each (b, g) row: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // One warp per row. The splits' (m, l) are read one split per lane (32 at a
 // time) and M is a warp maximum; the partial O rows (512 B, 16 B a lane) are
-// loaded eight splits at a time and added in split order, the weight and l of
-// split s coming from lane s % 32 by shuffle. The additions are those of a
-// plain loop over s = 0, 1, ...; the batching only keeps many loads in flight.
+// added in split order, the weight and l of split s coming from lane s % 32 by
+// shuffle. With at most 32 splits, every (m, l) and the first 16 partial rows
+// are loaded in one round before M is known (the merge follows a kernel
+// boundary, where each dependent round of loads costs about a microsecond),
+// later rows eight at a time. The additions are those of a plain loop over
+// s = 0, 1, ...; the batching only keeps many loads in flight.
 __global__ void __launch_bounds__(128)
     attn_combine_kernel(const Params p) {
   const int g = blockIdx.y, b = blockIdx.z;
@@ -562,14 +577,61 @@ __global__ void __launch_bounds__(128)
   const int ns = (nkeys + p.split - 1) / p.split;
   if (ns <= 1) return;  // written directly by the main kernel
   const size_t base = (size_t)(b * p.Hkv + g) * p.nsplit_max;
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < ns; s0 += 32)
-    if (s0 + lane < ns) M = fmaxf(M, p.ws_ml[(base + s0 + lane) * ROWS + r].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += 32) {
+  if (ns <= 32) {
+    // one round of loads: every (m, l) and the first 16 splits' partial rows
+    // go out together; the max and the weights follow from registers
+    const float2 ml = lane < ns ? p.ws_ml[(base + lane) * ROWS + r] : make_float2(-INFINITY, 0.f);
+    float4 o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      o[j] = j < ns ? *reinterpret_cast<const float4*>(p.ws_o + ((base + j) * ROWS + r) * DH + lane * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = ml.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wl, j);
+      const float l = __shfl_sync(0xffffffffu, ml.y, j);
+      if (j < ns) {
+        L += w * l;
+        acc.x += w * o[j].x;
+        acc.y += w * o[j].y;
+        acc.z += w * o[j].z;
+        acc.w += w * o[j].w;
+      }
+    }
+    for (int j0 = 16; j0 < ns; j0 += 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        o[j] = (j0 + j < ns) ? *reinterpret_cast<const float4*>(
+                                   p.ws_o + ((base + j0 + j) * ROWS + r) * DH + lane * 4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+        const float l = __shfl_sync(0xffffffffu, ml.y, (j0 + j) & 31);
+        if (j0 + j < ns) {
+          L += w * l;
+          acc.x += w * o[j].x;
+          acc.y += w * o[j].y;
+          acc.z += w * o[j].z;
+          acc.w += w * o[j].w;
+        }
+      }
+    }
+  }
+  float M = -INFINITY;
+  if (ns > 32) {
+    for (int s0 = 0; s0 < ns; s0 += 32)
+      if (s0 + lane < ns) M = fmaxf(M, p.ws_ml[(base + s0 + lane) * ROWS + r].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  }
+  for (int s0 = 0; ns > 32 && s0 < ns; s0 += 32) {
     const int cnt = min(32, ns - s0);
     const float2 ml = lane < cnt ? p.ws_ml[(base + s0 + lane) * ROWS + r] : make_float2(-INFINITY, 0.f);
     const float wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);
@@ -736,7 +798,7 @@ size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
 ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
-                              cudaStream_t stream, const int4* remap, int ncache) {
+                              cudaStream_t stream, const int4* remap, int ncache, int early_kv) {
   const int G = Hq / Hkv;
   const int nsplit = (Lmax + split - 1) / split;
   const size_t need = attn_bf16_workspace(B, T, Hq, Hkv, Lmax, split);
@@ -773,6 +835,9 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   prm.vc = static_cast<const __nv_bfloat16*>(v);
   prm.remap = remap;
   prm.ncache = remap != nullptr ? ncache : B;
+  // early K/V needs a final kv_len and no table written by the launch before
+  // (no remap, no launch order: one sequence)
+  prm.early_kv = (early_kv && remap == nullptr && B == 1) ? 1 : 0;
   prm.ws_o = static_cast<float*>(ws);
   const size_t partials = attn_partials_bytes(B, Hkv, nsplit);
   prm.ws_ml = partials ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +

@@ -236,12 +236,16 @@ __global__ void __launch_bounds__(1024)
   const int ntile = d >> 7;
   float* xr = x + (size_t)m * d;
   float ss = 0.f;
-  for (int t = warp; t < ntile; t += nw) {  // uniform over the warp
+  float4 keep0 = make_float4(0.f, 0.f, 0.f, 0.f), keep1 = keep0;  // a warp's first two tiles
+  int it = 0;
+  for (int t = warp; t < ntile; t += nw, ++it) {  // uniform over the warp
     float4* xp = reinterpret_cast<float4*>(xr + t * 128 + lane * 4);
     const float4 xo = *xp;
     const float4 acc = tile_sum4<MT>(pp, t, m, lane * 4);
     const float4 v = make_float4(xo.x + acc.x, xo.y + acc.y, xo.z + acc.z, xo.w + acc.w);
     *xp = v;
+    if (it == 0) keep0 = v;
+    if (it == 1) keep1 = v;
     ss = fmaf(v.x, v.x, ss);
     ss = fmaf(v.y, v.y, ss);
     ss = fmaf(v.z, v.z, ss);
@@ -260,8 +264,9 @@ __global__ void __launch_bounds__(1024)
   }
   __syncthreads();
   const float inv = inv_s;
-  for (int t = warp; t < ntile; t += nw) {
-    const float4 v = *reinterpret_cast<const float4*>(xr + t * 128 + lane * 4);
+  it = 0;
+  for (int t = warp; t < ntile; t += nw, ++it) {
+    const float4 v = it == 0 ? keep0 : (it == 1 ? keep1 : *reinterpret_cast<const float4*>(xr + t * 128 + lane * 4));
     uint2 o;
     o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x * inv)) |
           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y * inv)) << 16);
@@ -303,13 +308,18 @@ __global__ void __launch_bounds__(32)
                      const int32_t* blk_pos, const float2* __restrict__ rope,
                      __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ kc,
                      __nv_bfloat16* __restrict__ vc, unsigned int* status) {
-  griddep_launch();
+  // Dependents launch only once the QKV projection (and so, through the
+  // chain of waits, every kernel before it) has completed: the attention
+  // after this kernel then reads kv_len and streams the prefix K/V before
+  // its own wait.
   griddep_wait();
+  griddep_launch();
   const int h = blockIdx.x, m = blockIdx.y, lane = threadIdx.x;
+  // the partials' loads go out first: they do not wait for the position
+  const float4 y = tile_sum4<MT>(pp, h, m, lane * 4);
   const int P = checked_prefix(kv_len[0], Lmax - T, status);
   const int pos = blk_pos != nullptr ? blk_pos[2 * (m >> 5)] + (m & 31) : P + m;
   const int slot = blk_pos != nullptr ? blk_pos[2 * (m >> 5) + 1] + (m & 31) : P + m;
-  const float4 y = tile_sum4<MT>(pp, h, m, lane * 4);
   if (h < Hq + Hkv) {
     // rows 4l, 4l+1: dims 2l, 2l+64; rows 4l+2, 4l+3: dims 2l+1, 2l+65
     const float4 cs = __ldg(reinterpret_cast<const float4*>(rope + (size_t)pos * 64 + 2 * lane));
