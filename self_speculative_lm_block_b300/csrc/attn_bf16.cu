@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // early_kv: the tiles of prefix keys (written by earlier steps) that fit
       // the ring go out before the wait for the previous kernel
       const int npre = !p.early_kv ? 0 : min(min(ntiles, NST), max(0, (P - k_begin) / BN));
+      const uint64_t kvpol = l2_evict_first_policy();  // K/V: read once per step
       for (int j = 0; j < ntiles; ++j) {
         if (j == npre && p.early_kv) griddep_wait();
         const int st = j % NST, use = j / NST;
@@ -283,11 +284,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* dk = sK + st * KT_BYTES;
         uint8_t* dv = sV + st * KT_BYTES;
         mbar_arrive_expect_tx(&k_full[st], KT_BYTES);
-        tma_load_2d(dk, &tmK, &k_full[st], 0, key);
-        tma_load_2d(dk + 8192, &tmK, &k_full[st], 64, key);
+        tma_load_2d_hint(dk, &tmK, &k_full[st], 0, key, kvpol);
+        tma_load_2d_hint(dk + 8192, &tmK, &k_full[st], 64, key, kvpol);
         mbar_arrive_expect_tx(&v_full[st], KT_BYTES);
-        tma_load_2d(dv, &tmV, &v_full[st], 0, key);
-        tma_load_2d(dv + 8192, &tmV, &v_full[st], 64, key);
+        tma_load_2d_hint(dv, &tmV, &v_full[st], 0, key, kvpol);
+        tma_load_2d_hint(dv + 8192, &tmV, &v_full[st], 64, key, kvpol);
         issued = j + 1;
       }
       if (*abort_flag) {

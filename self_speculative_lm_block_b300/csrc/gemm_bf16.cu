@@ -385,14 +385,15 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
       // tiles after it.
       const int nk = kb1 - kb0;
       const int npre = nk < NST ? nk : NST;
+      const uint64_t wpol = l2_evict_first_policy();  // weights: read once per forward
       {
         int tile = kb0 / p.nks, ks = kb0 % p.nks;
         for (int j = 0; j < npre; ++j) {
           mbar_arrive_expect_tx(&full[j], A_BYTES + B_BYTES);
           if (p.w_tiled)
-            tma_load_2d(sA + j * A_BYTES, &tmW, &full[j], 0, (kb0 + j) * BM);
+            tma_load_2d_hint(sA + j * A_BYTES, &tmW, &full[j], 0, (kb0 + j) * BM, wpol);
           else
-            tma_load_2d(sA + j * A_BYTES, &tmW, &full[j], ks * BK, tile * BM);
+            tma_load_2d_hint(sA + j * A_BYTES, &tmW, &full[j], ks * BK, tile * BM, wpol);
           if (++ks == p.nks) {
             ks = 0;
             ++tile;
@@ -408,9 +409,9 @@ __global__ void __launch_bounds__(THREADS, Geo<MT>::MIN_BLOCKS)
           if (kc >= NST && !mbar_wait(&empty[st], ((kc / NST) - 1) & 1, p.status, abort_flag)) break;
           mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
           if (p.w_tiled)
-            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], 0, (kb0 + kc) * BM);
+            tma_load_2d_hint(sA + st * A_BYTES, &tmW, &full[st], 0, (kb0 + kc) * BM, wpol);
           else
-            tma_load_2d(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM);
+            tma_load_2d_hint(sA + st * A_BYTES, &tmW, &full[st], ks * BK, tile * BM, wpol);
         }
         tma_load_2d(sB + st * B_BYTES, &tmX, &full[st], ks * BK, 0);
         if (++ks == p.nks) {
