@@ -276,6 +276,62 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// residual_rmsnorm_kernel for a few token rows (an AR step) with the row
+// spread over a cluster of C CTAs (blockIdx.x = rank), one warp a tile, so
+// that the row's ~100 KB of loads (x and the partials at d = 4096) are taken
+// by C SMs instead of one. For d / 128 <= 32 tiles, where the one-CTA kernel
+// gives each warp one tile, the arithmetic is that kernel's: the tiles' sums
+// of squares are added in tile order (warp 0 of every CTA reads all of them
+// from the cluster's shared memory after a cluster barrier), so a row's
+// result does not depend on which kernel ran it.
+template <int MT>
+__global__ void __launch_bounds__(256)
+    residual_rmsnorm_cluster_kernel(float* __restrict__ x, int d, float eps, __nv_bfloat16* __restrict__ h,
+                                    const PartialPlan pp) {
+  griddep_launch();
+  griddep_wait();
+  const int m = blockIdx.y, rank = blockIdx.x;  // the cluster spans the grid's x
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int ntile = d >> 7;
+  const int t = rank * nw + warp;
+  float4* xp = reinterpret_cast<float4*>(x + (size_t)m * d + t * 128 + lane * 4);
+  const float4 xo = *xp;
+  const float4 acc = tile_sum4<MT>(pp, t, m, lane * 4);
+  const float4 v = make_float4(xo.x + acc.x, xo.y + acc.y, xo.z + acc.z, xo.w + acc.w);
+  *xp = v;
+  float ss = 0.f;
+  ss = fmaf(v.x, v.x, ss);
+  ss = fmaf(v.y, v.y, ss);
+  ss = fmaf(v.z, v.z, ss);
+  ss = fmaf(v.w, v.w, ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float wsum[8];
+  __shared__ float inv_s;
+  if (lane == 0) wsum[warp] = ss;
+  cluster_sync_all();  // every tile's sum is in its CTA's shared memory
+  if (warp == 0) {
+    const float tv = lane < ntile ? ld_cluster_f32(smem_u32(&wsum[lane % nw]), lane / nw) : 0.f;
+    float tv_all[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) tv_all[j] = __shfl_sync(0xffffffffu, tv, j);
+    float tot = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ntile) tot += tv_all[j];
+    if (lane == 0) inv_s = 1.f / sqrtf(tot / (float)d + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  uint2 o;
+  o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x * inv)) |
+        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y * inv)) << 16);
+  o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z * inv)) |
+        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w * inv)) << 16);
+  *reinterpret_cast<uint2*>(h + (size_t)m * d + t * 128 + lane * 4) = o;
+  cluster_sync_all();  // no CTA leaves while another still reads its sums
+}
+
 // SwiGLU of the gate/up projection: tile rows 2i and 2i+1 hold gate j and up j
 // (j = tile * 64 + i); act[m][j] = bf16(silu(g) * u), the expression of the
 // projection kernel's SwiGLU epilogue. Grid (tiles / 8, token rows), one warp
@@ -595,7 +651,14 @@ ndiff_status launch_residual_rmsnorm(float* x, int T, int d, float eps, __nv_bfl
   if (T <= 0) return NDIFF_OK;
   if (d % 128 != 0)
     return set_error(NDIFF_ERR_UNSUPPORTED, "residual_rmsnorm: d_model %d is not a multiple of 128", d);
-  const int threads = (d / 128) * 32 < 1024 ? (d / 128) * 32 : 1024;
+  const int ntile = d / 128;
+  if (mt == 32 && T <= 4 && ntile <= 32 && ntile % 8 == 0) {
+    // an AR step: the row over a cluster of 8 CTAs, ntile / 8 warps each
+    NDIFF_CUDA_TRY(launch_k_cluster(mk::residual_rmsnorm_cluster_kernel<32>, dim3(8, T), dim3(32 * (ntile / 8)),
+                                    0, s, 8, x, d, eps, h, pp));
+    return NDIFF_OK;
+  }
+  const int threads = ntile * 32 < 1024 ? ntile * 32 : 1024;
   NDIFF_MT_DISPATCH(mk::residual_rmsnorm_kernel, mt, dim3(T), dim3(threads), x, d, eps, h, pp);
   return NDIFF_OK;
 }

@@ -495,6 +495,28 @@ def test_bf16_block_rows_equal_single_token_forwards(nd):
     m.close()
 
 
+def test_bf16_full_width_block_rows_equal_single_token_forwards(nd):
+    """The same at the 8B width (d_model 4096, 32/8 heads x 128, SwiGLU 12288),
+    one layer and a 4096-id vocabulary: the token steps run the projections'
+    merges and the RMSNorm in their few-row forms (the norm over a cluster of
+    CTAs), the 32-row block in the one-CTA forms, and every row must agree bit
+    for bit."""
+    c = dict(synth.MODEL_8B)
+    c.update(layers=1, vocab=4096)
+    pr = synth.prompt(40, c["vocab"], 23)
+    m = _gpu_model(nd, c, "bf16", max_seq=128)
+    m.prefill(pr)
+    ar = m.generate(0, 32)
+    m.prefill(pr)
+    blk = m.forward([int(pr[-1])] + ar[:31], OA.CAUSAL)
+    m.prefill(pr)
+    for i in range(32):
+        one = m.forward([int(pr[-1]) if i == 0 else ar[i - 1]], OA.CAUSAL)
+        assert np.array_equal(one[0], blk[i]), i
+        m.step(0)
+    m.close()
+
+
 def test_bf16_selfspec_equals_ar_and_tracks_oracle(nd):
     c = MID_BF16
     cfg = _ocfg(c, "bf16")
