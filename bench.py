@@ -50,11 +50,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward at 8B"
-# DRAM bytes (read + write) of one attention launch, from ncu captures of the
-# current attention kernel on these workloads (summaries under profiles/);
-# None where no capture exists.
-ATTN_TRAFFIC = {"attn-batched": 1016157440 + 9754880, "attn-long": 539051520 + 3462400,
-                "attn-single": None}
+# DRAM bytes (read + write) of one attention launch and its split merge, from
+# ncu captures of the current kernels on these workloads (summary under
+# profiles/); None where no capture exists.
+ATTN_TRAFFIC = {"attn-batched": 1016170496 + 1828608,
+                "attn-long": 539061504 + 369152 + 8535552,
+                "attn-single": 17218816 + 512 + 9067776}
 SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126e6
 
