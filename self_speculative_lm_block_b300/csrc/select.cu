@@ -21,9 +21,11 @@
 // are 16-byte aligned:
 // unmask_quad_kernel: four lanes per sequence, for B >= 256. Each lane loads
 //   8 of the row's confidences with two coalesced 16-byte loads, turns them
-//   into order-preserving integer keys (0 marks an unmasked slot), and counts
-//   for each of its slots the slots that beat it: 28 comparisons among its
-//   own and 3 x 64 against the keys its three partners pass by shuffle.
+//   into order-preserving integer keys (0 marks an unmasked slot). For k <= 8
+//   it sorts its eight slots and the k winners are taken one per round, the
+//   largest of the four lanes' heads; for larger k it counts for each of its
+//   slots the slots that beat it: 28 comparisons among its own and 3 x 64
+//   against the keys its three partners pass by shuffle.
 //   The lane merges the chosen tokens into its 16-byte chunks of the draft and
 //   next-input rows (one shuffle brings the lower lane's last slot for the
 //   shift by one) and writes back whole chunks, so no store is a partial
@@ -168,7 +170,22 @@ __device__ __forceinline__ constexpr int quad_slot(int q, int e) {
   return e < 4 ? 4 * q + e : 16 + 4 * q + (e - 4);
 }
 
-__global__ void __launch_bounds__(128)
+// 64-bit xor shuffle.
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// EXTRACT (k <= 8): the k winners are taken one at a time instead of ranking
+// every slot. Each lane sorts its eight slots by the composite key
+// (key << 5) | (31 - slot), unique per slot and ordered as the selection
+// orders slots (larger key first, the lower slot on equal keys), with a
+// 19-comparator sorting network; round r then takes the largest head of the
+// four lanes' sorted lists (two shuffle-max steps), which is the slot of rank
+// r. About half the instructions of the pairwise ranking at k = 8.
+template <bool EXTRACT>
+__global__ void __launch_bounds__(128, 10)
     unmask_quad_kernel(const float* __restrict__ conf, const int32_t* __restrict__ pred, int B,
                        int k, uint32_t* mask_bits, int32_t* block_in, int32_t* draft,
                        int32_t* chosen) {
@@ -184,9 +201,6 @@ __global__ void __launch_bounds__(128)
   const int4* gp = reinterpret_cast<const int4*>(pred) + (size_t)row * 8;
   const int4 c0 = __ldg(gc + q), c1 = __ldg(gc + 4 + q);
   const int4 p0 = __ldg(gp + q), p1 = __ldg(gp + 4 + q);
-  int4* gd = reinterpret_cast<int4*>(draft) + (size_t)row * 8;
-  int4* gb = reinterpret_cast<int4*>(block_in) + (size_t)row * 8;
-  const int4 d0 = gd[q], d1 = gd[4 + q], i0 = gb[q], i1 = gb[4 + q];
   const uint32_t mask = mask_bits[row];
   uint32_t key[8] = {order_key(__int_as_float(c0.x)), order_key(__int_as_float(c0.y)),
                      order_key(__int_as_float(c0.z)), order_key(__int_as_float(c0.w)),
@@ -195,54 +209,91 @@ __global__ void __launch_bounds__(128)
   const int32_t pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
   for (int e = 0; e < 8; ++e) key[e] = ((mask >> quad_slot(q, e)) & 1u) ? key[e] : 0u;
-  // rank[e] = number of slots that beat own slot e: o beats m when
-  // key_o + [slot_o < slot_m] > key_m (ties go to the lower slot; the +1 never
-  // overflows since every key is <= key(+inf) = 0xff800000).
-  int rank[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) rank[e] = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-#pragma unroll
-    for (int f = e + 1; f < 8; ++f) {  // own slots rise with e
-      const int p = key[f] > key[e] ? 1 : 0;
-      rank[e] += p;
-      rank[f] += 1 - p;
-    }
-  }
-#pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    uint32_t o[8];
-#pragma unroll
-    for (int f = 0; f < 8; ++f) o[f] = __shfl_xor_sync(0xffffffffu, key[f], d);
-    // the partner's first-half slots lie below every own second-half slot and
-    // its second-half slots above every own first-half slot; within a half
-    // the lower lane has the lower slots
-    const uint32_t lower = ((q ^ d) < q) ? 1u : 0u;
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-      const uint32_t same = o[f] + lower, below = o[f] + 1u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rank[e] += same > key[e] ? 1 : 0;
-#pragma unroll
-      for (int e = 4; e < 8; ++e) rank[e] += below > key[e] ? 1 : 0;
-    }
-#pragma unroll
-    for (int f = 4; f < 8; ++f) {
-      const uint32_t same = o[f] + lower;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rank[e] += o[f] > key[e] ? 1 : 0;
-#pragma unroll
-      for (int e = 4; e < 8; ++e) rank[e] += same > key[e] ? 1 : 0;
-    }
-  }
   const int kk = min(k, __popc(mask));
   bool sel[8];
   uint32_t taken = 0u;
+  if constexpr (EXTRACT) {
+    unsigned long long sk[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    sel[e] = key[e] != 0u && rank[e] < kk;
-    if (sel[e]) taken |= 1u << quad_slot(q, e);
+    for (int e = 0; e < 8; ++e) sk[e] = ((unsigned long long)key[e] << 5) | (uint32_t)(31 - quad_slot(q, e));
+    constexpr int NET[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2}, {5, 6},
+                                {0, 4}, {1, 5}, {2, 6}, {3, 7}, {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+    for (int c = 0; c < 19; ++c) {  // descending
+      const unsigned long long a = sk[NET[c][0]], z = sk[NET[c][1]];
+      const bool sw = z > a;
+      sk[NET[c][0]] = sw ? z : a;
+      sk[NET[c][1]] = sw ? a : z;
+    }
+    for (int r = 0; r < k; ++r) {  // k <= 8, the same for every lane
+      const unsigned long long head = sk[0];
+      unsigned long long m = head, o = shfl_xor_u64(m, 1);
+      m = o > m ? o : m;
+      o = shfl_xor_u64(m, 2);
+      m = o > m ? o : m;
+      if (r < kk && head == m) {  // this lane holds the slot of rank r
+        const int slot = 31 - (int)(m & 31u);
+        taken |= 1u << slot;
+        if (live) chosen[(size_t)b * k + r] = slot;
+#pragma unroll
+        for (int e = 0; e < 7; ++e) sk[e] = sk[e + 1];
+        sk[7] = 0ull;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sel[e] = (taken >> quad_slot(q, e)) & 1u;
+  } else {
+    // rank[e] = number of slots that beat own slot e: o beats m when
+    // key_o + [slot_o < slot_m] > key_m (ties go to the lower slot; the +1 never
+    // overflows since every key is <= key(+inf) = 0xff800000).
+    int rank[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rank[e] = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+#pragma unroll
+      for (int f = e + 1; f < 8; ++f) {  // own slots rise with e
+        const int p = key[f] > key[e] ? 1 : 0;
+        rank[e] += p;
+        rank[f] += 1 - p;
+      }
+    }
+#pragma unroll
+    for (int d = 1; d < 4; ++d) {
+      uint32_t o[8];
+#pragma unroll
+      for (int f = 0; f < 8; ++f) o[f] = __shfl_xor_sync(0xffffffffu, key[f], d);
+      // the partner's first-half slots lie below every own second-half slot and
+      // its second-half slots above every own first-half slot; within a half
+      // the lower lane has the lower slots
+      const uint32_t lower = ((q ^ d) < q) ? 1u : 0u;
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const uint32_t same = o[f] + lower, below = o[f] + 1u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rank[e] += same > key[e] ? 1 : 0;
+#pragma unroll
+        for (int e = 4; e < 8; ++e) rank[e] += below > key[e] ? 1 : 0;
+      }
+#pragma unroll
+      for (int f = 4; f < 8; ++f) {
+        const uint32_t same = o[f] + lower;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rank[e] += o[f] > key[e] ? 1 : 0;
+#pragma unroll
+        for (int e = 4; e < 8; ++e) rank[e] += same > key[e] ? 1 : 0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sel[e] = key[e] != 0u && rank[e] < kk;
+      if (sel[e]) taken |= 1u << quad_slot(q, e);
+    }
+    if (live) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (sel[e]) chosen[(size_t)b * k + rank[e]] = quad_slot(q, e);
+    }
   }
   // block_in[i + 1] takes pred[i]: the first slot of each of the lane's two
   // chunks follows the last slot of the lower lane's chunk (lane 3's first
@@ -255,6 +306,11 @@ __global__ void __launch_bounds__(128)
   taken |= __shfl_xor_sync(0xffffffffu, taken, 1);
   taken |= __shfl_xor_sync(0xffffffffu, taken, 2);
   if (!live) return;
+  // the draft and next-input chunks are read only now, to keep the selection's
+  // registers free (more resident warps hide the extra round of loads)
+  int4* gd = reinterpret_cast<int4*>(draft) + (size_t)row * 8;
+  int4* gb = reinterpret_cast<int4*>(block_in) + (size_t)row * 8;
+  const int4 d0 = gd[q], d1 = gd[4 + q], i0 = gb[q], i1 = gb[4 + q];
   const bool in0 = q > 0 && nb_sel3;
   const bool in4 = q > 0 ? (nb_sel7 != 0) : (nb_sel3 != 0);
   const int32_t v4 = q > 0 ? nb_pv7 : nb_pv3;
@@ -271,9 +327,6 @@ __global__ void __launch_bounds__(128)
   if (sel[4] || sel[5] || sel[6] || sel[7]) gd[4 + q] = nd1;
   if (in0 || sel[0] || sel[1] || sel[2]) gb[q] = ni0;
   if (in4 || sel[4] || sel[5] || sel[6]) gb[4 + q] = ni1;
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-    if (sel[e]) chosen[(size_t)b * k + rank[e]] = quad_slot(q, e);
   for (int r = kk + q; r < k; r += 4) chosen[(size_t)b * k + r] = -1;
   if (q == 0) mask_bits[b] = mask & ~taken;
 }
@@ -348,7 +401,7 @@ ndiff_status launch_unmask(const float* conf, const int32_t* pred, int B, int T,
   if (B == 0) return NDIFF_OK;
   if (T == 32 && B >= UNMASK_QUAD_MIN_B && aligned16(conf) && aligned16(pred) &&
       aligned16(draft) && aligned16(block_in)) {
-    NDIFF_CUDA_TRY(launch_k(unmask_quad_kernel,
+    NDIFF_CUDA_TRY(launch_k(k <= 8 ? unmask_quad_kernel<true> : unmask_quad_kernel<false>,
                             dim3((B + QUAD_ROWS_PER_CTA - 1) / QUAD_ROWS_PER_CTA), dim3(128), 0,
                             stream, conf, pred, B, k, mask_bits, block_in, draft, chosen));
     return NDIFF_OK;

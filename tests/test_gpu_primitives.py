@@ -210,8 +210,9 @@ def test_unmask(nd, T, ties, allm):
 @pytest.mark.parametrize("ties,allm", [(False, False), (True, False), (True, True)])
 def test_unmask_row_parallel_batches(nd, B, ties, allm):
     """Batches of 32-slot blocks from 256 sequences up take the four-lanes-a-
-    sequence layout (ranks from pairwise key comparisons, keys passed by
-    shuffle); a ragged last CTA and every k in {1, 4, 8, 32}, bit for bit."""
+    sequence layout (k <= 8: winners extracted from per-lane sorted lists; k >
+    8: ranks from pairwise key comparisons, keys passed by shuffle); a ragged
+    last CTA and every k in {1, 4, 8, 32}, bit for bit."""
     T = 32
     conf, pred, mask = synth.unmask_inputs(B, T, 151936, 301 + B, ties=ties, all_masked=allm)
     for k in (1, 4, 8, 32):

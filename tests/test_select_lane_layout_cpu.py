@@ -5,7 +5,10 @@ partner's key, the shuffles between the four lanes, and the merge of chosen
 tokens into each lane's 16-byte chunks of the draft and next-input rows with
 the shift by one crossing lanes — agrees with the oracle's unmask round on
 random rows, tie-heavy rows, signed zeros, infinities and full masks. The GPU
-kernel itself is checked against the oracle by the GPU parity tests."""
+kernel itself is checked against the oracle by the GPU parity tests. For
+k <= 8 the kernel takes the winners by extraction instead of ranking every
+slot (a sorting network per lane, then the largest of the four lanes' heads
+per round); the model of that path must give the same result."""
 import numpy as np
 
 from oracle import decode as OD
@@ -22,7 +25,36 @@ def _slot(q, e):
     return 4 * q + e if e < 4 else 16 + 4 * q + (e - 4)
 
 
-def _lane_model(conf, pred, mask, k, block_in, draft):
+# the 19-comparator sorting network of the extraction path (descending)
+_NET = [(0, 1), (2, 3), (4, 5), (6, 7), (0, 2), (1, 3), (4, 6), (5, 7), (1, 2), (5, 6),
+        (0, 4), (1, 5), (2, 6), (3, 7), (2, 4), (3, 5), (1, 2), (3, 4), (5, 6)]
+
+
+def _extract_ranks(key, mask, k):
+    """The k <= 8 path: each lane sorts its composite keys (key << 5 | 31 - slot)
+    with the network; round r takes the largest of the four lanes' heads."""
+    kk = min(k, bin(mask).count("1"))
+    lists = []
+    for q in range(4):
+        sk = [(key[q][e] << 5) | (31 - _slot(q, e)) for e in range(8)]
+        for a, b in _NET:
+            if sk[b] > sk[a]:
+                sk[a], sk[b] = sk[b], sk[a]
+        lists.append(sk)
+    rank = [[99] * 8 for _ in range(4)]
+    for r in range(k):
+        heads = [lst[0] for lst in lists]
+        m = max(max(heads[0], heads[1]), max(heads[2], heads[3]))
+        if r < kk:
+            q = heads.index(m)
+            slot = 31 - (m & 31)
+            e = next(e for e in range(8) if _slot(q, e) == slot)
+            rank[q][e] = r
+            lists[q] = lists[q][1:] + [0]
+    return rank
+
+
+def _lane_model(conf, pred, mask, k, block_in, draft, extract=False):
     key = [[_key(conf[_slot(q, e)]) if (mask >> _slot(q, e)) & 1 else 0 for e in range(8)]
            for q in range(4)]
     rank = [[0] * 8 for _ in range(4)]
@@ -45,6 +77,8 @@ def _lane_model(conf, pred, mask, k, block_in, draft):
                         adj = 0 if e < 4 else lower
                     rank[q][e] += int(o[f] + adj > key[q][e])
     kk = min(k, bin(mask).count("1"))
+    if extract:
+        rank = _extract_ranks(key, mask, k)
     sel = [[key[q][e] != 0 and rank[q][e] < kk for e in range(8)] for q in range(4)]
     chosen = [-1] * k
     taken = 0
@@ -86,8 +120,20 @@ def test_lane_model_matches_oracle_unmask():
         k = int(rng.integers(1, 33))
         block_in = rng.integers(-5, 0, 32).astype(np.int32)
         draft = rng.integers(-9, -5, 32).astype(np.int32)
-        m, ch, bi, dr = _lane_model(conf, pred, mask, k, block_in, draft)
         rm, rb, rd, rch = OD.unmask(conf[None], pred[None], np.array([mask], np.uint32),
                                     block_in[None], draft[None], k)
-        assert m == rm[0] and ch == list(rch[0]), trial
-        assert np.array_equal(bi, rb[0]) and np.array_equal(dr, rd[0]), trial
+        for extract in ((False, True) if k <= 8 else (False,)):
+            m, ch, bi, dr = _lane_model(conf, pred, mask, k, block_in, draft, extract)
+            assert m == rm[0] and ch == list(rch[0]), (trial, extract)
+            assert np.array_equal(bi, rb[0]) and np.array_equal(dr, rd[0]), (trial, extract)
+
+
+def test_extraction_network_sorts_every_zero_one_input():
+    """The network sorts (0-1 principle: every 0/1 input of length 8 suffices)."""
+    import itertools
+    for bits in itertools.product([0, 1], repeat=8):
+        s = list(bits)
+        for a, b in _NET:
+            if s[b] > s[a]:
+                s[a], s[b] = s[b], s[a]
+        assert s == sorted(bits, reverse=True), bits
