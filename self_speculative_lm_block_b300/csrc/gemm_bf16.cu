@@ -11,31 +11,37 @@
 // a weight stream with the tensor cores doing 32 columns of work per weight.
 //
 // Design (swap-AB: the weight tile is the MMA's 128-row A operand, the token
-// rows are its N = 32 columns, so the accumulator is 128 lanes x 32 fp32
-// columns of TMEM):
-//   * Work items are (128-row tile of W, K split). A persistent grid of at most
-//     one CTA per SM walks the items round-robin. Warp 0 streams 128x64 weight
-//     tiles and the matching 32x64 activation tile through a 5-stage TMA ring
-//     (128-byte swizzle); warp 1 issues tcgen05.mma (M128 N32 K16) into one of
-//     two TMEM accumulators; warps 2-5 drain the other accumulator, so the
-//     epilogue of one item overlaps the loads of the next.
-//   * About 100 KB of shared memory per CTA, so two CTAs fit on an SM: under
-//     programmatic dependent launch the next projection's CTAs start next to
-//     the running ones and stream their first weight tiles (which no earlier
-//     kernel writes) before griddepcontrol.wait; the activation tiles and every
-//     global write come after it.
-//   * K splits: every split writes its fp32 partial tile to the workspace and
-//     bumps a per-tile counter; the last split to arrive adds the partials in
-//     split order 0..S-1 and runs the fused epilogue, then resets the counter.
-//     The split boundaries depend only on (N, K, SM count), never on the number
-//     of token rows, and the MMA column count is always 32, so a token row's
-//     result is the same whether it is computed alone (AR) or inside a block.
+// rows are its N = MT columns (32, or 64 / 128 for the fused and quadratic
+// forwards), so the accumulator is 128 lanes x MT fp32 columns of TMEM):
+//   * Stream-K: one CTA per SM; CTA c owns the contiguous run
+//     [c U / G, (c + 1) U / G) of all tiles' k-steps (U = tiles x K / 64), in
+//     tiled weight storage a contiguous run of 16 KB boxes. Warp 0 streams the
+//     128x64 weight tiles and the matching MTx64 activation tiles through a TMA
+//     ring (128-byte swizzle; the weight loads carry an L2 evict-first hint);
+//     warp 1 issues tcgen05.mma (M128 N MT K16) into one of two TMEM
+//     accumulators, one per segment (the part of one tile a CTA owns); warps
+//     2-5 drain the other accumulator, so the epilogue of one segment overlaps
+//     the loads of the next.
+//   * About 100 KB of shared memory per CTA at MT = 32, so two CTAs fit on an
+//     SM: under programmatic dependent launch the next projection's CTAs start
+//     next to the running ones and stream their first weight tiles (which no
+//     earlier kernel writes) before griddepcontrol.wait; the activation tiles
+//     and every global write come after it.
+//   * Segments of a tile split over several CTAs: with GEMM_EPI_PARTIAL (the
+//     model's forward of one sequence) each segment stores its partial tile
+//     and the kernel after the projection sums them; with the other epilogues
+//     the last contributor to arrive at a per-tile counter adds the partials in
+//     k order and runs the epilogue, then resets the counter. The partition
+//     depends only on (N, K, grid), never on the number of token rows, so a
+//     token row's result is the same whether it is computed alone (AR) or
+//     inside a block.
 //   * Fused epilogues: fp32 store (logits), residual add (x += y), SwiGLU and
 //     QKV with rotate-half RoPE from a precomputed table plus the K/V-cache
-//     write at the block's positions. The weights are stored so that the two
-//     rows an epilogue combines are adjacent (gate j / up j; RoPE dims i / i+64
-//     of a q or k head), i.e. held by neighbouring lanes, and one warp shuffle
-//     brings them together.
+//     write at the block's positions, the LM head's argmax (its own
+//     instantiation). The weights are stored so that the two rows an epilogue
+//     combines are adjacent (gate j / up j; RoPE dims i / i+64 of a q or k
+//     head), i.e. held by neighbouring lanes, and one warp shuffle brings them
+//     together.
 //   * Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 //     the device status word, lets issued TMA copies land, frees TMEM and exits.
 #include <cuda_bf16.h>

@@ -109,8 +109,9 @@ struct GemmPlan {
 
 // The weight-streaming projection for mt = 32 token rows (a block, or one
 // token), mt = 64 (two blocks: the fused verify + draft forward) or mt = 128
-// (four blocks: the quadratic forward). The K split depends on (N, K) only,
-// so a row's arithmetic is the same for every row count and every mt.
+// (four blocks: the quadratic forward). The stream-K partition depends on
+// (N, K, grid) only, so a row's arithmetic is the same for every row count
+// and every mt.
 GemmPlan gemm_plan(int N, int K);
 // Most segments (tiles touched) of one CTA's run of k-steps under the plan.
 int gemm_plan_maxseg(const GemmPlan& pl);
