@@ -22,11 +22,15 @@
 //     accumulators, one per segment (the part of one tile a CTA owns); warps
 //     2-5 drain the other accumulator, so the epilogue of one segment overlaps
 //     the loads of the next.
-//   * About 100 KB of shared memory per CTA at MT = 32, so two CTAs fit on an
-//     SM: under programmatic dependent launch the next projection's CTAs start
-//     next to the running ones and stream their first weight tiles (which no
-//     earlier kernel writes) before griddepcontrol.wait; the activation tiles
-//     and every global write come after it.
+//   * One CTA per SM (~124 KB of shared memory at MT = 32: a six-stage ring).
+//     Under programmatic dependent launch the next projection's CTAs start as
+//     the running ones leave their SMs and stream their first six weight tiles
+//     (which no earlier kernel writes, ~14 MB over the GPU) before
+//     griddepcontrol.wait, i.e. while the small merge kernel between the two
+//     projections runs; the activation tiles and every global write come after
+//     it. With two CTAs per SM the next projection started next to the running
+//     one, its prefetch competed with that projection's own stream, and HBM
+//     sat idle during the merge kernel (8B: 3.38 vs 3.27 ms per AR forward).
 //   * Segments of a tile split over several CTAs: with GEMM_EPI_PARTIAL (the
 //     model's forward of one sequence) each segment stores its partial tile
 //     and the kernel after the projection sums them; with the other epilogues
@@ -63,7 +67,7 @@ constexpr int THREADS = 192;
 template <int MT_>
 struct Geo {
   static constexpr int MT = MT_;
-  static constexpr int NST = MT_ == 32 ? 5 : (MT_ == 64 ? 7 : 6);  // pipeline stages
+  static constexpr int NST = MT_ == 32 ? 6 : (MT_ == 64 ? 7 : 6);  // pipeline stages
   static constexpr int B_BYTES = MT_ * BK * 2;           // 4 KB / 8 KB
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NST * A_BYTES;
@@ -73,12 +77,15 @@ struct Geo {
   static constexpr int N_BARS = 2 * NST + 4 + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 64 + 1024;
   static constexpr int TMEM_COLS = 2 * MT_;              // two accumulators
-  static constexpr int MIN_BLOCKS = MT_ == 32 ? 2 : 1;
+  static constexpr int MIN_BLOCKS = 1;
 };
 
 static_assert(Geo<32>::OFF_B % 1024 == 0 && Geo<64>::OFF_B % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
-static_assert(2 * Geo<32>::SMEM_BYTES <= 227 * 1024, "two CTAs per SM at 32 token rows");
+// At 32 token rows six stages take ~124 KB, so one CTA runs per SM (see the
+// file header for why that is faster than two).
+static_assert(Geo<32>::SMEM_BYTES <= 227 * 1024 && 2 * Geo<32>::SMEM_BYTES > 228 * 1024,
+              "one CTA per SM at 32 token rows");
 static_assert(Geo<64>::SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 static_assert(Geo<128>::OFF_B % 1024 == 0 && Geo<128>::SMEM_BYTES <= 227 * 1024,
               "shared memory per CTA at 128 token rows");
