@@ -84,6 +84,8 @@ struct Params {
   const int4* remap;     // per sequence {x, S, cache index, 0}: virtual keys >= x sit at
                          // cache rows S + (key - x) of that cache; nullptr: none
   int ncache;            // caches behind k/v when remap is set
+  const char* l2pf;      // nullptr, or bytes (the next projection's weights) that the CTAs prefetch
+  size_t l2pf_bytes;     // into L2 between them once their own K/V loads are out
   int early_kv;          // 1: kv_len is final when the kernel starts (the previous kernel
                          // triggers its dependents only after its own wait), so the prefix
                          // K/V tiles stream before griddepcontrol.wait; q and the block's own
@@ -290,6 +292,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d_hint(dv, &tmV, &v_full[st], 0, key, kvpol);
         tma_load_2d_hint(dv + 8192, &tmV, &v_full[st], 64, key, kvpol);
         issued = j + 1;
+      }
+      if (p.l2pf != nullptr) {
+        // A decode step's attention leaves HBM mostly idle (a few MB of K/V):
+        // the CTAs pull the output projection's weights into L2 meanwhile, in
+        // 64 KB bulk prefetches, an equal slice each.
+        const int nct = gridDim.x * gridDim.y * gridDim.z;
+        const int cid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        const size_t per = ((p.l2pf_bytes / nct) + 65535) & ~(size_t)65535;
+        const size_t b0 = per * cid, b1 = b0 + per < p.l2pf_bytes ? b0 + per : p.l2pf_bytes;
+        for (size_t o = b0; o < b1; o += 65536) {
+          const uint32_t n = (uint32_t)(b1 - o < 65536 ? b1 - o : 65536);
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.l2pf + o), "r"(n) : "memory");
+        }
       }
       if (*abort_flag) {
         // Let every issued copy land before the CTA's shared memory goes away.
@@ -799,7 +814,8 @@ size_t attn_bf16_workspace(int B, int T, int Hq, int Hkv, int Lmax, int split) {
 ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const int32_t* kv_len,
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
-                              cudaStream_t stream, const int4* remap, int ncache, int early_kv) {
+                              cudaStream_t stream, const int4* remap, int ncache, int early_kv,
+                              const void* l2pf, size_t l2pf_bytes) {
   const int G = Hq / Hkv;
   const int nsplit = (Lmax + split - 1) / split;
   const size_t need = attn_bf16_workspace(B, T, Hq, Hkv, Lmax, split);
@@ -839,6 +855,10 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   // early K/V needs a final kv_len and no table written by the launch before
   // (no remap, no launch order: one sequence)
   prm.early_kv = (early_kv && remap == nullptr && B == 1) ? 1 : 0;
+  // the prefetch wants 16-byte aligned addresses and sizes
+  const bool pf_ok = l2pf != nullptr && (reinterpret_cast<uintptr_t>(l2pf) & 15) == 0;
+  prm.l2pf = pf_ok ? static_cast<const char*>(l2pf) : nullptr;
+  prm.l2pf_bytes = pf_ok ? (l2pf_bytes & ~(size_t)15) : 0;
   prm.ws_o = static_cast<float*>(ws);
   const size_t partials = attn_partials_bytes(B, Hkv, nsplit);
   prm.ws_ml = partials ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +

@@ -324,14 +324,18 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
         __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(m->qb);
         __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(m->ob);
         TRY(launch_attn_bf16(qb, ly.kc, ly.vc, m->kv_len, 1, kBlock, m->Hq, m->Hkv, m->Lmax, 1,
-                             scale, m->attn_split, ob, m->aws, m->aws_bytes, s, nullptr, 0, 1));
+                             scale, m->attn_split, ob, m->aws, m->aws_bytes, s, nullptr, 0, 1, ly.wo,
+                             (size_t)m->d * m->HD * 2));
         TRY(launch_attn_bf16(qb + half, ly.kc, ly.vc, m->kv_len2, 1, kBlock, m->Hq, m->Hkv,
                              m->Lmax, 0, scale, m->attn_split, ob + half, m->aws, m->aws_bytes, s));
       } else {
-        // one sequence: the QKV merge before it lets the prefix K/V stream early
+        // one sequence: the QKV merge before it lets the prefix K/V stream early,
+        // and the attention CTAs pull the output projection's weights into L2
+        // while HBM would otherwise idle
         TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, B, T, m->Hq, m->Hkv, m->Lmax, causal,
                              scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s, nullptr, 0,
-                             defer ? 1 : 0));
+                             defer ? 1 : 0, defer ? ly.wo : nullptr,
+                             defer ? (size_t)m->d * m->HD * 2 : 0));
       }
       p = gp;
       p.N = m->d;
