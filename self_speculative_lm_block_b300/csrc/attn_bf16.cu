@@ -86,6 +86,9 @@ struct Params {
   int ncache;            // caches behind k/v when remap is set
   const char* l2pf;      // nullptr, or bytes (the next projection's weights) that the CTAs prefetch
   size_t l2pf_bytes;     // into L2 between them once their own K/V loads are out
+  const char* rpf;       // nullptr, or a stream-K projection's weights (tiled, 16 KB a k-step):
+  int rpf_U, rpf_G;      // of each of its G runs of U / G k-steps, k-steps [6, 12) past the run's
+                         // start (the projection's CTAs load the first six themselves)
   int early_kv;          // 1: kv_len is final when the kernel starts (the previous kernel
                          // triggers its dependents only after its own wait), so the prefix
                          // K/V tiles stream before griddepcontrol.wait; q and the block's own
@@ -304,6 +307,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (size_t o = b0; o < b1; o += 65536) {
           const uint32_t n = (uint32_t)(b1 - o < 65536 ? b1 - o : 65536);
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.l2pf + o), "r"(n) : "memory");
+        }
+        if (p.rpf != nullptr) {
+          for (int c = cid; c < p.rpf_G; c += nct) {
+            const int s0 = (int)((long long)c * p.rpf_U / p.rpf_G);
+            const int s1 = (int)((long long)(c + 1) * p.rpf_U / p.rpf_G);
+            const int k0 = s0 + 6, k1 = min(s1, k0 + 6);
+            if (k1 > k0)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.rpf + (size_t)k0 * 16384),
+                           "r"((uint32_t)(k1 - k0) * 16384u) : "memory");
+          }
         }
       }
       if (*abort_flag) {
@@ -815,7 +828,8 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
                               cudaStream_t stream, const int4* remap, int ncache, int early_kv,
-                              const void* l2pf, size_t l2pf_bytes) {
+                              const void* l2pf, size_t l2pf_bytes, const void* rpf, int rpf_U,
+                              int rpf_G) {
   const int G = Hq / Hkv;
   const int nsplit = (Lmax + split - 1) / split;
   const size_t need = attn_bf16_workspace(B, T, Hq, Hkv, Lmax, split);
@@ -859,6 +873,11 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
   const bool pf_ok = l2pf != nullptr && (reinterpret_cast<uintptr_t>(l2pf) & 15) == 0;
   prm.l2pf = pf_ok ? static_cast<const char*>(l2pf) : nullptr;
   prm.l2pf_bytes = pf_ok ? (l2pf_bytes & ~(size_t)15) : 0;
+  const bool rpf_ok = pf_ok && rpf != nullptr && (reinterpret_cast<uintptr_t>(rpf) & 15) == 0 && rpf_G > 0 &&
+                      rpf_U > 0;
+  prm.rpf = rpf_ok ? static_cast<const char*>(rpf) : nullptr;
+  prm.rpf_U = rpf_ok ? rpf_U : 0;
+  prm.rpf_G = rpf_ok ? rpf_G : 1;
   prm.ws_o = static_cast<float*>(ws);
   const size_t partials = attn_partials_bytes(B, Hkv, nsplit);
   prm.ws_ml = partials ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) +

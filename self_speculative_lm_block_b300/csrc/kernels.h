@@ -37,7 +37,8 @@ ndiff_status launch_attn_bf16(const void* q, const void* k, const void* v, const
                               int B, int T, int Hq, int Hkv, int Lmax, int causal, float scale,
                               int split, void* out, void* ws, size_t ws_bytes,
                               cudaStream_t stream, const int4* remap = nullptr, int ncache = 0,
-                              int early_kv = 0, const void* l2pf = nullptr, size_t l2pf_bytes = 0);
+                              int early_kv = 0, const void* l2pf = nullptr, size_t l2pf_bytes = 0,
+                              const void* rpf = nullptr, int rpf_U = 0, int rpf_G = 0);
 
 // attn_f32.cu
 ndiff_status launch_attn_f32(const float* q, const float* k, const float* v,

@@ -331,11 +331,14 @@ ndiff_status forward(ndiff_model* m, const int32_t* ids, int T, int causal, int 
       } else {
         // one sequence: the QKV merge before it lets the prefix K/V stream early,
         // and the attention CTAs pull the output projection's weights into L2
-        // while HBM would otherwise idle
+        // while HBM would otherwise idle; a block's longer attention also pulls
+        // the gate/up projection's next six k-steps of every run
+        const bool blk_pf = defer && T >= kBlock;
         TRY(launch_attn_bf16(m->qb, ly.kc, ly.vc, m->kv_len, B, T, m->Hq, m->Hkv, m->Lmax, causal,
                              scale, m->attn_split, m->ob, m->aws, m->aws_bytes, s, nullptr, 0,
                              defer ? 1 : 0, defer ? ly.wo : nullptr,
-                             defer ? (size_t)m->d * m->HD * 2 : 0));
+                             defer ? (size_t)m->d * m->HD * 2 : 0, blk_pf ? ly.wgu : nullptr,
+                             m->pl_gu.ntiles * m->pl_gu.nks, m->pl_gu.grid));
       }
       p = gp;
       p.N = m->d;
