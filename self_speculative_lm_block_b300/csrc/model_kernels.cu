@@ -357,9 +357,10 @@ __global__ void __launch_bounds__(256)
 // kernel's QKV epilogue; v rows are dims in order. q goes to q[m][h][128], k
 // and v to the caches at the token's cache row. Positions and cache rows:
 // kv_len[0] + m, or with blk_pos those of the token's 32-row block. Grid
-// (heads, token rows), one warp; lane l on rows 4l .. 4l+3.
+// (heads, token rows / R), R = min(T, 8) warps a CTA, one per token row; lane
+// l on rows 4l .. 4l+3.
 template <int MT>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(256)
     qkv_merge_kernel(const PartialPlan pp, int T, int Hq, int Hkv, int Lmax, const int32_t* kv_len,
                      const int32_t* blk_pos, const float2* __restrict__ rope,
                      __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ kc,
@@ -370,7 +371,9 @@ __global__ void __launch_bounds__(32)
   // its own wait.
   griddep_wait();
   griddep_launch();
-  const int h = blockIdx.x, m = blockIdx.y, lane = threadIdx.x;
+  const int h = blockIdx.x, lane = threadIdx.x & 31;
+  const int m = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (m >= T) return;  // uniform over the warp
   // the partials' loads go out first: they do not wait for the position
   const float4 y = tile_sum4<MT>(pp, h, m, lane * 4);
   const int P = checked_prefix(kv_len[0], Lmax - T, status);
@@ -675,7 +678,11 @@ ndiff_status launch_qkv_merge(const PartialPlan& pp, int T, int Hq, int Hkv, int
                               __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int mt,
                               cudaStream_t s) {
   if (T <= 0) return NDIFF_OK;
-  NDIFF_MT_DISPATCH(mk::qkv_merge_kernel, mt, dim3(Hq + 2 * Hkv, T), dim3(32), pp, T, Hq, Hkv, Lmax,
+  // one warp per (head, token row), up to 8 rows a CTA: a 32-row block is 192
+  // CTAs of 8 warps rather than 1536 of one
+  const int rows = T < 8 ? T : 8;
+  NDIFF_MT_DISPATCH(mk::qkv_merge_kernel, mt, dim3(Hq + 2 * Hkv, (T + rows - 1) / rows), dim3(32 * rows), pp, T,
+                    Hq, Hkv, Lmax,
                     kv_len, blk_pos, rope, q, kc, vc, device_status_word());
   return NDIFF_OK;
 }
