@@ -53,9 +53,9 @@ METRIC = "block-attn HBM GB/s (% of peak); self-spec tokens/s and tokens/forward
 # DRAM bytes (read + write) of one attention launch and its split merge, from
 # ncu captures of the current kernels on these workloads (summary under
 # profiles/); None where no capture exists.
-ATTN_TRAFFIC = {"attn-batched": 1016180992 + 1677312,
-                "attn-long": 539070464 + 514048 + 8535552,
-                "attn-single": 17226240 + 0 + 9068032}
+ATTN_TRAFFIC = {"attn-batched": 1016270592 + 1821696,
+                "attn-long": 539068672 + 389120 + 8535808,
+                "attn-single": 17227008 + 0 + 9068032}
 SPEC_HBM_GBS = 8000.0
 L2_BYTES = 126e6
 

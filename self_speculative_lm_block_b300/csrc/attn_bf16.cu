@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // 64 KB bulk prefetches, an equal slice each.
         const int nct = gridDim.x * gridDim.y * gridDim.z;
         const int cid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-        const size_t per = ((p.l2pf_bytes / nct) + 65535) & ~(size_t)65535;
+        const size_t per = ((p.l2pf_bytes + nct - 1) / nct + 65535) & ~(size_t)65535;
         const size_t b0 = per * cid, b1 = b0 + per < p.l2pf_bytes ? b0 + per : p.l2pf_bytes;
         for (size_t o = b0; o < b1; o += 65536) {
           const uint32_t n = (uint32_t)(b1 - o < 65536 ? b1 - o : 65536);
